@@ -1,0 +1,148 @@
+"""Seeded synthetic inputs for the GEMM workloads.
+
+This module only draws random numbers and rounds them to the element type the
+GPU receives.  It holds none of the GEMM arithmetic, so both the CUDA path and
+the CPU oracle can take their operands from it.
+
+Workloads (the shapes and distributions the pages analyse):
+
+* ``fp32_256``   FP32 SGEMM, M=N=K=256, alpha=1, beta=0, A,B ~ U[-1,1), seed 0.
+* ``fp32_4096``  FP32 SGEMM, M=N=K=4096, alpha=1.5, beta=0.5, A,B,C0 ~ U[-1,1),
+  seed 1 -- the 683 FLOP/byte case of "CUDA 算子工程 ch.10, 朴素 GEMM 与
+  Roofline 分析" section 10.3.1.
+* ``bf16_4096`` / ``bf16_8192``  BF16 GEMM with fp32 accumulation, alpha=1,
+  beta=0, A,B ~ normal(0, 1/sqrt(K)) rounded to bf16, seed 2.
+* ``prefill_<w>``  LLaMA-7B-shaped weight GEMMs at M=2048 tokens (d=4096,
+  FFN 11008, vocab 32000 as in section 10.1 of the same page): X ~ N(0,1),
+  W ~ N(0, 0.02), rounded to bf16, seed 3, alpha=1, beta=0.
+* ``decode_m<M>_<w>``  the same weight shapes with M in {1, 4, 16} tokens,
+  W ~ N(0, 0.02), X ~ N(0, 1), C0 ~ N(0, 1), seed 4, beta=1 (residual add).
+
+Every case draws from its own ``torch.Generator`` seeded with the case's seed,
+in the order A, B, C0, in fp32 on the CPU; bf16 cases are then rounded with
+round-to-nearest-even (``Tensor.to(torch.bfloat16)``).  "normal(0, s)" means
+standard deviation s.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import torch
+
+# LLaMA-7B weight shapes (K, N) for the per-layer GEMMs and the LM head.
+LLAMA7B_WEIGHTS = {
+    "qkv": (4096, 12288),
+    "o": (4096, 4096),
+    "gate": (4096, 11008),
+    "up": (4096, 11008),
+    "down": (11008, 4096),
+    "lm": (4096, 32000),
+}
+DECODE_M = (1, 4, 16)
+PREFILL_M = 2048
+
+
+@dataclasses.dataclass(frozen=True)
+class CaseSpec:
+    name: str
+    M: int
+    N: int
+    K: int
+    alpha: float
+    beta: float
+    in_dtype: str          # "f32" or "bf16"
+    seed: int
+    dist: str              # "uniform", "normal_invsqrtk", "llama"
+    c0: bool               # whether an initial C is drawn
+
+
+@dataclasses.dataclass
+class Case:
+    spec: CaseSpec
+    A: torch.Tensor        # M x K, row-major, CPU, element type the GPU gets
+    B: torch.Tensor        # K x N
+    C0: Optional[torch.Tensor]  # M x N or None (beta == 0)
+
+
+def _specs() -> dict:
+    s = {}
+    s["fp32_256"] = CaseSpec("fp32_256", 256, 256, 256, 1.0, 0.0, "f32", 0, "uniform", False)
+    s["fp32_4096"] = CaseSpec("fp32_4096", 4096, 4096, 4096, 1.5, 0.5, "f32", 1, "uniform", True)
+    for n in (4096, 8192):
+        s[f"bf16_{n}"] = CaseSpec(f"bf16_{n}", n, n, n, 1.0, 0.0, "bf16", 2, "normal_invsqrtk", False)
+    for w, (K, N) in LLAMA7B_WEIGHTS.items():
+        s[f"prefill_{w}"] = CaseSpec(f"prefill_{w}", PREFILL_M, N, K, 1.0, 0.0, "bf16", 3, "llama", False)
+        for m in DECODE_M:
+            s[f"decode_m{m}_{w}"] = CaseSpec(f"decode_m{m}_{w}", m, N, K, 1.0, 1.0, "bf16", 4, "llama", True)
+    return s
+
+
+SPECS = _specs()
+
+
+def spec(name: str) -> CaseSpec:
+    return SPECS[name]
+
+
+def _draw(spec_: CaseSpec, gen: torch.Generator, which: str, rows: int, cols: int) -> torch.Tensor:
+    shape = (rows, cols)
+    if spec_.dist == "uniform":
+        return torch.rand(shape, generator=gen, dtype=torch.float32) * 2.0 - 1.0
+    if spec_.dist == "normal_invsqrtk":
+        return torch.randn(shape, generator=gen, dtype=torch.float32) * (1.0 / math.sqrt(spec_.K))
+    if spec_.dist == "llama":
+        # activations and the initial C are N(0,1); weights N(0, 0.02)
+        std = 0.02 if which == "B" else 1.0
+        return torch.randn(shape, generator=gen, dtype=torch.float32) * std
+    raise ValueError(spec_.dist)
+
+
+def round_to(x: torch.Tensor, in_dtype: str) -> torch.Tensor:
+    """Round fp32 values to the GPU element type (RNE for bf16)."""
+    if in_dtype == "f32":
+        return x.contiguous()
+    if in_dtype == "bf16":
+        return x.to(torch.bfloat16).contiguous()
+    raise ValueError(in_dtype)
+
+
+def make(spec_or_name, M: Optional[int] = None, N: Optional[int] = None,
+         K: Optional[int] = None) -> Case:
+    """Draw the operands of a workload (optionally at a reduced M/N/K).
+
+    The overrides keep the seed and distributions of the named workload, which
+    is how parity tests at small sizes mirror the full-size configuration.
+    """
+    sp = SPECS[spec_or_name] if isinstance(spec_or_name, str) else spec_or_name
+    if M is not None or N is not None or K is not None:
+        sp = dataclasses.replace(sp, M=sp.M if M is None else M,
+                                 N=sp.N if N is None else N,
+                                 K=sp.K if K is None else K)
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(sp.seed)
+    A = round_to(_draw(sp, gen, "A", sp.M, sp.K), sp.in_dtype)
+    B = round_to(_draw(sp, gen, "B", sp.K, sp.N), sp.in_dtype)
+    C0 = None
+    if sp.c0:
+        C0 = _draw(sp, gen, "C", sp.M, sp.N)
+        # the initial C has the element type of the output it is added into
+        C0 = round_to(C0, sp.in_dtype)
+    return Case(sp, A, B, C0)
+
+
+def random_matrix(rows: int, cols: int, seed: int, dtype: str = "f32",
+                  dist: str = "uniform", std: float = 1.0) -> torch.Tensor:
+    """A seeded matrix for edge-case tests (odd shapes, padding, scaling)."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    if dist == "uniform":
+        x = torch.rand((rows, cols), generator=gen, dtype=torch.float32) * 2.0 - 1.0
+    elif dist == "normal":
+        x = torch.randn((rows, cols), generator=gen, dtype=torch.float32) * std
+    elif dist == "int":
+        x = torch.randint(-8, 9, (rows, cols), generator=gen).to(torch.float32)
+    else:
+        raise ValueError(dist)
+    return round_to(x, dtype)
