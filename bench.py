@@ -1,0 +1,445 @@
+#!/usr/bin/env python3
+"""Benchmark of the GEMM hot path on GB300.
+
+One step is one pass over every kernel family of the library, each on its
+headline workload, all inputs resident in HBM:
+
+  bf16   C[4096x4096] = A B, bf16 in/out, fp32 accumulate  (tcgen05 kernel)
+  fp32   C = 1.5 A B + 0.5 C at 4096^3                      (FP32 SIMT kernel)
+  decode C = X W + C, X with M in {1, 4, 16} rows, W the six LLaMA-7B weight
+         shapes (qkv, o, gate, up, down, LM head)            (split-K kernel)
+
+value = FLOPs of the step / device time of the step, in TFLOP/s.  Each part is
+also reported with its own roofline: TFLOP/s against the tensor or FP32 peak
+for the two square GEMMs, HBM GB/s for the decode GEMMs (their arithmetic
+intensity is about M FLOP/byte).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs the same step on its own GPU (replicas, weak
+scaling); time is the max over ranks.  ``--impl reference`` times the CPU
+oracle on a bounded sample of the same step instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s (bf16 TC & fp32) at 4096³, % of roofline; decode GEMM HBM GB/s"
+UNIT = "TFLOP/s"
+WEIGHTS = ("qkv", "o", "gate", "up", "down", "lm")
+DECODE_MS = (1, 4, 16)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "sm_max_mhz": 2070.0}
+
+# DRAM bytes per launch measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum)
+# for each kernel source file, valid only while the file hashes to `sha256`.
+NCU_TRAFFIC = {}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_sha(fname):
+    p = os.path.join(ROOT, "roofline_driven_optimisation_gb300", "csrc", fname)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def traffic_for(fname):
+    t = NCU_TRAFFIC.get(fname)
+    if t and t["sha256"] == kernel_sha(fname):
+        return t["bytes_per_launch"]
+    return None
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML (read-only)
+    every few milliseconds while running."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x2: "applications_clocks_setting"}
+
+    def __init__(self, device_index):
+        self.samples, self.reasons, self.ok = [], set(), False
+        self.max_mhz = None
+        self._stop = threading.Event()
+        try:
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if self.nv.nvmlDeviceGetHandleByIndex_v2(device_index, ctypes.byref(self.h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self.ok = True
+        except OSError:
+            self.ok = False
+
+    def _run(self):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk)) == 0:
+                self.samples.append(clk.value)
+            if self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(rs)) == 0:
+                for bit, name in self.REASONS.items():
+                    if rs.value & bit:
+                        self.reasons.add(name)
+            time.sleep(0.002)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.ok:
+            self._stop.set()
+            self.t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                    "samples": len(self.samples)}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+
+
+# ----------------------------------------------------------------- the step
+def build_step(torch):
+    """Operands of one step, drawn on the CPU by the seeded-input module."""
+    from roofline_driven_optimisation_gb300 import inputs
+    parts = []
+    c = inputs.make("bf16_4096")
+    parts.append(dict(name="bf16_4096", kernel="gemm_bf16_tc.cu", fn="bf16", M=4096, N=4096, K=4096,
+                      alpha=1.0, beta=0.0, A=c.A, B=c.B, C0=None, out=torch.bfloat16,
+                      in_bytes=2, out_bytes=2, bound="tensor"))
+    c = inputs.make("fp32_4096")
+    parts.append(dict(name="fp32_4096", kernel="gemm_f32_simt.cu", fn="f32", M=4096, N=4096, K=4096,
+                      alpha=1.5, beta=0.5, A=c.A, B=c.B, C0=c.C0, out=torch.float32,
+                      in_bytes=4, out_bytes=4, bound="alu"))
+    # one copy of each weight (the M = 16 case's), shared by the three M values;
+    # activations and the residual C come from each (M, weight) case
+    weights = {w: inputs.make(f"decode_m16_{w}").B for w in WEIGHTS}
+    for m in DECODE_MS:
+        for w in WEIGHTS:
+            c = inputs.make(f"decode_m{m}_{w}")
+            parts.append(dict(name=f"decode_m{m}_{w}", kernel="gemm_skinny.cu", fn="bf16", M=m,
+                              N=c.spec.N, K=c.spec.K, alpha=1.0, beta=1.0, A=c.A, B=weights[w],
+                              C0=c.C0, out=torch.bfloat16, in_bytes=2, out_bytes=2, bound="hbm"))
+            del c
+    return parts
+
+
+def launch(g, p, A, B, C, stream):
+    M, N, K = p["M"], p["N"], p["K"]
+    fn = g.gemm_bf16 if p["fn"] == "bf16" else g.gemm_f32
+    fn(M, N, K, p["alpha"], A.data_ptr(), K, B.data_ptr(), N, p["beta"], C.data_ptr(), N, stream)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import roofline_driven_optimisation_gb300 as g
+    from roofline_driven_optimisation_gb300 import roofline as R
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    g.load()
+
+    parts = build_step(torch)
+    for p in parts:
+        p["A_d"] = p["A"].to(dev)
+        p["B_d"] = p["B"].to(dev)
+        p["C_d"] = (p["C0"].to(dev) if p["C0"] is not None
+                    else torch.zeros((p["M"], p["N"]), dtype=p["out"], device=dev))
+    stream = torch.cuda.current_stream(dev)
+    s = stream.cuda_stream
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    def step(evs=None):
+        for i, p in enumerate(parts):
+            if evs is not None:
+                evs[i][0].record(stream)
+            launch(g, p, p["A_d"], p["B_d"], p["C_d"], s)
+            if evs is not None:
+                evs[i][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    status, where = g.device_status(s)
+    if status != 0:
+        raise RuntimeError(f"device status {status} at {where} after warm-up")
+
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in parts] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    with ClockSampler(local) as clocks:
+        t0.record(stream)
+        for k in range(args.steps):
+            step(evs[k])
+        t1.record(stream)
+        barrier()
+    elapsed_ms = t0.elapsed_time(t1)
+    status, where = g.device_status(s)
+    if status != 0:
+        raise RuntimeError(f"device status {status} at {where} in the timed region")
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    # per-part average launch durations, from events on the launching stream
+    pk, src = peaks()
+    hbm = pk["hbm_gbs"] * 1e9
+    bf16_peak = pk["bf16_tflops"] * 1e12
+    sm_max = pk.get("sm_max_mhz", 2070.0)
+    fp32_peak = R.fp32_peak(n_sm, sm_max * 1e6)
+    part_out = {}
+    flops_step = 0
+    bytes_by_kernel, time_by_kernel, flops_by_kernel, launches_by_kernel = {}, {}, {}, {}
+    for i, p in enumerate(parts):
+        ms = sum(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(args.steps)) / args.steps
+        fl = R.gemm_flops(p["M"], p["N"], p["K"])
+        by = R.gemm_bytes(p["M"], p["N"], p["K"], p["in_bytes"], p["out_bytes"], p["beta"] != 0)
+        flops_step += fl
+        kern = p["kernel"]
+        bytes_by_kernel[kern] = bytes_by_kernel.get(kern, 0) + by
+        flops_by_kernel[kern] = flops_by_kernel.get(kern, 0) + fl
+        time_by_kernel[kern] = time_by_kernel.get(kern, 0.0) + ms
+        launches_by_kernel[kern] = launches_by_kernel.get(kern, 0) + 1
+        ent = {"ms": round(ms, 5), "tflops": round(fl / (ms * 1e-3) / 1e12, 2),
+               "gbs": round(by / (ms * 1e-3) / 1e9, 1), "ai": round(fl / by, 2)}
+        if p["bound"] == "hbm":
+            ent["frac_hbm"] = round(by / (ms * 1e-3) / hbm, 4)
+        elif p["bound"] == "tensor":
+            ent["frac_tensor"] = round(fl / (ms * 1e-3) / bf16_peak, 4)
+        else:
+            ent["frac_fp32"] = round(fl / (ms * 1e-3) / fp32_peak, 4)
+        part_out[p["name"]] = ent
+
+    # dominant kernel = largest share of the step's device time
+    dom = max(time_by_kernel, key=time_by_kernel.get)
+    dom_parts = [p for p in parts if p["kernel"] == dom]
+    launches = launches_by_kernel[dom]
+    avg_ms = time_by_kernel[dom] / launches
+    bound = dom_parts[0]["bound"]
+    if bound == "hbm":
+        achieved = bytes_by_kernel[dom] / launches / (avg_ms * 1e-3) / 1e9
+        peak, unit, rb = pk["hbm_gbs"], "GB/s", "hbm"
+    elif bound == "tensor":
+        achieved = flops_by_kernel[dom] / launches / (avg_ms * 1e-3) / 1e12
+        peak, unit, rb = pk["bf16_tflops"], "TFLOP/s", "tensor"
+    else:
+        achieved = flops_by_kernel[dom] / launches / (avg_ms * 1e-3) / 1e12
+        peak, unit, rb = fp32_peak / 1e12, "TFLOP/s", "alu"
+    tr = traffic_for(dom)
+    roofline = {"bound": rb, "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": unit,
+                "frac": round(achieved / peak, 4),
+                "traffic": (tr if tr is None else int(tr)),
+                "kernel": dom, "peak_source": src if rb != "alu" else
+                f"{n_sm} SMs x 128 FP32 lanes x 2 FLOP x {sm_max:.0f} MHz",
+                "algorithmic_bytes_per_launch": int(bytes_by_kernel[dom] / launches),
+                "algorithmic_flops_per_launch": int(flops_by_kernel[dom] / launches)}
+
+    ms_step = elapsed_ms / args.steps
+    value = world * flops_step / (ms_step * 1e-3) / 1e12
+    e2e = run_e2e(args, g, torch, dev, parts, s, world)
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16/f32",
+        "data": "synthetic",
+        "config": {"workload": "bf16 4096^3 + fp32 4096^3 (alpha 1.5, beta 0.5) + decode M{1,4,16} x "
+                               "LLaMA-7B weights (qkv,o,gate,up,down,lm), beta 1",
+                   "parallelism": f"replicas x{world}",
+                   "l2": "no flush: step working set ~0.92 GB > 129 MB L2; each input is touched "
+                         "once per step"},
+        "roofline": roofline,
+        "parts": part_out,
+        "e2e": e2e,
+        "gpu_launches": len(parts) * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0:
+        result["cpu_baseline"] = cpu_baseline(parts, args.cpu_seconds)
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_e2e(args, g, torch, dev, parts, s, world):
+    """Same step through the public API with host buffers: every step copies
+    its inputs host->device from pinned memory and reads its results back."""
+    host = []
+    h2d = d2h = 0
+    for p in parts:
+        hA = p["A"].pin_memory()
+        hB = p["B"].pin_memory()
+        hC0 = p["C0"].pin_memory() if p["C0"] is not None else None
+        hC = torch.empty((p["M"], p["N"]), dtype=p["out"]).pin_memory()
+        host.append((hA, hB, hC0, hC))
+        h2d += hA.numel() * hA.element_size() + hB.numel() * hB.element_size()
+        if hC0 is not None:
+            h2d += hC0.numel() * hC0.element_size()
+        d2h += hC.numel() * hC.element_size()
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        for p, (hA, hB, hC0, hC) in zip(parts, host):
+            p["A_d"].copy_(hA, non_blocking=True)
+            p["B_d"].copy_(hB, non_blocking=True)
+            if hC0 is not None:
+                p["C_d"].copy_(hC0, non_blocking=True)
+            launch(g, p, p["A_d"], p["B_d"], p["C_d"], s)
+            hC.copy_(p["C_d"], non_blocking=True)
+
+    steps = max(1, min(args.steps, 20))
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = t0.elapsed_time(t1) / steps
+    flops = sum(2 * p["M"] * p["N"] * p["K"] for p in parts)
+    return {"value": round(world * flops / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
+            "ms_per_step": round(ms, 4), "steps": steps,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ----------------------------------------------------------------- CPU oracle
+def oracle_sample_step(parts, frac, threads):
+    """One bounded sample of the step on the CPU oracle: the first rows of each
+    square GEMM and the first columns of each decode GEMM. Returns FLOPs."""
+    import oracle
+    flops = 0
+    for p in parts:
+        M, N, K = p["M"], p["N"], p["K"]
+        if p["bound"] == "hbm":
+            n = max(1, int(N * frac))
+            C0 = p["C0"][:, :n] if p["C0"] is not None else None
+            oracle.gemm(p["A"], p["B"][:, :n], p["alpha"], p["beta"], C0, threads)
+            flops += 2 * M * n * K
+        else:
+            r = max(1, int(M * frac))
+            C0 = p["C0"][:r] if p["C0"] is not None else None
+            oracle.gemm(p["A"][:r], p["B"], p["alpha"], p["beta"], C0, threads)
+            flops += 2 * r * N * K
+    return flops
+
+
+def _calibrate(parts, threads, target_s):
+    """Row fraction whose oracle sample takes about target_s seconds."""
+    frac = 1.0 / 512
+    t = time.perf_counter()
+    oracle_sample_step(parts, frac, threads)
+    dt = max(time.perf_counter() - t, 1e-3)
+    return min(1.0, frac * target_s / dt)
+
+
+def cpu_baseline(parts, target_s=15.0):
+    import oracle
+    threads = oracle.default_threads()
+    frac = _calibrate(parts, threads, target_s)
+    t = time.perf_counter()
+    fl = oracle_sample_step(parts, frac, threads)
+    dt = time.perf_counter() - t
+    return {"value": round(fl / dt / 1e12, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"fp64 oracle on the first {frac:.4%} of the rows of the two 4096^3 GEMMs and of "
+                      f"the columns of the 18 decode GEMMs ({fl / 1e9:.1f} GFLOP, {dt:.1f} s)"}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import torch
+    import oracle
+    parts = build_step(torch)
+    threads = oracle.default_threads()
+    budget = float(os.environ.get("BENCH_REFERENCE_SECONDS", "150"))
+    frac = _calibrate(parts, threads, budget / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample_step(parts, frac, threads)
+    t = time.perf_counter()
+    fl = 0
+    for _ in range(args.steps):
+        fl += oracle_sample_step(parts, frac, threads)
+    dt = time.perf_counter() - t
+    value = fl / dt / 1e12
+    sample = (f"each step: fp64 oracle on the first {frac:.4%} of the rows of the two 4096^3 GEMMs "
+              f"and of the columns of the 18 decode GEMMs ({fl / args.steps / 1e9:.2f} GFLOP)")
+    print(json.dumps({
+        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": "bf16 4096^3 + fp32 4096^3 (alpha 1.5, beta 0.5) + decode M{1,4,16} x "
+                               "LLaMA-7B weights (qkv,o,gate,up,down,lm), beta 1",
+                   "parallelism": "CPU oracle, rank 0 only"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

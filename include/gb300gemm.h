@@ -1,0 +1,145 @@
+/*
+ * gb300gemm -- dense GEMM for NVIDIA GB300 (sm_103a), C ABI.
+ *
+ * Every entry point computes
+ *
+ *     C = alpha * A * B + beta * C
+ *
+ * the general matrix multiply of "CUDA 算子工程, ch.10 朴素 GEMM 与 Roofline
+ * 分析", section 10.1 (the GEMM equation), on row-major matrices as indexed by
+ * the naive kernel of section 10.2 (A[row*K + k], B[k*N + col],
+ * C[row*N + col]), with explicit leading dimensions:
+ *
+ *     A is M x K, element (i, k) at A[i*lda + k], lda >= K
+ *     B is K x N, element (k, j) at B[k*ldb + j], ldb >= N
+ *     C is M x N, element (i, j) at C[i*ldc + j], ldc >= N
+ *
+ * Conventions shared by all GEMM entry points
+ *   - All matrix pointers are DEVICE pointers owned by the caller; the library
+ *     never frees or retains them past the call.  A and B are read only.
+ *   - Products are accumulated in fp32; the epilogue alpha*acc + beta*C is
+ *     evaluated in fp32 and rounded once (round-to-nearest-even) to C's type.
+ *   - beta == 0 makes C write-only: the old C is never read, so NaN or Inf
+ *     there does not reach the result.
+ *   - M == 0 or N == 0 is a no-op.  K == 0 gives C = beta*C.
+ *   - The call is asynchronous on `stream` (0 = legacy default stream).  It
+ *     performs no host synchronisation and no device allocation.
+ *   - Fast paths need 16-byte-aligned A and B and lda, ldb whose byte size is
+ *     a multiple of 16; anything else still runs, on a generic GPU kernel.
+ *     There is no CPU fallback.
+ *   - Results of one call are deterministic: the same inputs give the same
+ *     bits on every run (fixed reduction order, including split-K).
+ *   - Calls made concurrently from several host threads are safe.
+ *
+ * Errors: every entry point returns a gemm_status.  On a non-zero return
+ * nothing was launched and gemm_get_last_error() describes the cause.  Errors
+ * found on the device (a bounded wait that ran out) are recorded in a status
+ * word that gemm_device_status() reads.
+ */
+#ifndef GB300GEMM_H
+#define GB300GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+#include <cuda_bf16.h>
+typedef __nv_bfloat16 gemm_bf16_t;
+extern "C" {
+#else
+typedef uint16_t gemm_bf16_t; /* IEEE bfloat16 bit pattern */
+#endif
+
+typedef enum {
+  GEMM_OK = 0,
+  GEMM_ERR_INVALID_ARG = 1,   /* negative size, ld too small, null pointer */
+  GEMM_ERR_MISALIGNED = 2,    /* pointer not aligned to its element size */
+  GEMM_ERR_UNSUPPORTED = 3,   /* size beyond the supported range, no sm_103a device */
+  GEMM_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed (message has its text) */
+  GEMM_ERR_DEVICE_TIMEOUT = 5 /* a kernel's bounded wait ran out (device status only) */
+} gemm_status;
+
+/*
+ * FP32 SGEMM on the CUDA cores ("CUDA 算子工程 ch.10", sections 10.4-10.6:
+ * block tile in shared memory, warp tile, register tile).
+ * A, B, C: fp32.  alpha, beta: fp32.
+ */
+int gemm_f32(int M, int N, int K, float alpha, const float* A, int lda, const float* B, int ldb,
+             float beta, float* C, int ldc, cudaStream_t stream);
+
+/*
+ * BF16 GEMM with fp32 accumulation and bf16 C, on the tensor cores
+ * (tcgen05.mma fed by TMA, "Kernel 性能从何而来", section "优化阶梯").  Small M
+ * (decode-shaped, M <= 16) runs on a memory-bound split-K kernel instead
+ * (same page, section "优化 Memory-Bound Kernel").
+ * A, B, C: bf16.  alpha, beta: fp32.
+ */
+int gemm_bf16(int M, int N, int K, float alpha, const gemm_bf16_t* A, int lda,
+              const gemm_bf16_t* B, int ldb, float beta, gemm_bf16_t* C, int ldc,
+              cudaStream_t stream);
+
+/*
+ * As gemm_bf16, but C is fp32 (read when beta != 0, written always).
+ */
+int gemm_bf16_f32out(int M, int N, int K, float alpha, const gemm_bf16_t* A, int lda,
+                     const gemm_bf16_t* B, int ldb, float beta, float* C, int ldc,
+                     cudaStream_t stream);
+
+/*
+ * Message for the last non-OK return on the calling host thread ("" if none).
+ * The string is owned by the library and valid until the next call on this
+ * thread.
+ */
+const char* gemm_get_last_error(void);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word of the
+ * current device.  Returns GEMM_OK, GEMM_ERR_DEVICE_TIMEOUT (a kernel gave up
+ * a bounded wait and returned early; its C is unspecified), or GEMM_ERR_CUDA
+ * if synchronisation itself failed.  If `where` is not NULL it receives the
+ * kernel-specific location code of the first failure (0 if none).
+ */
+int gemm_device_status(cudaStream_t stream, int* where);
+
+/* Kernel families, for gemm_last_path() and gemm_force_path(). */
+typedef enum {
+  GEMM_PATH_AUTO = 0,     /* shape dispatcher (default) */
+  GEMM_PATH_GENERIC = 1,  /* correctness-first tiled kernel, any alignment */
+  GEMM_PATH_F32_SIMT = 2, /* register-tiled FP32 kernel */
+  GEMM_PATH_BF16_TC = 3,  /* tcgen05/TMEM/TMA warp-specialised kernel */
+  GEMM_PATH_SKINNY = 4    /* decode-shaped split-K kernel (bf16, M <= 16) */
+} gemm_path;
+
+/*
+ * Pin the kernel family for later calls on this host thread (GEMM_PATH_AUTO
+ * restores the dispatcher).  A forced path that cannot run the call (wrong
+ * element type, misalignment, M too large for the skinny kernel) makes that
+ * call return GEMM_ERR_UNSUPPORTED.  For A/B measurements and tests.
+ */
+int gemm_force_path(int path);
+
+/* Kernel family the last successful call on this host thread launched
+ * (GEMM_PATH_AUTO if it launched nothing). */
+int gemm_last_path(void);
+
+/*
+ * Upper bound, in nanoseconds, on any single wait inside a kernel launched
+ * later by this process (default 1e9).  After it a kernel records
+ * GEMM_ERR_DEVICE_TIMEOUT in the status word and returns.  0 restores the
+ * default.
+ */
+int gemm_set_wait_timeout_ns(uint64_t timeout_ns);
+
+/*
+ * Self-test of the bounded-wait mechanism: launches one CTA that waits on a
+ * shared-memory barrier nothing ever arrives at, with the given bound, then
+ * returns.  Afterwards gemm_device_status() reports GEMM_ERR_DEVICE_TIMEOUT.
+ * timeout_ns must be in (0, 1e9].
+ */
+int gemm_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GB300GEMM_H */

@@ -1,1 +1,161 @@
-"""GB300 dense GEMM library (C-ABI) and its Python binding."""
+"""GB300 dense GEMM: Python binding of the C-ABI library ``libgb300gemm.so``.
+
+The binding only marshals arguments (device pointers, sizes, leading
+dimensions, the CUDA stream handle) to the C entry points declared in
+``include/gb300gemm.h``; every step of the computation runs in the library's
+CUDA kernels.  There is no CPU fallback: if the library is missing or cannot
+be loaded, every call raises.
+
+Low-level calls (same names and argument order as the C ABI; pointers and the
+stream are integers):
+
+    gemm_f32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+    gemm_bf16(...), gemm_bf16_f32out(...)
+
+Tensor convenience wrapper (reads pointers, strides and the current stream):
+
+    gemm(A, B, C, alpha=1.0, beta=0.0)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+GEMM_OK = 0
+GEMM_ERR_INVALID_ARG = 1
+GEMM_ERR_MISALIGNED = 2
+GEMM_ERR_UNSUPPORTED = 3
+GEMM_ERR_CUDA = 4
+GEMM_ERR_DEVICE_TIMEOUT = 5
+
+PATH_AUTO, PATH_GENERIC, PATH_F32_SIMT, PATH_BF16_TC, PATH_SKINNY = range(5)
+PATH_NAMES = {PATH_AUTO: "none", PATH_GENERIC: "generic", PATH_F32_SIMT: "f32_simt",
+              PATH_BF16_TC: "bf16_tc", PATH_SKINNY: "skinny"}
+
+# every symbol the public header declares
+EXPORTS = ("gemm_f32", "gemm_bf16", "gemm_bf16_f32out", "gemm_get_last_error",
+           "gemm_device_status", "gemm_force_path", "gemm_last_path",
+           "gemm_set_wait_timeout_ns", "gemm_selftest_wait_timeout")
+
+_lib = None
+_lock = threading.Lock()
+
+
+class GemmError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"gemm error {code}: {message}")
+        self.code = code
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def build(force: bool = False) -> str:
+    return _build.build(force=force)
+
+
+def load(path: str | None = None):
+    """Load the C library (built in-tree by ``build()``) and declare signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or library_path()
+        if not os.path.exists(p):
+            raise RuntimeError(f"CUDA GEMM library not built: {p} (run __graft_entry__.build())")
+        lib = ctypes.CDLL(p)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        for name in ("gemm_f32", "gemm_bf16", "gemm_bf16_f32out"):
+            fn = getattr(lib, name)
+            fn.argtypes = [i, i, i, f, vp, i, vp, i, f, vp, i, vp]
+            fn.restype = i
+        lib.gemm_get_last_error.argtypes = []
+        lib.gemm_get_last_error.restype = ctypes.c_char_p
+        lib.gemm_device_status.argtypes = [vp, ctypes.POINTER(i)]
+        lib.gemm_device_status.restype = i
+        lib.gemm_force_path.argtypes = [i]
+        lib.gemm_force_path.restype = i
+        lib.gemm_last_path.argtypes = []
+        lib.gemm_last_path.restype = i
+        lib.gemm_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+        lib.gemm_set_wait_timeout_ns.restype = i
+        lib.gemm_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+        lib.gemm_selftest_wait_timeout.restype = i
+        _lib = lib
+        return lib
+
+
+def _check(rc: int):
+    if rc != GEMM_OK:
+        msg = _lib.gemm_get_last_error().decode(errors="replace")
+        raise GemmError(rc, msg)
+
+
+def gemm_f32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0):
+    _check(load().gemm_f32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream))
+
+
+def gemm_bf16(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0):
+    _check(load().gemm_bf16(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream))
+
+
+def gemm_bf16_f32out(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0):
+    _check(load().gemm_bf16_f32out(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream))
+
+
+def device_status(stream=0) -> tuple[int, int]:
+    """(status code, location code) of the device status word; clears it."""
+    where = ctypes.c_int(0)
+    rc = load().gemm_device_status(stream, ctypes.byref(where))
+    return rc, where.value
+
+
+def force_path(path: int):
+    _check(load().gemm_force_path(path))
+
+
+def last_path() -> int:
+    return load().gemm_last_path()
+
+
+def set_wait_timeout_ns(ns: int):
+    _check(load().gemm_set_wait_timeout_ns(ns))
+
+
+def selftest_wait_timeout(ns: int, stream=0):
+    _check(load().gemm_selftest_wait_timeout(ns, stream))
+
+
+def _ld(t) -> int:
+    """Leading dimension of a row-major 2-D tensor (unit stride along columns)."""
+    if t.dim() != 2 or (t.stride(1) != 1 and t.shape[1] > 1):
+        raise ValueError("expected a 2-D row-major tensor with unit column stride")
+    return max(int(t.stride(0)), int(t.shape[1]), 1)
+
+
+def gemm(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
+    """C = alpha*A@B + beta*C for CUDA tensors (fp32/fp32/fp32, bf16/bf16/bf16
+    or bf16/bf16/fp32).  Argument marshalling only."""
+    import torch
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K or tuple(C.shape) != (M, N):
+        raise ValueError(f"shape mismatch {tuple(A.shape)} @ {tuple(B.shape)} -> {tuple(C.shape)}")
+    if not (A.is_cuda and B.is_cuda and C.is_cuda):
+        raise ValueError("gemm() takes CUDA tensors")
+    s = stream if stream is not None else torch.cuda.current_stream(A.device).cuda_stream
+    args = (M, N, K, float(alpha), A.data_ptr(), _ld(A), B.data_ptr(), _ld(B), float(beta),
+            C.data_ptr(), _ld(C), s)
+    if A.dtype == torch.float32 and B.dtype == torch.float32 and C.dtype == torch.float32:
+        gemm_f32(*args)
+    elif A.dtype == torch.bfloat16 and B.dtype == torch.bfloat16 and C.dtype == torch.bfloat16:
+        gemm_bf16(*args)
+    elif A.dtype == torch.bfloat16 and B.dtype == torch.bfloat16 and C.dtype == torch.float32:
+        gemm_bf16_f32out(*args)
+    else:
+        raise TypeError(f"unsupported dtypes {A.dtype}, {B.dtype} -> {C.dtype}")
+    return C

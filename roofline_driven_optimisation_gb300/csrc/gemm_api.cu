@@ -1,0 +1,331 @@
+// C ABI of the GEMM library: argument validation, the shape dispatcher, TMA
+// tensor-map encoding, and the device status word.
+//
+// Dispatch (one rule per kernel family):
+//   fp32 in/out, TMA-eligible operands           -> register-tiled FP32 kernel
+//   bf16 in, M <= 16, TMA-eligible operands       -> split-K skinny kernel
+//   bf16 in, M > 16, TMA-eligible operands        -> tcgen05 tensor-core kernel
+//   anything else (K == 0, misaligned operands)   -> generic tiled kernel
+// The rule follows the roofline classification of "Kernel 性能从何而来"
+// ("用 Roofline 指导优化"): a decode-shaped GEMM has an arithmetic intensity
+// of about M FLOP/byte and is bandwidth-bound, a large one is compute-bound.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include "gb300gemm.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace g3 {
+namespace {
+
+// ---------------------------------------------------------------- errors
+thread_local char t_msg[512] = "";
+thread_local int t_forced_path = GEMM_PATH_AUTO;
+thread_local int t_last_path = GEMM_PATH_AUTO;
+std::atomic<uint64_t> g_timeout_ns{1000000000ull};
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_msg, sizeof(t_msg), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+// ---------------------------------------------------------------- devices
+__device__ int g_status_word[2];
+
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+  bool ready = false;
+  bool supported = false;
+  int num_sms = 0;
+  int* status = nullptr;
+};
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_dev_mutex;
+
+int device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(GEMM_ERR_UNSUPPORTED, "device index %d", dev);
+  DeviceInfo& d = g_devices[dev];
+  if (!d.ready) {
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (!d.ready) {
+      int major = 0, minor = 0, sms = 0;
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
+      d.supported = (major == 10 && minor == 3);
+      d.num_sms = sms;
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_status_word);
+      if (e != cudaSuccess)
+        return fail(GEMM_ERR_CUDA, "status word address: %s", cudaGetErrorString(e));
+      d.status = static_cast<int*>(p);
+      d.ready = true;
+    }
+  }
+  if (!d.supported)
+    return fail(GEMM_ERR_UNSUPPORTED, "device %d is not an sm_103 (GB300) GPU", dev);
+  *out = &d;
+  return GEMM_OK;
+}
+
+// ---------------------------------------------------------------- tensor maps
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  });
+  return fn;
+}
+
+struct MapKey {
+  uintptr_t ptr;
+  uint64_t cols, rows, ld_bytes;
+  uint32_t box_cols, box_rows, dtype, swizzle;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && cols == o.cols && rows == o.rows && ld_bytes == o.ld_bytes &&
+           box_cols == o.box_cols && box_rows == o.box_rows && dtype == o.dtype &&
+           swizzle == o.swizzle;
+  }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    uint64_t h = k.ptr * 0x9E3779B97F4A7C15ull;
+    h ^= (k.cols + 0x9E37u) * 0xC2B2AE3D27D4EB4Full + (h << 6) + (h >> 2);
+    h ^= (k.rows + 0x7F4Au) * 0x165667B19E3779F9ull + (h << 6) + (h >> 2);
+    h ^= (k.ld_bytes ^ ((uint64_t)k.box_cols << 32) ^ ((uint64_t)k.box_rows << 48) ^
+          ((uint64_t)k.dtype << 8) ^ k.swizzle) * 0x27D4EB2F165667C5ull;
+    return (size_t)h;
+  }
+};
+thread_local std::unordered_map<MapKey, CUtensorMap, MapKeyHash> t_maps;
+
+// 2-D row-major matrix (rows x cols, leading dimension ld_bytes) as a TMA
+// tensor with box (box_cols x box_rows); elements outside read as zero.
+int make_map(const void* ptr, uint64_t cols, uint64_t rows, uint64_t ld_bytes, uint32_t box_cols,
+             uint32_t box_rows, CUtensorMapDataType dtype, CUtensorMapSwizzle swizzle,
+             const CUtensorMap** out) {
+  MapKey key{reinterpret_cast<uintptr_t>(ptr), cols, rows, ld_bytes, box_cols, box_rows,
+             (uint32_t)dtype, (uint32_t)swizzle};
+  auto it = t_maps.find(key);
+  if (it != t_maps.end()) {
+    *out = &it->second;
+    return GEMM_OK;
+  }
+  EncodeFn fn = encode_fn();
+  if (!fn) return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  if (t_maps.size() > 1024) t_maps.clear();
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {ld_bytes};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(&map, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for %llux%llu ld=%llu", (int)r,
+                (unsigned long long)rows, (unsigned long long)cols, (unsigned long long)ld_bytes);
+  auto ins = t_maps.emplace(key, map);
+  *out = &ins.first->second;
+  return GEMM_OK;
+}
+
+// ---------------------------------------------------------------- dispatch
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int lda, const void* B,
+        int ldb, float beta, void* C, int ldc, cudaStream_t stream) {
+  t_msg[0] = '\0';
+  t_last_path = GEMM_PATH_AUTO;
+  if (M < 0 || N < 0 || K < 0) return fail(GEMM_ERR_INVALID_ARG, "negative size M=%d N=%d K=%d", M, N, K);
+  if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
+    return fail(GEMM_ERR_INVALID_ARG, "leading dimension too small (lda=%d ldb=%d ldc=%d, K=%d N=%d)",
+                lda, ldb, ldc, K, N);
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (C == nullptr) return fail(GEMM_ERR_INVALID_ARG, "C is NULL");
+  if (K > 0 && (A == nullptr || B == nullptr)) return fail(GEMM_ERR_INVALID_ARG, "A or B is NULL");
+  const size_t in_sz = in == Elem::F32 ? 4 : 2, out_sz = out == Elem::F32 ? 4 : 2;
+  if ((reinterpret_cast<uintptr_t>(A) % in_sz) || (reinterpret_cast<uintptr_t>(B) % in_sz) ||
+      (reinterpret_cast<uintptr_t>(C) % out_sz))
+    return fail(GEMM_ERR_MISALIGNED, "a matrix pointer is not aligned to its element size");
+
+  DeviceInfo* dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc != GEMM_OK) return rc;
+
+  GemmArgs a;
+  a.M = M; a.N = N; a.K = K; a.alpha = alpha; a.beta = beta;
+  a.A = A; a.lda = lda; a.B = B; a.ldb = ldb; a.C = C; a.ldc = ldc;
+  a.in = in; a.out = out;
+  a.status = dev->status;
+  a.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+
+  const bool tma_ok = K > 0 && aligned16(A) && aligned16(B) && ((size_t)lda * in_sz) % 16 == 0 &&
+                      ((size_t)ldb * in_sz) % 16 == 0;
+  int path;
+  const int forced = t_forced_path;
+  if (forced == GEMM_PATH_AUTO) {
+    if (!tma_ok) path = GEMM_PATH_GENERIC;
+    else if (in == Elem::F32) path = GEMM_PATH_F32_SIMT;
+    else if (M <= kSkMaxM) path = GEMM_PATH_SKINNY;
+    else path = GEMM_PATH_BF16_TC;
+  } else {
+    path = forced;
+    const bool fits = forced == GEMM_PATH_GENERIC ||
+                      (tma_ok && ((forced == GEMM_PATH_F32_SIMT && in == Elem::F32) ||
+                                  (forced == GEMM_PATH_BF16_TC && in == Elem::BF16) ||
+                                  (forced == GEMM_PATH_SKINNY && in == Elem::BF16 && M <= kSkMaxM)));
+    if (!fits) return fail(GEMM_ERR_UNSUPPORTED, "forced path %d cannot run this call", forced);
+  }
+
+  int err = cudaSuccess;
+  const CUtensorMap *mA = nullptr, *mB = nullptr;
+  switch (path) {
+    case GEMM_PATH_GENERIC:
+      err = launch_generic(a, stream);
+      break;
+    case GEMM_PATH_F32_SIMT:
+      if ((rc = make_map(A, K, M, (uint64_t)lda * 4, kSimtBK, kSimtBM, CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                         CU_TENSOR_MAP_SWIZZLE_64B, &mA)) != GEMM_OK)
+        return rc;
+      if ((rc = make_map(B, N, K, (uint64_t)ldb * 4, kSimtBN, kSimtBK, CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                         CU_TENSOR_MAP_SWIZZLE_NONE, &mB)) != GEMM_OK)
+        return rc;
+      err = launch_f32_simt(a, mA, mB, stream);
+      break;
+    case GEMM_PATH_BF16_TC:
+      if ((rc = make_map(A, K, M, (uint64_t)lda * 2, kTcBK, kTcBM, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         CU_TENSOR_MAP_SWIZZLE_128B, &mA)) != GEMM_OK)
+        return rc;
+      if ((rc = make_map(B, N, K, (uint64_t)ldb * 2, 64, kTcBK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         CU_TENSOR_MAP_SWIZZLE_128B, &mB)) != GEMM_OK)
+        return rc;
+      err = launch_bf16_tc(a, mA, mB, dev->num_sms, stream);
+      break;
+    case GEMM_PATH_SKINNY:
+      if ((rc = make_map(A, K, M, (uint64_t)lda * 2, kSkBK, kSkMaxM, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         CU_TENSOR_MAP_SWIZZLE_128B, &mA)) != GEMM_OK)
+        return rc;
+      if ((rc = make_map(B, N, K, (uint64_t)ldb * 2, 64, kSkBK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         CU_TENSOR_MAP_SWIZZLE_128B, &mB)) != GEMM_OK)
+        return rc;
+      err = launch_skinny(a, mA, mB, dev->num_sms, stream);
+      break;
+    default:
+      return fail(GEMM_ERR_INVALID_ARG, "unknown path %d", path);
+  }
+  if (err != cudaSuccess)
+    return fail(GEMM_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString((cudaError_t)err));
+  t_last_path = path;
+  return GEMM_OK;
+}
+
+__global__ void selftest_wait_kernel(int* status, uint64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // Nothing ever arrives on `bar`: the bounded wait must run out.
+  if (threadIdx.x == 0 && !mbar_wait(smem_u32(&bar), 0, timeout_ns, nullptr))
+    report_status(status, GEMM_ERR_DEVICE_TIMEOUT, kSiteSelftest);
+}
+
+}  // namespace
+}  // namespace g3
+
+using g3::Elem;
+
+extern "C" {
+
+int gemm_f32(int M, int N, int K, float alpha, const float* A, int lda, const float* B, int ldb,
+             float beta, float* C, int ldc, cudaStream_t stream) {
+  return g3::run(Elem::F32, Elem::F32, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+}
+
+int gemm_bf16(int M, int N, int K, float alpha, const gemm_bf16_t* A, int lda, const gemm_bf16_t* B,
+              int ldb, float beta, gemm_bf16_t* C, int ldc, cudaStream_t stream) {
+  return g3::run(Elem::BF16, Elem::BF16, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+}
+
+int gemm_bf16_f32out(int M, int N, int K, float alpha, const gemm_bf16_t* A, int lda,
+                     const gemm_bf16_t* B, int ldb, float beta, float* C, int ldc,
+                     cudaStream_t stream) {
+  return g3::run(Elem::BF16, Elem::F32, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+}
+
+const char* gemm_get_last_error(void) { return g3::t_msg; }
+
+int gemm_device_status(cudaStream_t stream, int* where) {
+  if (where) *where = 0;
+  g3::DeviceInfo* dev = nullptr;
+  int rc = g3::device_info(&dev);
+  if (rc != GEMM_OK) return rc;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return g3::fail(GEMM_ERR_CUDA, "stream sync: %s", cudaGetErrorString(e));
+  int word[2] = {0, 0};
+  e = cudaMemcpy(word, dev->status, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return g3::fail(GEMM_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+  if (word[0] != 0) {
+    const int zero[2] = {0, 0};
+    e = cudaMemcpy(dev->status, zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return g3::fail(GEMM_ERR_CUDA, "status clear: %s", cudaGetErrorString(e));
+  }
+  if (where) *where = word[1];
+  return word[0];
+}
+
+int gemm_force_path(int path) {
+  if (path < GEMM_PATH_AUTO || path > GEMM_PATH_SKINNY)
+    return g3::fail(GEMM_ERR_INVALID_ARG, "unknown path %d", path);
+  g3::t_forced_path = path;
+  return GEMM_OK;
+}
+
+int gemm_last_path(void) { return g3::t_last_path; }
+
+int gemm_set_wait_timeout_ns(uint64_t timeout_ns) {
+  g3::g_timeout_ns.store(timeout_ns == 0 ? 1000000000ull : timeout_ns);
+  return GEMM_OK;
+}
+
+int gemm_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stream) {
+  if (timeout_ns == 0 || timeout_ns > 1000000000ull)
+    return g3::fail(GEMM_ERR_INVALID_ARG, "timeout_ns must be in (0, 1e9]");
+  g3::DeviceInfo* dev = nullptr;
+  int rc = g3::device_info(&dev);
+  if (rc != GEMM_OK) return rc;
+  g3::selftest_wait_kernel<<<1, 32, 0, stream>>>(dev->status, timeout_ns);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return g3::fail(GEMM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+  return GEMM_OK;
+}
+
+}  // extern "C"

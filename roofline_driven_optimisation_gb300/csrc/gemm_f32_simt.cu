@@ -1,0 +1,240 @@
+// FP32 SGEMM on the CUDA cores: C = alpha*A*B + beta*C, row-major fp32.
+//
+// FP32 has no dense tensor-core route, so this path is the three-level tiling
+// of "CUDA 算子工程 ch.10 朴素 GEMM 与 Roofline 分析", section 10.4, done with
+// FFMA instead of MMA:
+//   * block tile 128 x 128 (section 10.4.1: each K column of A and B tile,
+//     256 floats, feeds 16384 FMAs, 64x reuse), K-slices of 16;
+//   * warp tile 64 x 32 (10.4.1: about 21x reuse from shared memory);
+//   * register tile 8 x 8 per thread (10.4.1: every loaded element used 8x;
+//     section 10.6 is the 4 x 4 version of the same idea).
+// The K-slices stream through a 4-stage shared-memory ring filled by TMA
+// ("Kernel 性能从何而来", section "优化阶梯": TMA-backed loads are the first big
+// step), one producer warp issuing copies and eight compute warps consuming
+// them, handed over with mbarriers (same page, "通过重叠执行减少硬件空闲").
+//
+// Shared-memory bank conflicts ("CUDA 算子工程 ch.4 内存层级与代价表", sections
+// 4.3.1-4.3.4): the A tile is stored [m][k] (64 bytes per row) with the TMA
+// 64-byte swizzle, so the eight rows a warp reads with one 128-bit load land
+// on eight disjoint groups of four banks; B is read along n, where a warp
+// needs only 64 contiguous bytes per load.  TMA zero-fills outside the
+// matrix, so ragged M, N, K need no guards in the main loop (the role the
+// bounds checks play in the thread-tile kernel of ch.10, 10.6).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace g3 {
+namespace {
+
+constexpr int BM = kSimtBM, BN = kSimtBN, BK = kSimtBK;
+constexpr int STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * BK * 4;  // 8 KB
+constexpr int B_STAGE_BYTES = BK * BN * 4;  // 8 KB
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int COMPUTE_WARPS = 8;
+constexpr int THREADS = (COMPUTE_WARPS + 1) * 32;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+
+struct SimtParams {
+  GemmArgs a;
+  int tiles_m, tiles_n;
+  int c_vec;  // C pointer 16-byte aligned and ldc % 4 == 0
+};
+
+__device__ __forceinline__ float4 lds128(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    sgemm_tma_kernel(const __grid_constant__ CUtensorMap mapA,
+                     const __grid_constant__ CUtensorMap mapB, const SimtParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - smem_u32(smem_raw));
+  const uint32_t bar_base = base + STAGES * STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + STAGES * STAGE_BYTES);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES);
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+  auto a_tile = [&](int s) { return base + s * STAGE_BYTES; };
+  auto b_tile = [&](int s) { return base + s * STAGE_BYTES + A_STAGE_BYTES; };
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const GemmArgs& a = p.a;
+
+  // Grouped raster over C tiles: 8 row-panels share the B column-panels
+  // that are in flight at the same time.
+  const int tile = blockIdx.x;
+  const int group = 8;
+  const int tiles_in_group = group * p.tiles_n;
+  const int g = tile / tiles_in_group;
+  const int first_m = g * group;
+  const int gsize = min(p.tiles_m - first_m, group);
+  const int tm_idx = first_m + (tile % tiles_in_group) % gsize;
+  const int tn_idx = (tile % tiles_in_group) / gsize;
+  const int m0 = tm_idx * BM, n0 = tn_idx * BN;
+  const int k_tiles = (a.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), COMPUTE_WARPS);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == COMPUTE_WARPS) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&mapA);
+      tma_prefetch_desc(&mapB);
+      int issued_parity[STAGES];
+      for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+      for (int kt = 0; kt < k_tiles; ++kt) {
+        const int s = kt % STAGES;
+        if (kt >= STAGES) {
+          if (!mbar_wait(empty_bar(s), ((kt / STAGES) - 1) & 1, a.timeout_ns, abort_flag)) {
+            if (!*abort_flag) report_status(a.status, 5, kSiteSimtProducer);
+            *abort_flag = 1;
+            break;
+          }
+        }
+        mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
+        tma_load_2d(a_tile(s), &mapA, full_bar(s), kt * BK, m0);
+        tma_load_2d(b_tile(s), &mapB, full_bar(s), n0, kt * BK);
+        issued_parity[s] = (kt / STAGES) & 1;
+      }
+      if (*abort_flag) {
+        // Let every copy already issued land before shared memory is released.
+        for (int s = 0; s < STAGES; ++s)
+          if (issued_parity[s] >= 0 &&
+              !mbar_wait(full_bar(s), issued_parity[s], a.timeout_ns, nullptr))
+            report_status(a.status, 5, kSiteSimtDrain);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ compute
+    const int wm = warp / 4, wn = warp % 4;
+    const int tm = lane % 8, tn = lane / 8;
+    const int sw = (tm >> 1) & 3;                // 64-byte swizzle phase of my rows
+    const uint32_t a_row_off = (uint32_t)(wm * 64 + tm) * 64u;
+    const uint32_t b_col_off = (uint32_t)(wn * 32 + tn * 4) * 4u;
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+    bool ok = true;
+    for (int kt = 0; kt < k_tiles; ++kt) {
+      const int s = kt % STAGES;
+      if (!mbar_wait(full_bar(s), (kt / STAGES) & 1, a.timeout_ns, abort_flag)) {
+        if (!*abort_flag) report_status(a.status, 5, kSiteSimtConsumer);
+        *abort_flag = 1;
+        ok = false;
+        break;
+      }
+      const uint32_t at = a_tile(s) + a_row_off;
+      const uint32_t bt = b_tile(s) + b_col_off;
+#pragma unroll
+      for (int kq = 0; kq < BK / 4; ++kq) {
+        float4 av[8];
+        const uint32_t chunk = (uint32_t)((kq ^ sw) * 16);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) av[i] = lds128(at + i * 8 * 64 + chunk);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t brow = bt + (uint32_t)(kq * 4 + kk) * (BN * 4);
+          const float4 b0 = lds128(brow);
+          const float4 b1 = lds128(brow + 64);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float ai = kk == 0 ? av[i].x : kk == 1 ? av[i].y : kk == 2 ? av[i].z : av[i].w;
+            acc[i][0] = fmaf(ai, b0.x, acc[i][0]);
+            acc[i][1] = fmaf(ai, b0.y, acc[i][1]);
+            acc[i][2] = fmaf(ai, b0.z, acc[i][2]);
+            acc[i][3] = fmaf(ai, b0.w, acc[i][3]);
+            acc[i][4] = fmaf(ai, b1.x, acc[i][4]);
+            acc[i][5] = fmaf(ai, b1.y, acc[i][5]);
+            acc[i][6] = fmaf(ai, b1.z, acc[i][6]);
+            acc[i][7] = fmaf(ai, b1.w, acc[i][7]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar(s));
+    }
+
+    if (ok) {
+      // ---------------------------------------------------------- epilogue
+      float* C = static_cast<float*>(a.C);
+      const bool beta_nz = a.beta != 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const long long m = (long long)m0 + wm * 64 + i * 8 + tm;
+        if (m >= a.M) continue;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const long long n = (long long)n0 + wn * 32 + h * 16 + tn * 4;
+          float* cp = C + m * a.ldc + n;
+          float v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) v[j] = a.alpha * acc[i][h * 4 + j];
+          if (p.c_vec && n + 3 < a.N) {
+            if (beta_nz) {
+              const float4 c = *reinterpret_cast<const float4*>(cp);
+              v[0] = fmaf(a.beta, c.x, v[0]);
+              v[1] = fmaf(a.beta, c.y, v[1]);
+              v[2] = fmaf(a.beta, c.z, v[2]);
+              v[3] = fmaf(a.beta, c.w, v[3]);
+            }
+            *reinterpret_cast<float4*>(cp) = make_float4(v[0], v[1], v[2], v[3]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              if (n + j < a.N) {
+                float r = v[j];
+                if (beta_nz) r = fmaf(a.beta, cp[j], r);
+                cp[j] = r;
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+}
+
+}  // namespace
+
+int launch_f32_simt(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
+                    cudaStream_t s) {
+  static bool attr_done = false;  // idempotent; a race only repeats the call
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(sgemm_tma_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  SimtParams p;
+  p.a = a;
+  p.tiles_m = (a.M + BM - 1) / BM;
+  p.tiles_n = (a.N + BN - 1) / BN;
+  p.c_vec = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && (a.ldc % 4) == 0) ? 1 : 0;
+  const long long tiles = (long long)p.tiles_m * p.tiles_n;
+  if (tiles <= 0) return cudaSuccess;
+  sgemm_tma_kernel<<<(unsigned)tiles, THREADS, SMEM_BYTES, s>>>(*mapA, *mapB, p);
+  return cudaGetLastError();
+}
+
+}  // namespace g3

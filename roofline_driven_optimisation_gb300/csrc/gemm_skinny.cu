@@ -1,0 +1,306 @@
+// Decode-shaped GEMM (M <= 16 rows of activations against a K x N weight):
+// C = alpha*A*B + beta*C with bf16 A (M x K), bf16 B (K x N), fp32
+// accumulation, bf16 or fp32 C.
+//
+// With M this small the arithmetic intensity is about M FLOP per byte of B,
+// far left of the ridge point, so the kernel is judged by HBM bandwidth
+// ("CUDA 算子工程 ch.4 内存层级与代价表", 4.6: small-batch GEMM is
+// bandwidth-bound; "Kernel 性能从何而来", section "优化 Memory-Bound Kernel":
+// move every byte once, use TMA for regular tiles, keep enough requests in
+// flight).  Design:
+//   * each B element is read from HBM exactly once, by TMA, into a 6-stage
+//     shared-memory ring (16 KB of B per stage), with an evict-first L2 hint;
+//   * the math runs on the tensor cores with the operands swapped,
+//     D^T = B^T A^T: the 128-column slab of B is the MMA's M = 128 operand
+//     (N-major in shared memory) and the <= 16 activation rows are the
+//     MMA's N = 16 operand (K-major), so no shuffle of B is needed and the
+//     tensor pipe has far more throughput than the stream needs;
+//   * K is split over the CTAs of a thread-block cluster (split S <= 8);
+//     each CTA leaves its 128 x 16 fp32 partial in its own shared memory and
+//     the partials are summed across the cluster through distributed shared
+//     memory in rank order 0..S-1 -- a fixed order, so results are
+//     bit-reproducible, and no global workspace is used;
+//   * the beta*C residual and the conversion are fused into that reduction
+//     (same page, section "优化 Memory-Bound Kernel": fuse the elementwise
+//     epilogue instead of a second pass over C).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace g3 {
+namespace {
+
+constexpr int BN = kSkBN;    // B columns per CTA (MMA M)
+constexpr int BK = kSkBK;    // K per stage
+constexpr int MN = kSkMaxM;  // MMA N: activation rows, zero-padded by TMA
+constexpr int STAGES = 6;
+constexpr int UMMA_K = 16;
+constexpr int B_BOX_BYTES = 64 * BK * 2;                 // 8 KB: 64 columns x 64 k
+constexpr int B_STAGE_BYTES = BN * BK * 2;               // 16 KB
+constexpr int A_STAGE_BYTES = MN * BK * 2;               // 2 KB
+constexpr int STAGE_BYTES = B_STAGE_BYTES + A_STAGE_BYTES;
+constexpr int THREADS = 128;
+constexpr int TMEM_COLS = 32;
+constexpr int PARTIAL_BYTES = MN * BN * 4;               // 8 KB, aliases stage 0 after the main loop
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 256 + 1024;
+constexpr int MAX_SPLIT = 8;
+static_assert(PARTIAL_BYTES <= STAGE_BYTES, "partial tile aliases one stage");
+static_assert(STAGE_BYTES % 1024 == 0, "stages stay 1024-byte aligned");
+
+struct SkinnyParams {
+  GemmArgs a;
+  int split;       // CTAs per cluster along K
+  int k_tiles;     // total K stages
+  int c_vec;       // unused by the scalar stores; kept for symmetry
+};
+
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(THREADS, 2)
+    gemm_skinny_kernel(const __grid_constant__ CUtensorMap mapA,
+                       const __grid_constant__ CUtensorMap mapB, const SkinnyParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t bar_base = base + STAGES * STAGE_BYTES;
+  uint8_t* bar_ptr = base_ptr + STAGES * STAGE_BYTES;
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+  const uint32_t tfull_bar = bar_base + 8u * (2 * STAGES);
+  const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_ptr + 8 * (2 * STAGES + 2));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_ptr + 8 * (2 * STAGES + 2) + 8);
+  auto b_tile = [&](int s) { return base + s * STAGE_BYTES; };
+  auto a_tile = [&](int s) { return base + s * STAGE_BYTES + B_STAGE_BYTES; };
+  float* partial = reinterpret_cast<float*>(base_ptr);  // [MN][BN], valid after the main loop
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const GemmArgs& a = p.a;
+  const int rank = (int)cluster_ctarank();          // position along K inside the cluster
+  const int n0 = blockIdx.y * BN;
+  const int kt_begin = (int)((long long)p.k_tiles * rank / p.split);
+  const int kt_end = (int)((long long)p.k_tiles * (rank + 1) / p.split);
+  const int my_kt = kt_end - kt_begin;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(tfull_bar, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (elect_one_sync() && my_kt > 0) {
+      tma_prefetch_desc(&mapA);
+      tma_prefetch_desc(&mapB);
+      const uint64_t stream_policy = l2_policy_evict_first();
+      int issued_parity[STAGES];
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int kt = kt_begin; kt < kt_end; ++kt) {
+        if (!mbar_wait(empty_bar(stage), phase ^ 1u, a.timeout_ns, abort_flag)) {
+          if (!*abort_flag) report_status(a.status, 5, kSiteSkinnyProducer);
+          *abort_flag = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
+#pragma unroll
+        for (int j = 0; j < BN / 64; ++j)
+          tma_load_2d_hint(b_tile(stage) + j * B_BOX_BYTES, &mapB, full_bar(stage), n0 + j * 64,
+                           kt * BK, stream_policy);
+        tma_load_2d(a_tile(stage), &mapA, full_bar(stage), kt * BK, 0);
+        issued_parity[stage] = (int)phase;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (*abort_flag) {
+        for (int s = 0; s < STAGES; ++s)
+          if (issued_parity[s] >= 0 &&
+              !mbar_wait(full_bar(s), (uint32_t)issued_parity[s], a.timeout_ns, nullptr))
+            report_status(a.status, 5, kSiteSkinnyDrain);
+      }
+    }
+  } else if (warp == 1) {
+    if (elect_one_sync() && my_kt > 0) {
+      // D^T (128 x 16) += B^T (128 x 16, N-major) * A^T (16 x 16, K-major)
+      constexpr uint32_t idesc = idesc_bf16_f32(BN, MN, /*A MN-major*/ 1, /*B K-major*/ 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int kt = 0; kt < my_kt; ++kt) {
+        if (!mbar_wait(full_bar(stage), phase, a.timeout_ns, abort_flag)) {
+          if (!*abort_flag) report_status(a.status, 5, kSiteSkinnyMma);
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+          const uint64_t bdesc = smem_desc_sw128(b_tile(stage) + kk * UMMA_K * 128, B_BOX_BYTES, 1024);
+          const uint64_t adesc = smem_desc_sw128(a_tile(stage) + kk * UMMA_K * 2, 16, 1024);
+          tc_mma_f16(tmem_base, bdesc, adesc, idesc, (kt | kk) != 0 ? 1u : 0u);
+        }
+        tc_commit(empty_bar(stage));
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (ok) {
+        tc_commit(tfull_bar);
+      } else {
+        tc_commit(drain_bar);
+        if (!mbar_wait(drain_bar, 0, a.timeout_ns, nullptr)) report_status(a.status, 5, kSiteSkinnyDrain);
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- partials
+  // All four warps: TMEM lanes [32w, 32w+32) hold columns n0+32w+lane of
+  // D^T, one fp32 per activation row.
+  __syncwarp();
+  bool have = false;
+  if (my_kt > 0) {
+    have = mbar_wait(tfull_bar, 0, a.timeout_ns, abort_flag);
+    if (!have && !*abort_flag) {
+      report_status(a.status, 5, kSiteSkinnyEpilogue);
+      *abort_flag = 1;
+    }
+  }
+  __syncwarp();
+  tc_fence_after();
+  __syncthreads();  // every role has left the main loop: stage 0 may now be reused
+  uint32_t r[16];
+  if (my_kt > 0 && !*abort_flag) {
+    tmem_ld_32x32b_x16(tmem_base + ((uint32_t)(warp * 32) << 16), r);
+    tc_wait_ld();
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) r[j] = 0u;
+  }
+  const int n_local = warp * 32 + lane;
+#pragma unroll
+  for (int m = 0; m < MN; ++m) partial[m * BN + n_local] = __uint_as_float(r[m]);
+
+  cluster_sync();  // partials of every rank are visible cluster-wide
+
+  // ---------------------------------------------------------------- reduce
+  const int cols = BN / p.split;  // columns this rank finishes
+  const int items = a.M * cols;
+  const uint32_t partial_addr = smem_u32(partial);
+  for (int it = threadIdx.x; it < items; it += THREADS) {
+    const int m = it / cols;
+    const int nl = rank * cols + it % cols;
+    const long long n = (long long)n0 + nl;
+    float sum = 0.f;
+    for (int q = 0; q < p.split; ++q)
+      sum += ld_dsmem_f32(map_to_rank(partial_addr + (uint32_t)(m * BN + nl) * 4u, (uint32_t)q));
+    if (n < a.N) {
+      float v = a.alpha * sum;
+      if (OUT_BF16) {
+        __nv_bfloat16* C = static_cast<__nv_bfloat16*>(a.C) + (long long)m * a.ldc + n;
+        if (a.beta != 0.f) v = fmaf(a.beta, __bfloat162float(*C), v);
+        *C = __float2bfloat16_rn(v);
+      } else {
+        float* C = static_cast<float*>(a.C) + (long long)m * a.ldc + n;
+        if (a.beta != 0.f) v = fmaf(a.beta, *C, v);
+        *C = v;
+      }
+    }
+  }
+
+  cluster_sync();  // no rank leaves while others may still read its partial
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+int choose_split(int tiles_n, int k_tiles, int num_sms) {
+  static int forced = -1;
+  if (forced < 0) {
+    const char* e = std::getenv("GB300GEMM_SKINNY_SPLIT");
+    forced = e ? std::atoi(e) : 0;
+  }
+  int s = 1;
+  if (forced == 1 || forced == 2 || forced == 4 || forced == 8) {
+    s = forced;
+  } else {
+    const int target = 2 * num_sms;  // two CTAs fit on an SM
+    while (s * 2 <= MAX_SPLIT && tiles_n * s * 2 <= target) s *= 2;
+  }
+  while (s > 1 && s > k_tiles) s /= 2;
+  return s;
+}
+
+template <bool OUT_BF16>
+int launch_impl(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB, int num_sms,
+                cudaStream_t s) {
+  static int attr_done_mask = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 31 && !(attr_done_mask & (1 << dev))) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_skinny_kernel<OUT_BF16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done_mask |= (1 << dev);
+  }
+  SkinnyParams p;
+  p.a = a;
+  p.k_tiles = (a.K + BK - 1) / BK;
+  const int tiles_n = (a.N + BN - 1) / BN;
+  if (tiles_n <= 0 || a.M <= 0) return cudaSuccess;
+  if (tiles_n > 65535) return cudaErrorInvalidConfiguration;
+  p.split = choose_split(tiles_n, p.k_tiles, num_sms);
+  p.c_vec = 0;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.split, (unsigned)tiles_n, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)p.split;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<OUT_BF16>, *mapA, *mapB, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int launch_skinny(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB, int num_sms,
+                  cudaStream_t s) {
+  if (a.out == Elem::BF16) return launch_impl<true>(a, mapA, mapB, num_sms, s);
+  return launch_impl<false>(a, mapA, mapB, num_sms, s);
+}
+
+}  // namespace g3

@@ -1,0 +1,66 @@
+// Interface between the C-ABI/dispatcher (gemm_api.cu) and the kernel
+// translation units.  Not installed; not part of the public ABI.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace g3 {
+
+enum class Elem : int { F32 = 0, BF16 = 1 };
+
+// One GEMM call after validation: C = alpha*A*B + beta*C, row-major.
+struct GemmArgs {
+  int M, N, K;
+  float alpha, beta;
+  const void* A;
+  long long lda;
+  const void* B;
+  long long ldb;
+  void* C;
+  long long ldc;
+  Elem in, out;
+  int* status;          // device status word (2 ints)
+  uint64_t timeout_ns;  // bound on any single wait inside a kernel
+};
+
+// Location codes recorded with a device timeout (status[1]).
+enum WaitSite : int {
+  kSiteSelftest = 1,
+  kSiteTcProducer = 10,
+  kSiteTcMma = 11,
+  kSiteTcEpilogue = 12,
+  kSiteTcDrain = 13,
+  kSiteSimtProducer = 20,
+  kSiteSimtConsumer = 21,
+  kSiteSimtDrain = 22,
+  kSiteSkinnyProducer = 30,
+  kSiteSkinnyMma = 31,
+  kSiteSkinnyEpilogue = 32,
+  kSiteSkinnyDrain = 33,
+};
+
+// Each launcher returns a cudaError_t (as int) from the launch.
+int launch_generic(const GemmArgs& a, cudaStream_t s);
+
+// FP32 SIMT kernel: TMA tiles of A (16 k x 128 m, 64-byte swizzle) and
+// B (128 n x 16 k).
+int launch_f32_simt(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
+                    cudaStream_t s);
+constexpr int kSimtBM = 128, kSimtBN = 128, kSimtBK = 16;
+
+// BF16 tcgen05 kernel: TMA tiles of A (64 k x 128 m) and B (64 n x 64 k),
+// 128-byte swizzle.
+int launch_bf16_tc(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
+                   int num_sms, cudaStream_t s);
+constexpr int kTcBM = 128, kTcBN = 256, kTcBK = 64;
+
+// Skinny (M <= 16) split-K kernel: TMA tiles of B (64 n x 64 k) and A
+// (64 k x 16 rows), 128-byte swizzle.
+int launch_skinny(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
+                  int num_sms, cudaStream_t s);
+constexpr int kSkMaxM = 16, kSkBN = 128, kSkBK = 64;
+
+int launch_selftest_wait(int* status, uint64_t timeout_ns, cudaStream_t s);
+
+}  // namespace g3

@@ -1,0 +1,259 @@
+"""GPU parity: every kernel family against the CPU oracle, through the C ABI.
+
+Sizes the oracle finishes in seconds still span several tiles and a ragged
+tail; full-size workloads are checked on sampled rows and columns.  Scores are
+the normwise error max|C_gpu - C_ref| / max(sum_k |A||B|) with the bounds
+1e-5 (fp32 path), 4e-3 (bf16 inputs, bf16 C), 1e-5 (bf16 inputs, fp32 C).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import roofline_driven_optimisation_gb300 as g
+from roofline_driven_optimisation_gb300 import inputs
+from gpu_util import check, run_abi, sampled_check
+
+pytestmark = pytest.mark.gpu
+
+F32, BF16 = torch.float32, torch.bfloat16
+
+
+def expected_path(M, N, K, in_kind):
+    """Kernel family the dispatcher must pick for packed row-major operands:
+    TMA needs leading dimensions whose byte size is a multiple of 16."""
+    per16 = 4 if in_kind == "f32" else 8
+    if K == 0 or K % per16 or N % per16:
+        return g.PATH_GENERIC
+    if in_kind == "f32":
+        return g.PATH_F32_SIMT
+    return g.PATH_SKINNY if M <= 16 else g.PATH_BF16_TC
+
+
+# ------------------------------------------------------------------ fp32 path
+def test_fp32_256_full(cuda_lib):
+    c = inputs.make("fp32_256")
+    err, path = check(c.A, c.B, None, 1.0, 0.0, F32)
+    assert path == g.PATH_F32_SIMT
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (7, 9, 5), (129, 257, 33), (129, 260, 36),
+                                   (300, 200, 1000), (513, 388, 96), (64, 4100, 20), (1, 132, 4)])
+def test_fp32_ragged(cuda_lib, M, N, K):
+    c = inputs.make("fp32_4096", M=M, N=N, K=K)
+    err, path = check(c.A, c.B, c.C0, 1.5, 0.5, F32)
+    assert path == expected_path(M, N, K, "f32")
+
+
+@pytest.mark.parametrize("alpha,beta", [(0.0, 0.0), (1.0, 0.0), (-1.0, 0.5), (1.5, 1.0), (1.0, 0.5)])
+def test_fp32_alpha_beta_grid(cuda_lib, alpha, beta):
+    c = inputs.make("fp32_4096", M=200, N=160, K=64)
+    check(c.A, c.B, c.C0, alpha, beta, F32)
+
+
+def test_fp32_beta_zero_ignores_nan_c(cuda_lib):
+    c = inputs.make("fp32_256", M=130, N=140, K=40)
+    C, _, _ = run_abi(c.A, c.B, None, 1.0, 0.0, F32, c_fill=float("nan"))
+    assert torch.isfinite(C).all()
+
+
+def test_fp32_padded_leading_dims(cuda_lib):
+    c = inputs.make("fp32_4096", M=150, N=260, K=72)
+    err, path = check(c.A, c.B, c.C0, 1.5, 0.5, F32, pad=(4, 8, 12))
+    assert path == g.PATH_F32_SIMT
+
+
+def test_fp32_misaligned_runs_generic(cuda_lib):
+    c = inputs.make("fp32_4096", M=70, N=92, K=52)
+    err, path = check(c.A, c.B, c.C0, 1.5, 0.5, F32)
+    assert path == g.PATH_F32_SIMT
+    err, path = check(c.A, c.B, c.C0, 1.5, 0.5, F32, offset=(1, 0, 0))
+    assert path == g.PATH_GENERIC
+    err, path = check(c.A, c.B, c.C0, 1.5, 0.5, F32, pad=(1, 0, 0))   # lda*4 not a multiple of 16
+    assert path == g.PATH_GENERIC
+
+
+def test_fp32_unaligned_c_uses_scalar_epilogue(cuda_lib):
+    c = inputs.make("fp32_4096", M=140, N=132, K=40)
+    err, path = check(c.A, c.B, c.C0, 1.5, 0.5, F32, offset=(0, 0, 1), pad=(0, 0, 3))
+    assert path == g.PATH_F32_SIMT
+
+
+def test_fp32_k_zero(cuda_lib):
+    c = inputs.make("fp32_4096", M=33, N=45, K=1)
+    A = c.A[:, :0].contiguous()
+    B = c.B[:0, :].contiguous()
+    C, _, path = run_abi(A, B, c.C0, 1.5, 0.5, F32)
+    assert path == g.PATH_GENERIC
+    assert torch.equal(C, 0.5 * c.C0)
+
+
+def test_fp32_forced_generic_matches_oracle(cuda_lib):
+    c = inputs.make("fp32_4096", M=190, N=170, K=150)
+    err, path = check(c.A, c.B, c.C0, 1.5, 0.5, F32, path=g.PATH_GENERIC)
+    assert path == g.PATH_GENERIC
+
+
+def test_fp32_4096_full_size_sampled(cuda_lib):
+    c = inputs.make("fp32_4096")
+    A, B, C = c.A.cuda(), c.B.cuda(), c.C0.cuda()
+    g.gemm(A, B, C, 1.5, 0.5)
+    torch.cuda.synchronize()
+    assert g.last_path() == g.PATH_F32_SIMT
+    gen = np.random.default_rng(11)
+    rows = np.sort(gen.choice(4096, 24, replace=False))
+    cols = np.sort(gen.choice(4096, 24, replace=False))
+    sampled_check(A, B, C, c.A, c.B, c.C0, 1.5, 0.5, oracle.TOL_F32, rows, cols)
+
+
+# ------------------------------------------------------------------ bf16 tensor-core path
+@pytest.mark.parametrize("out", [BF16, F32])
+@pytest.mark.parametrize("M,N,K", [(17, 8, 64), (128, 256, 64), (256, 512, 320), (300, 520, 200),
+                                   (129, 296, 1000), (640, 264, 72), (1000, 1000, 1000),
+                                   (33, 300, 100), (260, 136, 8)])
+def test_bf16_tc_ragged(cuda_lib, M, N, K, out):
+    c = inputs.make("bf16_4096", M=M, N=N, K=K)
+    err, path = check(c.A, c.B, None, 1.0, 0.0, out)
+    assert path == expected_path(M, N, K, "bf16")
+
+
+@pytest.mark.parametrize("out", [BF16, F32])
+@pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (0.0, 0.5), (-1.0, 1.0), (1.5, 0.5)])
+def test_bf16_tc_alpha_beta(cuda_lib, out, alpha, beta):
+    c = inputs.make("decode_m16_o", M=200, N=384, K=256)   # normal C0 for the beta term
+    err, path = check(c.A, c.B, c.C0, alpha, beta, out)
+    assert path == g.PATH_BF16_TC
+
+
+def test_bf16_tc_padded_and_unaligned_c(cuda_lib):
+    c = inputs.make("bf16_4096", M=260, N=272, K=136)
+    check(c.A, c.B, None, 1.0, 0.0, BF16, pad=(8, 16, 3))
+    err, path = check(c.A, c.B, None, 1.0, 0.0, BF16, offset=(0, 0, 1))
+    assert path == g.PATH_BF16_TC
+    err, path = check(c.A, c.B, None, 1.0, 0.0, F32, offset=(0, 0, 1), pad=(0, 0, 1))
+    assert path == g.PATH_BF16_TC
+
+
+def test_bf16_misaligned_runs_generic(cuda_lib):
+    c = inputs.make("bf16_4096", M=100, N=120, K=88)
+    for kw in (dict(offset=(1, 0, 0)), dict(offset=(0, 3, 0)), dict(pad=(2, 0, 0)), dict(pad=(0, 1, 0))):
+        err, path = check(c.A, c.B, None, 1.0, 0.0, BF16, **kw)
+        assert path == g.PATH_GENERIC, kw
+    err, path = check(c.A, c.B, None, 1.0, 0.0, F32, offset=(1, 0, 0))
+    assert path == g.PATH_GENERIC
+
+
+def test_bf16_deterministic(cuda_lib):
+    c = inputs.make("bf16_4096", M=512, N=768, K=640)
+    outs = [run_abi(c.A, c.B, None, 1.0, 0.0, F32)[0] for _ in range(2)]
+    assert torch.equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("n", [4096, 8192])
+@pytest.mark.parametrize("out", [BF16, F32])
+def test_bf16_square_full_size_sampled(cuda_lib, n, out):
+    c = inputs.make(f"bf16_{n}")
+    A, B = c.A.cuda(), c.B.cuda()
+    C = torch.full((n, n), float("nan"), dtype=out, device="cuda")
+    g.gemm(A, B, C, 1.0, 0.0)
+    torch.cuda.synchronize()
+    assert g.last_path() == g.PATH_BF16_TC
+    gen = np.random.default_rng(n)
+    rows = np.sort(gen.choice(n, 16, replace=False))
+    cols = np.sort(gen.choice(n, 16, replace=False))
+    tol = oracle.TOL_BF16_OUT if out == BF16 else oracle.TOL_BF16_F32OUT
+    sampled_check(A, B, C, c.A, c.B, None, 1.0, 0.0, tol, rows, cols)
+
+
+@pytest.mark.parametrize("w", ["qkv", "o", "gate", "down", "lm"])
+def test_prefill_full_size_sampled(cuda_lib, w):
+    c = inputs.make(f"prefill_{w}")
+    A, B = c.A.cuda(), c.B.cuda()
+    C = torch.empty((c.spec.M, c.spec.N), dtype=BF16, device="cuda")
+    g.gemm(A, B, C, 1.0, 0.0)
+    torch.cuda.synchronize()
+    gen = np.random.default_rng(3)
+    rows = np.sort(gen.choice(c.spec.M, 8, replace=False))
+    cols = np.sort(gen.choice(c.spec.N, 8, replace=False))
+    sampled_check(A, B, C, c.A, c.B, None, 1.0, 0.0, oracle.TOL_BF16_OUT, rows, cols)
+
+
+# ------------------------------------------------------------------ skinny split-K path
+@pytest.mark.parametrize("m", [1, 4, 16])
+@pytest.mark.parametrize("N,K", [(384, 512), (4104, 1000), (200, 64), (96, 11008), (1000, 72), (8, 8)])
+def test_skinny_ragged(cuda_lib, m, N, K):
+    c = inputs.make(f"decode_m{m}_o", M=m, N=N, K=K)
+    for out in (BF16, F32):
+        err, path = check(c.A, c.B, c.C0, 1.0, 1.0, out)
+        assert path == g.PATH_SKINNY
+
+
+@pytest.mark.parametrize("m", [2, 3, 5, 9, 15])
+def test_skinny_odd_m(cuda_lib, m):
+    c = inputs.make("decode_m16_o", M=m, N=520, K=392)
+    err, path = check(c.A, c.B, c.C0, 1.5, 0.5, BF16, pad=(8, 8, 5))
+    assert path == g.PATH_SKINNY
+
+
+@pytest.mark.parametrize("m", [1, 4, 16])
+@pytest.mark.parametrize("w", ["qkv", "o", "gate", "down", "lm"])
+def test_decode_full_size(cuda_lib, m, w):
+    # decode GEMMs are small enough for the oracle to check every element
+    c = inputs.make(f"decode_m{m}_{w}")
+    err, path = check(c.A, c.B, c.C0, 1.0, 1.0, BF16)
+    assert path == g.PATH_SKINNY
+
+
+def test_skinny_deterministic_and_split_consistent(cuda_lib):
+    c = inputs.make("decode_m16_down", K=4096, N=1024)
+    a = run_abi(c.A, c.B, c.C0, 1.0, 1.0, F32)[0]
+    b = run_abi(c.A, c.B, c.C0, 1.0, 1.0, F32)[0]
+    assert torch.equal(a, b)
+
+
+def test_forced_paths_agree(cuda_lib):
+    c = inputs.make("decode_m16_o", M=16, N=640, K=512)
+    e1, p1 = check(c.A, c.B, c.C0, 1.0, 1.0, F32, path=g.PATH_SKINNY)
+    e2, p2 = check(c.A, c.B, c.C0, 1.0, 1.0, F32, path=g.PATH_BF16_TC)
+    e3, p3 = check(c.A, c.B, c.C0, 1.0, 1.0, F32, path=g.PATH_GENERIC)
+    assert (p1, p2, p3) == (g.PATH_SKINNY, g.PATH_BF16_TC, g.PATH_GENERIC)
+
+
+def test_forced_path_rejects_wrong_family(cuda_lib):
+    c = inputs.make("decode_m16_o", M=32, N=64, K=64)
+    with pytest.raises(g.GemmError) as e:
+        run_abi(c.A, c.B, c.C0, 1.0, 1.0, BF16, path=g.PATH_SKINNY)   # M > 16
+    assert e.value.code == g.GEMM_ERR_UNSUPPORTED
+    f = inputs.make("fp32_256", M=16, N=16, K=16)
+    with pytest.raises(g.GemmError) as e:
+        run_abi(f.A, f.B, None, 1.0, 0.0, F32, path=g.PATH_BF16_TC)
+    assert e.value.code == g.GEMM_ERR_UNSUPPORTED
+
+
+# ------------------------------------------------------------------ status and errors
+def test_bounded_wait_reports_timeout(cuda_lib):
+    assert g.device_status()[0] == 0
+    g.selftest_wait_timeout(2_000_000)   # 2 ms on a barrier nothing arrives at
+    status, where = g.device_status()
+    assert status == g.GEMM_ERR_DEVICE_TIMEOUT and where == 1
+    assert g.device_status()[0] == 0      # read-and-clear
+    # the context is still usable
+    c = inputs.make("fp32_256", M=64, N=64, K=64)
+    check(c.A, c.B, None, 1.0, 0.0, F32)
+
+
+def test_invalid_arguments(cuda_lib):
+    x = torch.zeros(1024, device="cuda")
+    p = x.data_ptr()
+    s = torch.cuda.current_stream().cuda_stream
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_f32(4, 4, 8, 1.0, p, 4, p, 4, 0.0, p, 4, s)     # lda < K
+    assert e.value.code == g.GEMM_ERR_INVALID_ARG
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_f32(4, 4, 4, 1.0, 0, 4, p, 4, 0.0, p, 4, s)     # null A
+    assert e.value.code == g.GEMM_ERR_INVALID_ARG
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_f32(4, 4, 4, 1.0, p + 2, 4, p, 4, 0.0, p, 4, s)  # not float-aligned
+    assert e.value.code == g.GEMM_ERR_MISALIGNED
+    g.gemm_f32(0, 4, 4, 1.0, 0, 4, 0, 4, 0.0, 0, 4, s)         # no-op
+    assert g.last_path() == g.PATH_AUTO
