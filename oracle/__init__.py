@@ -9,7 +9,10 @@ package imports nothing from it.
   ``oracle.c`` (a triple loop over rows, k and columns, k summed in order).
 * :func:`normwise_error` is the score the GPU result is held to:
   ``max|C_gpu - C_ref| / max_{m,n} sum_k |A[m,k]| |B[k,n]|``, the denominator
-  being the same oracle GEMM applied to |A| and |B|.
+  being the same oracle GEMM applied to |A| and |B|
+  (:func:`abs_product_max`).  For alpha != 1 or beta != 0 the scale of the
+  whole expression, ``max(|alpha| sum_k |A||B| + |beta| |C0|)``, is used
+  (:func:`normwise_denominator`); it equals the former at alpha=1, beta=0.
 * ``oracle.roofline_ref`` restates the FLOP, arithmetic-intensity and roofline
   formulas of the pages.
 
@@ -114,6 +117,28 @@ def abs_product_max(A, B, threads: int | None = None) -> float:
         return 0.0
     P = gemm(A64, B64, 1.0, 0.0, None, threads)
     return float(P.max()) if P.size else 0.0
+
+
+def normwise_denominator(A, B, alpha: float = 1.0, beta: float = 0.0, C0=None,
+                         threads: int | None = None) -> float:
+    """max_{m,n} (|alpha| sum_k |A[m,k]||B[k,n]| + |beta| |C0[m,n]|).
+
+    The normwise scale of the whole expression alpha*A*B + beta*C0.  With
+    alpha = 1 and beta = 0 it is exactly max sum_k |A||B|; with beta != 0 the
+    rounding of C to its output type is relative to |C|, which includes
+    beta*C0, so the C0 term belongs in the scale.
+    """
+    A64 = np.abs(to_f64(A))
+    B64 = np.abs(to_f64(B))
+    M, N = A64.shape[0], B64.shape[1]
+    if M == 0 or N == 0:
+        return 0.0
+    if beta != 0.0:
+        c0 = np.abs(to_f64(C0))
+        P = gemm(A64, B64, abs(alpha), abs(beta), c0, threads)
+    else:
+        P = gemm(A64, B64, abs(alpha), 0.0, None, threads)
+    return float(P.max())
 
 
 def normwise_error(C_gpu, C_ref: np.ndarray, denom: float) -> float:

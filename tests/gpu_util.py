@@ -62,18 +62,25 @@ def run_abi(A_cpu, B_cpu, C0_cpu, alpha, beta, out_dtype, *, pad=(0, 0, 0), offs
     return C_full[:, :N].clone(), C_full[:, N:].clone(), ran
 
 
-def check(A_cpu, B_cpu, C0_cpu, alpha, beta, out_dtype, *, tol=None, **kw):
-    """Run through the ABI, score against the oracle; returns (err, path)."""
+def check(A_cpu, B_cpu, C0_cpu, alpha, beta, out_dtype, *, tol=None, strict=False, **kw):
+    """Run through the ABI, score against the oracle; returns (err, path).
+
+    The scale is that of the whole expression (|alpha||A||B| + |beta||C0|);
+    strict=True also requires the bound with the plain max sum_k |A||B|."""
     in_kind = "f32" if A_cpu.dtype == torch.float32 else "bf16"
     tol = TOL[(in_kind, out_dtype)] if tol is None else tol
     C, pad_cols, ran = run_abi(A_cpu, B_cpu, C0_cpu, alpha, beta, out_dtype, **kw)
     C0_exact = C0_cpu.to(out_dtype) if C0_cpu is not None else None
     ref = oracle.gemm(A_cpu, B_cpu, alpha, beta, C0_exact)
-    denom = oracle.abs_product_max(A_cpu, B_cpu)
+    denom = oracle.normwise_denominator(A_cpu, B_cpu, alpha, beta, C0_exact)
     if denom == 0.0:
         denom = 1.0
     err = oracle.normwise_error(C, ref, denom)
     assert err <= tol, f"normwise error {err:.3e} > {tol:g} (path {g.PATH_NAMES.get(ran)})"
+    if strict:
+        plain = oracle.abs_product_max(A_cpu, B_cpu)
+        err_plain = oracle.normwise_error(C, ref, plain if plain else 1.0)
+        assert err_plain <= tol, f"normwise error (plain scale) {err_plain:.3e} > {tol:g}"
     # the padding of C's rows is never written
     if pad_cols.numel():
         pc = pad_cols.to(torch.float64).numpy()
@@ -96,7 +103,7 @@ def sampled_check(A_dev, B_dev, C_dev, A_cpu, B_cpu, C0_cpu, alpha, beta, tol, r
             G = C_cpu[:, cols]
             C0_s = C0_cpu[:, cols] if C0_cpu is not None else None
         ref = oracle.gemm(A_s, B_s, alpha, beta, C0_s)
-        denom = oracle.abs_product_max(A_s, B_s)
+        denom = oracle.normwise_denominator(A_s, B_s, alpha, beta, C0_s)
         err = oracle.normwise_error(G, ref, denom if denom else 1.0)
         worst = max(worst, err)
     assert worst <= tol, f"sampled normwise error {worst:.3e} > {tol:g}"

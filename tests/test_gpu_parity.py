@@ -33,7 +33,7 @@ def expected_path(M, N, K, in_kind):
 # ------------------------------------------------------------------ fp32 path
 def test_fp32_256_full(cuda_lib):
     c = inputs.make("fp32_256")
-    err, path = check(c.A, c.B, None, 1.0, 0.0, F32)
+    err, path = check(c.A, c.B, None, 1.0, 0.0, F32, strict=True)
     assert path == g.PATH_F32_SIMT
 
 
@@ -200,7 +200,7 @@ def test_skinny_odd_m(cuda_lib, m):
 def test_decode_full_size(cuda_lib, m, w):
     # decode GEMMs are small enough for the oracle to check every element
     c = inputs.make(f"decode_m{m}_{w}")
-    err, path = check(c.A, c.B, c.C0, 1.0, 1.0, BF16)
+    err, path = check(c.A, c.B, c.C0, 1.0, 1.0, BF16, strict=True)
     assert path == g.PATH_SKINNY
 
 

@@ -200,3 +200,15 @@ def test_normwise_error_definition():
     assert oracle.normwise_error(G, ref, denom) == 0.01
     G[0, 0] = np.nan
     assert oracle.normwise_error(G, ref, denom) == float("inf")
+
+
+def test_normwise_denominator_of_the_full_expression():
+    A = np.array([[1.0, -2.0], [3.0, 4.0]])
+    B = np.array([[5.0, 6.0], [-7.0, 8.0]])
+    C0 = np.array([[-10.0, 0.0], [1.0, 2.0]])
+    # alpha = 1, beta = 0: the plain max sum_k |A||B| (= 50)
+    assert oracle.normwise_denominator(A, B) == oracle.abs_product_max(A, B) == 50.0
+    # |alpha| |A||B| + |beta| |C0| = 0.5*[[19,22],[43,50]] + 2*[[10,0],[1,2]] -> max(29.5, 11, 23.5, 29)
+    assert oracle.normwise_denominator(A, B, -0.5, -2.0, C0) == 29.5
+    # beta = 0 never reads C0
+    assert oracle.normwise_denominator(A, B, 1.0, 0.0, np.full((2, 2), np.nan)) == 50.0
