@@ -1,0 +1,58 @@
+"""Run one named GEMM workload through the C ABI a few times (for profiling).
+
+    python -m roofline_driven_optimisation_gb300.run_case --case bf16_8192 --reps 3
+    python -m roofline_driven_optimisation_gb300.run_case --case decode_m16_lm --out f32
+
+Prints the kernel family and the CUDA-event time of each call.  Workload
+names are those of ``roofline_driven_optimisation_gb300.inputs``.
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def main():
+    import torch
+    import roofline_driven_optimisation_gb300 as g
+    from roofline_driven_optimisation_gb300 import inputs
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--case", required=True, choices=sorted(inputs.SPECS))
+    ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--out", default="auto", choices=["auto", "bf16", "f32"])
+    ap.add_argument("--M", type=int)
+    ap.add_argument("--N", type=int)
+    ap.add_argument("--K", type=int)
+    a = ap.parse_args()
+
+    g.load()
+    c = inputs.make(a.case, M=a.M, N=a.N, K=a.K)
+    sp = c.spec
+    if sp.in_dtype == "f32":
+        out = torch.float32
+    else:
+        out = torch.float32 if a.out == "f32" else torch.bfloat16
+    A, B = c.A.cuda(), c.B.cuda()
+    C = c.C0.to(out).cuda() if c.C0 is not None else torch.zeros((sp.M, sp.N), dtype=out, device="cuda")
+    for i in range(a.reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.gemm(A, B, C, sp.alpha, sp.beta)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        print(f"{a.case} M={sp.M} N={sp.N} K={sp.K} path={g.PATH_NAMES[g.last_path()]} "
+              f"call {i}: {ms:.4f} ms, {2 * sp.M * sp.N * sp.K / ms / 1e9:.1f} TFLOP/s")
+    status, where = g.device_status()
+    if status != 0:
+        raise SystemExit(f"device status {status} at site {where}")
+
+
+if __name__ == "__main__":
+    main()
