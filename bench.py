@@ -46,7 +46,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM bytes per launch measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum)
 # for each kernel source file, valid only while the file hashes to `sha256`.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/sgemm_tma_kernel_fp32_4096.md: 425.7 MB read + 56.4 MB written
+    "gemm_f32_simt.cu": {"sha256": "e2d4e4fff5d5e3707ad8cd3347fa0d420cd77d411fdf96feaedca8e614e039a7",
+                         "bytes_per_launch": 482115328},
+}
 
 
 def peaks():
