@@ -374,12 +374,15 @@ def oracle_sample_step(parts, frac, threads):
 
 
 def _calibrate(parts, threads, target_s):
-    """Row fraction whose oracle sample takes about target_s seconds."""
-    frac = 1.0 / 512
-    t = time.perf_counter()
-    oracle_sample_step(parts, frac, threads)
-    dt = max(time.perf_counter() - t, 1e-3)
-    return min(1.0, frac * target_s / dt)
+    """Row fraction whose oracle sample takes about target_s seconds (two
+    rounds: the first run is dominated by fixed per-call costs)."""
+    frac = 1.0 / 256
+    for _ in range(2):
+        t = time.perf_counter()
+        oracle_sample_step(parts, frac, threads)
+        dt = max(time.perf_counter() - t, 1e-3)
+        frac = min(1.0, frac * target_s / dt) if _ == 1 else min(1.0, frac * min(8.0, target_s / dt))
+    return frac
 
 
 def cpu_baseline(parts, target_s=15.0):

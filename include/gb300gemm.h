@@ -124,6 +124,18 @@ int gemm_force_path(int path);
 int gemm_last_path(void);
 
 /*
+ * Pin the C tile width of the tensor-core kernel for later calls on this host
+ * thread: 128, 192, 224 or 256 columns (tiles are 128 rows high); 0 restores
+ * the automatic choice, which minimises the work of the last partial wave of
+ * tiles over the SMs.  Other values return GEMM_ERR_INVALID_ARG.  For A/B
+ * measurements and tests.
+ */
+int gemm_force_tile_n(int bn);
+
+/* Tile width the last tensor-core call on this host thread used (0 if none). */
+int gemm_last_tile_n(void);
+
+/*
  * Upper bound, in nanoseconds, on any single wait inside a kernel launched
  * later by this process (default 1e9).  After it a kernel records
  * GEMM_ERR_DEVICE_TIMEOUT in the status word and returns.  0 restores the

@@ -37,8 +37,8 @@ PATH_NAMES = {PATH_AUTO: "none", PATH_GENERIC: "generic", PATH_F32_SIMT: "f32_si
 
 # every symbol the public header declares
 EXPORTS = ("gemm_f32", "gemm_bf16", "gemm_bf16_f32out", "gemm_get_last_error",
-           "gemm_device_status", "gemm_force_path", "gemm_last_path",
-           "gemm_set_wait_timeout_ns", "gemm_selftest_wait_timeout")
+           "gemm_device_status", "gemm_force_path", "gemm_last_path", "gemm_force_tile_n",
+           "gemm_last_tile_n", "gemm_set_wait_timeout_ns", "gemm_selftest_wait_timeout")
 
 _lib = None
 _lock = threading.Lock()
@@ -81,6 +81,10 @@ def load(path: str | None = None):
         lib.gemm_force_path.restype = i
         lib.gemm_last_path.argtypes = []
         lib.gemm_last_path.restype = i
+        lib.gemm_force_tile_n.argtypes = [i]
+        lib.gemm_force_tile_n.restype = i
+        lib.gemm_last_tile_n.argtypes = []
+        lib.gemm_last_tile_n.restype = i
         lib.gemm_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
         lib.gemm_set_wait_timeout_ns.restype = i
         lib.gemm_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
@@ -120,6 +124,14 @@ def force_path(path: int):
 
 def last_path() -> int:
     return load().gemm_last_path()
+
+
+def force_tile_n(bn: int):
+    _check(load().gemm_force_tile_n(bn))
+
+
+def last_tile_n() -> int:
+    return load().gemm_last_tile_n()
 
 
 def set_wait_timeout_ns(ns: int):

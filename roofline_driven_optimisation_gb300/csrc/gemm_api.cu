@@ -30,6 +30,8 @@ namespace {
 thread_local char t_msg[512] = "";
 thread_local int t_forced_path = GEMM_PATH_AUTO;
 thread_local int t_last_path = GEMM_PATH_AUTO;
+thread_local int t_forced_bn = 0;
+thread_local int t_last_bn = 0;
 std::atomic<uint64_t> g_timeout_ns{1000000000ull};
 
 int fail(int code, const char* fmt, ...) {
@@ -226,7 +228,11 @@ int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int 
       if ((rc = make_map(B, N, K, (uint64_t)ldb * 2, 64, kTcBK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                          CU_TENSOR_MAP_SWIZZLE_128B, &mB)) != GEMM_OK)
         return rc;
-      err = launch_bf16_tc(a, mA, mB, dev->num_sms, stream);
+    {
+      const int bn = t_forced_bn ? t_forced_bn : choose_tc_bn(M, N, dev->num_sms);
+      err = launch_bf16_tc(a, mA, mB, bn, dev->num_sms, stream);
+      if (err == cudaSuccess) t_last_bn = bn;
+    }
       break;
     case GEMM_PATH_SKINNY:
       if ((rc = make_map(A, K, M, (uint64_t)lda * 2, kSkBK, kSkMaxM, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
@@ -310,6 +316,15 @@ int gemm_force_path(int path) {
 }
 
 int gemm_last_path(void) { return g3::t_last_path; }
+
+int gemm_force_tile_n(int bn) {
+  if (bn != 0 && bn != 128 && bn != 192 && bn != 224 && bn != 256)
+    return g3::fail(GEMM_ERR_INVALID_ARG, "tile width %d is not 0, 128, 192, 224 or 256", bn);
+  g3::t_forced_bn = bn;
+  return GEMM_OK;
+}
+
+int gemm_last_tile_n(void) { return g3::t_last_bn; }
 
 int gemm_set_wait_timeout_ns(uint64_t timeout_ns) {
   g3::g_timeout_ns.store(timeout_ns == 0 ? 1000000000ull : timeout_ns);

@@ -37,22 +37,29 @@
 namespace g3 {
 namespace {
 
-constexpr int BM = kTcBM, BN = kTcBN, BK = kTcBK;
-constexpr int STAGES = 4;
+constexpr int BM = kTcBM, BK = kTcBK;
 constexpr int UMMA_K = 16;
 constexpr int A_STAGE_BYTES = BM * BK * 2;                // 16 KB
 constexpr int B_BOX_BYTES = 64 * BK * 2;                  // 8 KB (64 n x 64 k)
-constexpr int B_STAGE_BYTES = BN * BK * 2;                // 32 KB
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-constexpr int TMEM_COLS = 512;                            // 2 accumulators x 256 fp32 columns
+constexpr int TMEM_COLS = 512;                            // two accumulators of up to 256 columns
 constexpr int NUM_EPI_WARPS = 4;
 constexpr int THREADS = 64 + NUM_EPI_WARPS * 32;
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+constexpr int SMEM_LIMIT = 232448;                        // opt-in dynamic shared memory per CTA
 constexpr int RASTER_GROUP = 16;
 
-static_assert(BN % 64 == 0 && BN <= 256, "B tile is made of 64-column boxes");
-static_assert(2 * BN <= TMEM_COLS, "two accumulators must fit in TMEM");
+// Tile geometry for a C tile of BM x BN.  B is loaded as ceil(BN/64) boxes of
+// 64 columns; the MMA reads BN of them.
+template <int BN>
+struct TileCfg {
+  static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "tcgen05 N for M=128, 32-column epilogue");
+  static constexpr int B_BOXES = (BN + 63) / 64;
+  static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_BOXES * B_BOX_BYTES;
+  static constexpr int STAGES_FIT = (SMEM_LIMIT - BAR_BYTES - 1024) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+  static_assert(2 * BN <= TMEM_COLS, "two accumulators must fit in TMEM");
+};
 
 struct TcParams {
   GemmArgs a;
@@ -60,6 +67,7 @@ struct TcParams {
   int c_vec;  // C 16-byte aligned and ldc*sizeof(out) a multiple of 16
 };
 
+template <int BN>
 __device__ __forceinline__ void tile_coords(int tile, const TcParams& p, int& m0, int& n0) {
   const int per_group = RASTER_GROUP * p.tiles_n;
   const int g = tile / per_group;
@@ -150,10 +158,13 @@ __device__ __forceinline__ void store_row32(const TcParams& p, long long m, long
   }
 }
 
-template <bool OUT_BF16>
+template <int BN, bool OUT_BF16>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap mapA,
                         const __grid_constant__ CUtensorMap mapB, const TcParams p) {
+  using Cfg = TileCfg<BN>;
+  constexpr int STAGES = Cfg::STAGES;
+  constexpr int STAGE_BYTES = Cfg::STAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1024-byte alignment
@@ -201,15 +212,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (elect_one_sync()) {
       tma_prefetch_desc(&mapA);
       tma_prefetch_desc(&mapB);
-      int issued_parity[STAGES];
-#pragma unroll
-      for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+      // bit s of `issued`: slot s has had a copy issued; bit s of
+      // `issued_par`: the phase parity of its latest copy
+      uint32_t issued = 0, issued_par = 0;
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
         int m0, n0;
-        tile_coords(tile, p, m0, n0);
+        tile_coords<BN>(tile, p, m0, n0);
         for (int kt = 0; kt < p.k_tiles; ++kt) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, a.timeout_ns, abort_flag)) {
             if (!*abort_flag) report_status(a.status, 5, kSiteTcProducer);
@@ -220,10 +231,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
           tma_load_2d(a_tile(stage), &mapA, full_bar(stage), kt * BK, m0);
 #pragma unroll
-          for (int j = 0; j < BN / 64; ++j)
+          for (int j = 0; j < Cfg::B_BOXES; ++j)
             tma_load_2d(b_tile(stage) + j * B_BOX_BYTES, &mapB, full_bar(stage), n0 + j * 64,
                         kt * BK);
-          issued_parity[stage] = (int)phase;
+          issued |= 1u << stage;
+          issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -232,8 +244,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (*abort_flag) {
         for (int s = 0; s < STAGES; ++s)
-          if (issued_parity[s] >= 0 &&
-              !mbar_wait(full_bar(s), (uint32_t)issued_parity[s], a.timeout_ns, nullptr))
+          if (((issued >> s) & 1u) &&
+              !mbar_wait(full_bar(s), (issued_par >> s) & 1u, a.timeout_ns, nullptr))
             report_status(a.status, 5, kSiteTcDrain);
       }
     }
@@ -300,7 +312,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
       int m0, n0;
-      tile_coords(tile, p, m0, n0);
+      tile_coords<BN>(tile, p, m0, n0);
       if (!mbar_wait(tfull_bar(acc), acc_phase, a.timeout_ns, abort_flag)) {
         if (!*abort_flag) report_status(a.status, 5, kSiteTcEpilogue);
         *abort_flag = 1;
@@ -336,15 +348,16 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-template <bool OUT_BF16>
+template <int BN, bool OUT_BF16>
 int launch_impl(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB, int num_sms,
                 cudaStream_t s) {
+  using Cfg = TileCfg<BN>;
   static int attr_done_mask = 0;  // per-device bits; a race only repeats the call
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 31 && !(attr_done_mask & (1 << dev))) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc_kernel<OUT_BF16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc_kernel<BN, OUT_BF16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_done_mask |= (1 << dev);
   }
@@ -360,16 +373,52 @@ int launch_impl(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* m
   const int out_bytes = OUT_BF16 ? 2 : 4;
   p.c_vec = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && ((a.ldc * out_bytes) % 16) == 0) ? 1 : 0;
   const int grid = (int)(tiles < num_sms ? tiles : num_sms);
-  gemm_bf16_tc_kernel<OUT_BF16><<<grid, THREADS, SMEM_BYTES, s>>>(*mapA, *mapB, p);
+  gemm_bf16_tc_kernel<BN, OUT_BF16><<<grid, THREADS, Cfg::SMEM_BYTES, s>>>(*mapA, *mapB, p);
   return cudaGetLastError();
+}
+
+template <bool OUT_BF16>
+int launch_bn(int bn, const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
+              int num_sms, cudaStream_t s) {
+  switch (bn) {
+    case 256: return launch_impl<256, OUT_BF16>(a, mapA, mapB, num_sms, s);
+    case 224: return launch_impl<224, OUT_BF16>(a, mapA, mapB, num_sms, s);
+    case 192: return launch_impl<192, OUT_BF16>(a, mapA, mapB, num_sms, s);
+    case 128: return launch_impl<128, OUT_BF16>(a, mapA, mapB, num_sms, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
 
+// Tile width for a persistent grid: every wave of tiles costs about one
+// tile-time, so minimise waves(BN) * BN * cost_per_column(BN).  The relative
+// per-column costs are measured on GB300 at 8192^3, where the last-wave loss is
+// small: 1.000 (256), 1.012 (192), 1.070 (128); 224-wide MMAs cost 1.115 and
+// are never chosen automatically.  Ties go to the wider tile.
+int choose_tc_bn(int M, int N, int num_sms) {
+  static const int cands[] = {256, 192, 128};
+  static const int cost_milli[] = {1000, 1012, 1070};
+  const long long tiles_m = (M + BM - 1) / BM;
+  int best = 256;
+  long long best_cost = -1;
+  for (int i = 0; i < 3; ++i) {
+    const int bn = cands[i];
+    const long long tiles = tiles_m * ((N + bn - 1) / bn);
+    const long long waves = (tiles + num_sms - 1) / num_sms;
+    const long long cost = waves * bn * cost_milli[i];
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
 int launch_bf16_tc(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
-                   int num_sms, cudaStream_t s) {
-  if (a.out == Elem::BF16) return launch_impl<true>(a, mapA, mapB, num_sms, s);
-  return launch_impl<false>(a, mapA, mapB, num_sms, s);
+                   int bn, int num_sms, cudaStream_t s) {
+  if (a.out == Elem::BF16) return launch_bn<true>(bn, a, mapA, mapB, num_sms, s);
+  return launch_bn<false>(bn, a, mapA, mapB, num_sms, s);
 }
 
 }  // namespace g3

@@ -7,7 +7,9 @@
 //     256 floats, feeds 16384 FMAs, 64x reuse), K-slices of 16;
 //   * warp tile 64 x 32 (10.4.1: about 21x reuse from shared memory);
 //   * register tile 8 x 8 per thread (10.4.1: every loaded element used 8x;
-//     section 10.6 is the 4 x 4 version of the same idea).
+//     section 10.6 is the 4 x 4 version of the same idea), accumulated with
+//     the packed fma.rn.f32x2 (two IEEE fp32 FMAs per instruction), so the
+//     FMA pipe, not instruction issue, is the limit.
 // The K-slices stream through a 4-stage shared-memory ring filled by TMA
 // ("Kernel 性能从何而来", section "优化阶梯": TMA-backed loads are the first big
 // step), one producer warp issuing copies and eight compute warps consuming
@@ -35,7 +37,7 @@ constexpr int A_STAGE_BYTES = BM * BK * 4;  // 8 KB
 constexpr int B_STAGE_BYTES = BK * BN * 4;  // 8 KB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int COMPUTE_WARPS = 8;
-constexpr int THREADS = (COMPUTE_WARPS + 1) * 32;
+constexpr int THREADS = COMPUTE_WARPS * 32;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 
 struct SimtParams {
@@ -52,7 +54,37 @@ __device__ __forceinline__ float4 lds128(uint32_t addr) {
   return v;
 }
 
-__global__ void __launch_bounds__(THREADS, 1)
+__device__ __forceinline__ float2 lds64(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+  return v;
+}
+
+// Two consecutive float pairs from shared memory as packed 64-bit registers.
+__device__ __forceinline__ void lds_pairs(uint32_t addr, uint64_t& p0, uint64_t& p1) {
+  asm volatile("ld.shared.v2.b64 {%0,%1}, [%2];" : "=l"(p0), "=l"(p1) : "r"(addr));
+}
+
+// (x, x) as a packed pair.
+__device__ __forceinline__ uint64_t dup2(float x) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(x));
+  return r;
+}
+
+// d.lo += a.lo * b.lo; d.hi += a.hi * b.hi -- two IEEE fp32 FMAs in one
+// instruction, which halves the FMA issue slots of the outer product.
+__device__ __forceinline__ void ffma2(uint64_t& d, uint64_t a, uint64_t b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+
+__device__ __forceinline__ float2 unpack2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+
+__global__ void __launch_bounds__(THREADS, 2)
     sgemm_tma_kernel(const __grid_constant__ CUtensorMap mapA,
                      const __grid_constant__ CUtensorMap mapB, const SimtParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -92,120 +124,126 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   __syncthreads();
 
-  if (warp == COMPUTE_WARPS) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      tma_prefetch_desc(&mapA);
-      tma_prefetch_desc(&mapB);
-      int issued_parity[STAGES];
-      for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
-      for (int kt = 0; kt < k_tiles; ++kt) {
-        const int s = kt % STAGES;
-        if (kt >= STAGES) {
-          if (!mbar_wait(empty_bar(s), ((kt / STAGES) - 1) & 1, a.timeout_ns, abort_flag)) {
-            if (!*abort_flag) report_status(a.status, 5, kSiteSimtProducer);
-            *abort_flag = 1;
-            break;
-          }
+  // Lane 0 of warp 0 also issues the TMA copies: the first STAGES K-slices up
+  // front, then each slot again as soon as all eight warps have released it.
+  // (A dedicated producer warp would put five warps on one scheduler at two
+  // CTAs per SM and cap registers at 96.)
+  const bool producer = threadIdx.x == 0;
+  // slot s has a copy in flight when bit s of `issued` is set; its phase
+  // parity is bit s of `issued_par`
+  uint32_t issued = 0, issued_par = 0;
+  if (producer) {
+    tma_prefetch_desc(&mapA);
+    tma_prefetch_desc(&mapB);
+    for (int kt = 0; kt < k_tiles && kt < STAGES; ++kt) {
+      mbar_arrive_expect_tx(full_bar(kt), STAGE_BYTES);
+      tma_load_2d(a_tile(kt), &mapA, full_bar(kt), kt * BK, m0);
+      tma_load_2d(b_tile(kt), &mapB, full_bar(kt), n0, kt * BK);
+      issued |= 1u << kt;
+    }
+  }
+
+  const int wm = warp / 4, wn = warp % 4;
+  const int tm = lane % 8, tn = lane / 8;
+  const int sw = (tm >> 1) & 3;                // 64-byte swizzle phase of my rows
+  const uint32_t a_row_off = (uint32_t)(wm * 64 + tm) * 64u;
+  const uint32_t b_col_off = (uint32_t)(wn * 32 + tn * 4) * 4u;
+  // acc[i][q] holds C columns (2q, 2q+1) of my 8 columns, row i
+  uint64_t acc[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[i][q] = 0ull;
+
+  bool ok = true;
+  for (int kt = 0; kt < k_tiles; ++kt) {
+    const int s = kt % STAGES;
+    const uint32_t parity = (uint32_t)(kt / STAGES) & 1u;
+    if (!mbar_wait(full_bar(s), parity, a.timeout_ns, abort_flag)) {
+      if (!*abort_flag) report_status(a.status, 5, kSiteSimtConsumer);
+      *abort_flag = 1;
+      ok = false;
+      break;
+    }
+    const uint32_t at = a_tile(s) + a_row_off;
+    const uint32_t bt = b_tile(s) + b_col_off;
+#pragma unroll 4
+    for (int kp = 0; kp < BK / 2; ++kp) {
+      // rows i*8+tm, k = 2kp, 2kp+1: one 8-byte load per row inside the
+      // swizzled 16-byte chunk that holds k = 4*(kp/2) .. 4*(kp/2)+3
+      const uint32_t off = (uint32_t)((((kp >> 1) ^ sw) * 16) + (kp & 1) * 8);
+      float2 av[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) av[i] = lds64(at + i * 8 * 64 + off);
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        const uint32_t brow = bt + (uint32_t)(kp * 2 + kk) * (BN * 4);
+        uint64_t b[4];
+        lds_pairs(brow, b[0], b[1]);
+        lds_pairs(brow + 64, b[2], b[3]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint64_t a2 = dup2(kk == 0 ? av[i].x : av[i].y);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) ffma2(acc[i][q], a2, b[q]);
         }
-        mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
-        tma_load_2d(a_tile(s), &mapA, full_bar(s), kt * BK, m0);
-        tma_load_2d(b_tile(s), &mapB, full_bar(s), n0, kt * BK);
-        issued_parity[s] = (kt / STAGES) & 1;
-      }
-      if (*abort_flag) {
-        // Let every copy already issued land before shared memory is released.
-        for (int s = 0; s < STAGES; ++s)
-          if (issued_parity[s] >= 0 &&
-              !mbar_wait(full_bar(s), issued_parity[s], a.timeout_ns, nullptr))
-            report_status(a.status, 5, kSiteSimtDrain);
       }
     }
-  } else {
-    // ------------------------------------------------------------ compute
-    const int wm = warp / 4, wn = warp % 4;
-    const int tm = lane % 8, tn = lane / 8;
-    const int sw = (tm >> 1) & 3;                // 64-byte swizzle phase of my rows
-    const uint32_t a_row_off = (uint32_t)(wm * 64 + tm) * 64u;
-    const uint32_t b_col_off = (uint32_t)(wn * 32 + tn * 4) * 4u;
-    float acc[8][8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-
-    bool ok = true;
-    for (int kt = 0; kt < k_tiles; ++kt) {
-      const int s = kt % STAGES;
-      if (!mbar_wait(full_bar(s), (kt / STAGES) & 1, a.timeout_ns, abort_flag)) {
-        if (!*abort_flag) report_status(a.status, 5, kSiteSimtConsumer);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_bar(s));
+    if (producer && kt + STAGES < k_tiles) {
+      // refill slot s with K-slice kt+STAGES once every warp has released it
+      if (!mbar_wait(empty_bar(s), parity, a.timeout_ns, abort_flag)) {
+        if (!*abort_flag) report_status(a.status, 5, kSiteSimtProducer);
         *abort_flag = 1;
         ok = false;
         break;
       }
-      const uint32_t at = a_tile(s) + a_row_off;
-      const uint32_t bt = b_tile(s) + b_col_off;
-#pragma unroll
-      for (int kq = 0; kq < BK / 4; ++kq) {
-        float4 av[8];
-        const uint32_t chunk = (uint32_t)((kq ^ sw) * 16);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) av[i] = lds128(at + i * 8 * 64 + chunk);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint32_t brow = bt + (uint32_t)(kq * 4 + kk) * (BN * 4);
-          const float4 b0 = lds128(brow);
-          const float4 b1 = lds128(brow + 64);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float ai = kk == 0 ? av[i].x : kk == 1 ? av[i].y : kk == 2 ? av[i].z : av[i].w;
-            acc[i][0] = fmaf(ai, b0.x, acc[i][0]);
-            acc[i][1] = fmaf(ai, b0.y, acc[i][1]);
-            acc[i][2] = fmaf(ai, b0.z, acc[i][2]);
-            acc[i][3] = fmaf(ai, b0.w, acc[i][3]);
-            acc[i][4] = fmaf(ai, b1.x, acc[i][4]);
-            acc[i][5] = fmaf(ai, b1.y, acc[i][5]);
-            acc[i][6] = fmaf(ai, b1.z, acc[i][6]);
-            acc[i][7] = fmaf(ai, b1.w, acc[i][7]);
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty_bar(s));
+      const int kn = kt + STAGES;
+      mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
+      tma_load_2d(a_tile(s), &mapA, full_bar(s), kn * BK, m0);
+      tma_load_2d(b_tile(s), &mapB, full_bar(s), n0, kn * BK);
+      issued_par = (issued_par & ~(1u << s)) | ((uint32_t)((kn / STAGES) & 1) << s);
     }
+  }
+  if (producer && *abort_flag) {
+    // every copy already issued must land before shared memory is released
+    for (int s = 0; s < STAGES; ++s)
+      if (((issued >> s) & 1u) &&
+          !mbar_wait(full_bar(s), (issued_par >> s) & 1u, a.timeout_ns, nullptr))
+        report_status(a.status, 5, kSiteSimtDrain);
+  }
 
-    if (ok) {
-      // ---------------------------------------------------------- epilogue
-      float* C = static_cast<float*>(a.C);
-      const bool beta_nz = a.beta != 0.f;
+  if (ok) {
+    // ---------------------------------------------------------- epilogue
+    float* C = static_cast<float*>(a.C);
+    const bool beta_nz = a.beta != 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const long long m = (long long)m0 + wm * 64 + i * 8 + tm;
-        if (m >= a.M) continue;
+    for (int i = 0; i < 8; ++i) {
+      const long long m = (long long)m0 + wm * 64 + i * 8 + tm;
+      if (m >= a.M) continue;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const long long n = (long long)n0 + wn * 32 + h * 16 + tn * 4;
-          float* cp = C + m * a.ldc + n;
-          float v[4];
+      for (int h = 0; h < 2; ++h) {
+        const long long n = (long long)n0 + wn * 32 + h * 16 + tn * 4;
+        float* cp = C + m * a.ldc + n;
+        const float2 lo = unpack2(acc[i][2 * h]), hi = unpack2(acc[i][2 * h + 1]);
+        float v[4] = {a.alpha * lo.x, a.alpha * lo.y, a.alpha * hi.x, a.alpha * hi.y};
+        if (p.c_vec && n + 3 < a.N) {
+          if (beta_nz) {
+            const float4 c = *reinterpret_cast<const float4*>(cp);
+            v[0] = fmaf(a.beta, c.x, v[0]);
+            v[1] = fmaf(a.beta, c.y, v[1]);
+            v[2] = fmaf(a.beta, c.z, v[2]);
+            v[3] = fmaf(a.beta, c.w, v[3]);
+          }
+          *reinterpret_cast<float4*>(cp) = make_float4(v[0], v[1], v[2], v[3]);
+        } else {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) v[j] = a.alpha * acc[i][h * 4 + j];
-          if (p.c_vec && n + 3 < a.N) {
-            if (beta_nz) {
-              const float4 c = *reinterpret_cast<const float4*>(cp);
-              v[0] = fmaf(a.beta, c.x, v[0]);
-              v[1] = fmaf(a.beta, c.y, v[1]);
-              v[2] = fmaf(a.beta, c.z, v[2]);
-              v[3] = fmaf(a.beta, c.w, v[3]);
-            }
-            *reinterpret_cast<float4*>(cp) = make_float4(v[0], v[1], v[2], v[3]);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              if (n + j < a.N) {
-                float r = v[j];
-                if (beta_nz) r = fmaf(a.beta, cp[j], r);
-                cp[j] = r;
-              }
+          for (int j = 0; j < 4; ++j) {
+            if (n + j < a.N) {
+              float r = v[j];
+              if (beta_nz) r = fmaf(a.beta, cp[j], r);
+              cp[j] = r;
             }
           }
         }

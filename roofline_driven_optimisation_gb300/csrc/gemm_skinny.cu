@@ -38,7 +38,10 @@ namespace {
 constexpr int BN = kSkBN;    // B columns per CTA (MMA M)
 constexpr int BK = kSkBK;    // K per stage
 constexpr int MN = kSkMaxM;  // MMA N: activation rows, zero-padded by TMA
-constexpr int STAGES = 6;
+#ifndef GB300_SKINNY_STAGES
+#define GB300_SKINNY_STAGES 6
+#endif
+constexpr int STAGES = GB300_SKINNY_STAGES;
 constexpr int UMMA_K = 16;
 constexpr int B_BOX_BYTES = 64 * BK * 2;                 // 8 KB: 64 columns x 64 k
 constexpr int B_STAGE_BYTES = BN * BK * 2;               // 16 KB
@@ -111,9 +114,9 @@ __global__ void __launch_bounds__(THREADS, 2)
       tma_prefetch_desc(&mapA);
       tma_prefetch_desc(&mapB);
       const uint64_t stream_policy = l2_policy_evict_first();
-      int issued_parity[STAGES];
-#pragma unroll
-      for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+      // bit s of `issued`: slot s has had a copy issued; bit s of
+      // `issued_par`: the phase parity of its latest copy
+      uint32_t issued = 0, issued_par = 0;
       int stage = 0;
       uint32_t phase = 0;
       for (int kt = kt_begin; kt < kt_end; ++kt) {
@@ -128,7 +131,8 @@ __global__ void __launch_bounds__(THREADS, 2)
           tma_load_2d_hint(b_tile(stage) + j * B_BOX_BYTES, &mapB, full_bar(stage), n0 + j * 64,
                            kt * BK, stream_policy);
         tma_load_2d(a_tile(stage), &mapA, full_bar(stage), kt * BK, 0);
-        issued_parity[stage] = (int)phase;
+        issued |= 1u << stage;
+        issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -136,8 +140,8 @@ __global__ void __launch_bounds__(THREADS, 2)
       }
       if (*abort_flag) {
         for (int s = 0; s < STAGES; ++s)
-          if (issued_parity[s] >= 0 &&
-              !mbar_wait(full_bar(s), (uint32_t)issued_parity[s], a.timeout_ns, nullptr))
+          if (((issued >> s) & 1u) &&
+              !mbar_wait(full_bar(s), (issued_par >> s) & 1u, a.timeout_ns, nullptr))
             report_status(a.status, 5, kSiteSkinnyDrain);
       }
     }

@@ -50,10 +50,11 @@ int launch_f32_simt(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMa
 constexpr int kSimtBM = 128, kSimtBN = 128, kSimtBK = 16;
 
 // BF16 tcgen05 kernel: TMA tiles of A (64 k x 128 m) and B (64 n x 64 k),
-// 128-byte swizzle.
-int launch_bf16_tc(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
+// 128-byte swizzle; C tiles of 128 x bn with bn from choose_tc_bn().
+int choose_tc_bn(int M, int N, int num_sms);
+int launch_bf16_tc(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB, int bn,
                    int num_sms, cudaStream_t s);
-constexpr int kTcBM = 128, kTcBN = 256, kTcBK = 64;
+constexpr int kTcBM = 128, kTcBK = 64;
 
 // Skinny (M <= 16) split-K kernel: TMA tiles of B (64 n x 64 k) and A
 // (64 k x 16 rows), 128-byte swizzle.

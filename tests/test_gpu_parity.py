@@ -125,6 +125,32 @@ def test_bf16_tc_alpha_beta(cuda_lib, out, alpha, beta):
     assert path == g.PATH_BF16_TC
 
 
+@pytest.mark.parametrize("bn", [128, 192, 224, 256])
+@pytest.mark.parametrize("M,N,K", [(300, 1000, 200), (256, 4096, 128), (140, 456, 520)])
+def test_bf16_tc_every_tile_width(cuda_lib, bn, M, N, K):
+    c = inputs.make("decode_m16_o", M=M, N=N, K=K)
+    g.force_tile_n(bn)
+    try:
+        for out, beta in ((BF16, 0.0), (F32, 0.5)):
+            err, path = check(c.A, c.B, c.C0, 1.0, beta, out)
+            assert path == g.PATH_BF16_TC and g.last_tile_n() == bn
+    finally:
+        g.force_tile_n(0)
+
+
+def test_bf16_tc_tile_width_choice(cuda_lib):
+    # 8192^3 on 152 SMs: 256-wide tiles; 4096 x 4096: 128-wide tiles (7 waves
+    # of 128 cost less than 4 of 256 with the last one a third full)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for n, want in ((8192, 256), (4096, 128)):
+        c = inputs.make("bf16_4096", M=n, N=n, K=64)
+        check(c.A, c.B, None, 1.0, 0.0, BF16)
+        if sms == 152:
+            assert g.last_tile_n() == want, (n, g.last_tile_n())
+    with pytest.raises(g.GemmError):
+        g.force_tile_n(100)
+
+
 def test_bf16_tc_padded_and_unaligned_c(cuda_lib):
     c = inputs.make("bf16_4096", M=260, N=272, K=136)
     check(c.A, c.B, None, 1.0, 0.0, BF16, pad=(8, 16, 3))
