@@ -136,6 +136,19 @@ int gemm_force_tile_n(int bn);
 int gemm_last_tile_n(void);
 
 /*
+ * Pin how the tensor-core kernel maps C tiles to SMs for later calls on this
+ * host thread: 1 = one CTA per 128-row tile, 2 = a pair of CTAs (a cluster of
+ * two issuing one 256-row tcgen05 MMA) per 256-row tile, 0 = automatic.  With
+ * 2 only tile widths 128 and 256 exist; a forced width of 192 or 224 makes
+ * the call return GEMM_ERR_UNSUPPORTED.  For A/B measurements and tests.
+ */
+int gemm_force_tc_pair(int mode);
+
+/* 2 if the last tensor-core call on this host thread ran on CTA pairs, 1 if on
+ * single CTAs, 0 if none. */
+int gemm_last_tc_pair(void);
+
+/*
  * Upper bound, in nanoseconds, on any single wait inside a kernel launched
  * later by this process (default 1e9).  After it a kernel records
  * GEMM_ERR_DEVICE_TIMEOUT in the status word and returns.  0 restores the

@@ -32,6 +32,8 @@ thread_local int t_forced_path = GEMM_PATH_AUTO;
 thread_local int t_last_path = GEMM_PATH_AUTO;
 thread_local int t_forced_bn = 0;
 thread_local int t_last_bn = 0;
+thread_local int t_forced_pair = 0;
+thread_local int t_last_pair = 0;
 std::atomic<uint64_t> g_timeout_ns{1000000000ull};
 
 int fail(int code, const char* fmt, ...) {
@@ -229,9 +231,19 @@ int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int 
                          CU_TENSOR_MAP_SWIZZLE_128B, &mB)) != GEMM_OK)
         return rc;
     {
-      const int bn = t_forced_bn ? t_forced_bn : choose_tc_bn(M, N, dev->num_sms);
-      err = launch_bf16_tc(a, mA, mB, bn, dev->num_sms, stream);
-      if (err == cudaSuccess) t_last_bn = bn;
+      int pair = 1, bn = 256;
+      choose_tc_config(M, N, dev->num_sms, &pair, &bn);
+      if (t_forced_pair) pair = t_forced_pair;
+      if (t_forced_bn) bn = t_forced_bn;
+      else if (pair == 2 && bn != 128 && bn != 256) bn = 256;
+      if (pair == 2 && bn != 128 && bn != 256)
+        return fail(GEMM_ERR_UNSUPPORTED, "CTA-pair tiles are 128 or 256 wide, not %d", bn);
+      err = pair == 2 ? launch_bf16_tc_pair(a, mA, mB, bn, dev->num_sms, stream)
+                      : launch_bf16_tc(a, mA, mB, bn, dev->num_sms, stream);
+      if (err == cudaSuccess) {
+        t_last_bn = bn;
+        t_last_pair = pair;
+      }
     }
       break;
     case GEMM_PATH_SKINNY:
@@ -325,6 +337,14 @@ int gemm_force_tile_n(int bn) {
 }
 
 int gemm_last_tile_n(void) { return g3::t_last_bn; }
+
+int gemm_force_tc_pair(int mode) {
+  if (mode < 0 || mode > 2) return g3::fail(GEMM_ERR_INVALID_ARG, "pair mode %d is not 0, 1 or 2", mode);
+  g3::t_forced_pair = mode;
+  return GEMM_OK;
+}
+
+int gemm_last_tc_pair(void) { return g3::t_last_pair; }
 
 int gemm_set_wait_timeout_ns(uint64_t timeout_ns) {
   g3::g_timeout_ns.store(timeout_ns == 0 ? 1000000000ull : timeout_ns);

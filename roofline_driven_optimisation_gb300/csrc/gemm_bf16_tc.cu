@@ -33,6 +33,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "tc_epilogue.cuh"
 
 namespace g3 {
 namespace {
@@ -61,12 +62,6 @@ struct TileCfg {
   static_assert(2 * BN <= TMEM_COLS, "two accumulators must fit in TMEM");
 };
 
-struct TcParams {
-  GemmArgs a;
-  int tiles_m, tiles_n, num_tiles, k_tiles;
-  int c_vec;  // C 16-byte aligned and ldc*sizeof(out) a multiple of 16
-};
-
 template <int BN>
 __device__ __forceinline__ void tile_coords(int tile, const TcParams& p, int& m0, int& n0) {
   const int per_group = RASTER_GROUP * p.tiles_n;
@@ -76,86 +71,6 @@ __device__ __forceinline__ void tile_coords(int tile, const TcParams& p, int& m0
   const int local = tile % per_group;
   m0 = (first_m + local % gsize) * BM;
   n0 = (local / gsize) * BN;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// Epilogue for one row segment of 32 columns: v = alpha*acc (+ beta*C_old).
-template <bool OUT_BF16>
-__device__ __forceinline__ void store_row32(const TcParams& p, long long m, long long n,
-                                            const uint32_t (&r)[32]) {
-  const GemmArgs& a = p.a;
-  float v[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = a.alpha * __uint_as_float(r[j]);
-  const bool beta_nz = a.beta != 0.f;
-  const bool full = p.c_vec && (n + 32 <= a.N);
-  if (OUT_BF16) {
-    __nv_bfloat16* C = static_cast<__nv_bfloat16*>(a.C) + m * a.ldc + n;
-    if (full) {
-      uint4* c4 = reinterpret_cast<uint4*>(C);
-      if (beta_nz) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 old = c4[q];
-          const uint32_t w[4] = {old.x, old.y, old.z, old.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
-            v[q * 8 + 2 * e] = fmaf(a.beta, __low2float(h), v[q * 8 + 2 * e]);
-            v[q * 8 + 2 * e + 1] = fmaf(a.beta, __high2float(h), v[q * 8 + 2 * e + 1]);
-          }
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint4 o;
-        o.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
-        o.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
-        o.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
-        o.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
-        c4[q] = o;
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        if (n + j < a.N) {
-          float x = v[j];
-          if (beta_nz) x = fmaf(a.beta, __bfloat162float(C[j]), x);
-          C[j] = __float2bfloat16_rn(x);
-        }
-      }
-    }
-  } else {
-    float* C = static_cast<float*>(a.C) + m * a.ldc + n;
-    if (full) {
-      float4* c4 = reinterpret_cast<float4*>(C);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        float4 o = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        if (beta_nz) {
-          const float4 old = c4[q];
-          o.x = fmaf(a.beta, old.x, o.x);
-          o.y = fmaf(a.beta, old.y, o.y);
-          o.z = fmaf(a.beta, old.z, o.z);
-          o.w = fmaf(a.beta, old.w, o.w);
-        }
-        c4[q] = o;
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        if (n + j < a.N) {
-          float x = v[j];
-          if (beta_nz) x = fmaf(a.beta, C[j], x);
-          C[j] = x;
-        }
-      }
-    }
-  }
 }
 
 template <int BN, bool OUT_BF16>
@@ -413,6 +328,32 @@ int choose_tc_bn(int M, int N, int num_sms) {
     }
   }
   return best;
+}
+
+// Single CTA or CTA pair, and the tile width: the same wave model over both
+// families.  A pair tile (256 x bn) runs on two SMs, so per SM it is a
+// 128 x bn tile; measured at 8192^3 its per-column cost is 0.882 (bn = 256)
+// and 1.018 (bn = 128) of the single-CTA 256-wide tile.
+void choose_tc_config(int M, int N, int num_sms, int* pair, int* bn) {
+  *pair = 1;
+  *bn = choose_tc_bn(M, N, num_sms);
+  const long long single_tiles = (long long)((M + BM - 1) / BM) * ((N + *bn - 1) / *bn);
+  const long long single_waves = (single_tiles + num_sms - 1) / num_sms;
+  const int single_cost_milli = *bn == 256 ? 1000 : *bn == 192 ? 1012 : 1070;
+  long long best = single_waves * *bn * single_cost_milli;
+  static const int pair_bn[] = {256, 128};
+  static const int pair_cost_milli[] = {882, 1018};
+  const int clusters = num_sms / 2 > 0 ? num_sms / 2 : 1;
+  for (int i = 0; i < 2; ++i) {
+    const long long tiles = (long long)((M + 2 * BM - 1) / (2 * BM)) * ((N + pair_bn[i] - 1) / pair_bn[i]);
+    const long long waves = (tiles + clusters - 1) / clusters;
+    const long long cost = waves * pair_bn[i] * pair_cost_milli[i];
+    if (cost < best) {
+      best = cost;
+      *pair = 2;
+      *bn = pair_bn[i];
+    }
+  }
 }
 
 int launch_bf16_tc(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,

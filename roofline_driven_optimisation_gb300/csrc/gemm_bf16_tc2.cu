@@ -1,0 +1,346 @@
+// BF16 GEMM on a CTA pair: the same computation as gemm_bf16_tc.cu with C
+// tiles of 256 x BN computed by two CTAs (a cluster of two) that issue one
+// M = 256 tcgen05.mma together (cta_group::2).
+//
+// Why: a single CTA computing 128 x 256 moves 48 KB per 64-deep K-stage into
+// shared memory and the MMAs read all of it back.  In the pair each CTA loads
+// its 128 rows of A and only half of B's columns, and the MMA reads A from
+// each CTA and B from both, so every shared-memory and L2 byte feeds twice
+// the FLOPs -- the per-stage A/B intensity of "Kernel 性能从何而来" (section
+// "优化 Memory-Bound Kernel", blocking) rises from 2*128*256/(2*(128+256)) = 85
+// to 2*256*256/(2*2*(128+128)) = 128 FLOP/byte per CTA.  Section "优化阶梯"
+// of the same page names CTA clusters as the step after warp specialisation.
+//
+// Roles (192 threads per CTA, both CTAs): warp 0 = TMA producer (each CTA
+// loads its own A rows and B columns; the copies of both CTAs complete on the
+// leader CTA's barrier), warp 1 = TMEM allocation for the pair and, in the
+// leader only, the single MMA-issuing thread, warps 2-5 = epilogue of the
+// CTA's 128 rows.  The leader's commits arrive on both CTAs' barriers
+// (multicast), and both CTAs' epilogues arrive on the leader's
+// accumulator-empty barrier.  Waits are bounded as in the single-CTA kernel.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tc_epilogue.cuh"
+
+namespace g3 {
+namespace {
+
+constexpr int BM_CTA = kTcBM;    // rows per CTA
+constexpr int BM = 2 * BM_CTA;   // rows per pair tile
+constexpr int BK = kTcBK;
+constexpr int UMMA_K = 16;
+constexpr int A_STAGE_BYTES = BM_CTA * BK * 2;   // 16 KB
+constexpr int B_BOX_BYTES = 64 * BK * 2;         // 8 KB (64 n x 64 k)
+constexpr int TMEM_COLS = 512;
+constexpr int NUM_EPI_WARPS = 4;
+constexpr int THREADS = 64 + NUM_EPI_WARPS * 32;
+constexpr int BAR_BYTES = 256;
+constexpr int SMEM_LIMIT = 232448;
+constexpr int RASTER_GROUP = 8;
+constexpr uint64_t kDrainGraceNs = 50000;        // after an abort, time for the peer's copies to land
+constexpr uint16_t kBothCtas = 0x3;
+
+template <int BN>
+struct PairCfg {
+  static_assert(BN == 128 || BN == 256, "each CTA loads whole 64-column boxes of B");
+  static constexpr int B_BOXES = BN / 2 / 64;
+  static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_BOXES * B_BOX_BYTES;  // per CTA
+  static constexpr int STAGES_FIT = (SMEM_LIMIT - BAR_BYTES - 1024) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+};
+
+template <int BN>
+__device__ __forceinline__ void pair_tile_coords(int tile, const TcParams& p, int& m0, int& n0) {
+  const int per_group = RASTER_GROUP * p.tiles_n;
+  const int g = tile / per_group;
+  const int first_m = g * RASTER_GROUP;
+  const int gsize = min(p.tiles_m - first_m, RASTER_GROUP);
+  const int local = tile % per_group;
+  m0 = (first_m + local % gsize) * BM;
+  n0 = (local / gsize) * BN;
+}
+
+template <int BN, bool OUT_BF16>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_bf16_tc2_kernel(const __grid_constant__ CUtensorMap mapA,
+                         const __grid_constant__ CUtensorMap mapB, const TcParams p) {
+  using Cfg = PairCfg<BN>;
+  constexpr int STAGES = Cfg::STAGES;
+  constexpr int STAGE_BYTES = Cfg::STAGE_BYTES;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  // Same offsets in both CTAs: the paired MMA reads A and B at the
+  // descriptor's address in each CTA of the pair.
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t bar_base = base + STAGES * STAGE_BYTES;
+  uint8_t* bar_ptr = base_ptr + STAGES * STAGE_BYTES;
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar_base + 8u * (2 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar_base + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_ptr + 8 * (2 * STAGES + 5));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_ptr + 8 * (2 * STAGES + 5) + 8);
+  auto a_tile = [&](int s) { return base + s * STAGE_BYTES; };
+  auto b_tile = [&](int s) { return base + s * STAGE_BYTES + A_STAGE_BYTES; };
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const GemmArgs& a = p.a;
+  const uint32_t rank = cluster_ctarank() & 1u;  // clusters hold exactly one pair
+  const bool leader = rank == 0;
+  const int cluster_id = blockIdx.x >> 1;
+  const int num_clusters = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 2 * NUM_EPI_WARPS * 32);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();  // barriers initialised and TMEM allocated in both CTAs
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (elect_one_sync()) {
+      tma_prefetch_desc(&mapA);
+      tma_prefetch_desc(&mapB);
+      uint32_t issued = 0, issued_par = 0;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
+        int m0, n0;
+        pair_tile_coords<BN>(tile, p, m0, n0);
+        const int a_row = m0 + (int)rank * BM_CTA;
+        const int b_col = n0 + (int)rank * (BN / 2);
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, a.timeout_ns, abort_flag)) {
+            if (!*abort_flag) report_status(a.status, 5, kSiteTc2Producer);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          // both CTAs' copies of this stage complete on the leader's barrier
+          const uint32_t lead_full = map_to_rank(full_bar(stage), 0);
+          if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * STAGE_BYTES);
+          tma_load_2d_pair(a_tile(stage), &mapA, lead_full, kt * BK, a_row);
+#pragma unroll
+          for (int j = 0; j < Cfg::B_BOXES; ++j)
+            tma_load_2d_pair(b_tile(stage) + j * B_BOX_BYTES, &mapB, lead_full, b_col + j * 64,
+                             kt * BK);
+          issued |= 1u << stage;
+          issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (*abort_flag) {
+        if (leader) {
+          for (int s = 0; s < STAGES; ++s)
+            if (((issued >> s) & 1u) &&
+                !mbar_wait(full_bar(s), (issued_par >> s) & 1u, a.timeout_ns, nullptr))
+              report_status(a.status, 5, kSiteTc2Drain);
+        }
+        // the peer's copies complete on a barrier this CTA cannot wait on:
+        // give them a bounded grace period before shared memory is released
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < kDrainGraceNs) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (leader)
+    if (leader) {
+      if (elect_one_sync()) {
+        constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, /*A K-major*/ 0, /*B MN-major*/ 1);
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true, issued_any = false;
+        for (int tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
+          if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, a.timeout_ns, abort_flag)) {
+            if (!*abort_flag) report_status(a.status, 5, kSiteTc2Mma);
+            *abort_flag = 1;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+          for (int kt = 0; kt < p.k_tiles; ++kt) {
+            if (!mbar_wait(full_bar(stage), phase, a.timeout_ns, abort_flag)) {
+              if (!*abort_flag) report_status(a.status, 5, kSiteTc2Mma);
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+              const uint64_t adesc = smem_desc_sw128(a_tile(stage) + kk * UMMA_K * 2, 16, 1024);
+              const uint64_t bdesc =
+                  smem_desc_sw128(b_tile(stage) + kk * UMMA_K * 128, B_BOX_BYTES, 1024);
+              tc_mma_f16_pair(d_tmem, adesc, bdesc, idesc, (kt | kk) != 0 ? 1u : 0u);
+            }
+            issued_any = true;
+            tc_commit_pair_mc(empty_bar(stage), kBothCtas);  // frees the stage in both CTAs
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          tc_commit_pair_mc(tfull_bar(acc), kBothCtas);  // both halves of D are ready
+          if (++acc == 2) {
+            acc = 0;
+            acc_phase ^= 1u;
+          }
+        }
+        if (*abort_flag && issued_any) {
+          tc_commit_pair_mc(drain_bar, 0x1);
+          if (!mbar_wait(drain_bar, 0, a.timeout_ns, nullptr)) report_status(a.status, 5, kSiteTc2Drain);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp % 4;
+    const uint32_t lead_tempty0 = map_to_rank(tempty_bar(0), 0);
+    const uint32_t lead_tempty1 = map_to_rank(tempty_bar(1), 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = cluster_id; tile < p.num_tiles; tile += num_clusters) {
+      int m0, n0;
+      pair_tile_coords<BN>(tile, p, m0, n0);
+      if (!mbar_wait(tfull_bar(acc), acc_phase, a.timeout_ns, abort_flag)) {
+        if (!*abort_flag) report_status(a.status, 5, kSiteTc2Epilogue);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const long long m = (long long)m0 + rank * BM_CTA + quarter * 32 + lane;
+      const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_row + c * 32, r);
+        tc_wait_ld();
+        if (c == BN / 32 - 1) {
+          tc_fence_before();
+          mbar_arrive_remote(acc == 0 ? lead_tempty0 : lead_tempty1);
+        }
+        if (m < a.M && n0 + c * 32 < a.N) store_row32<OUT_BF16>(p, m, (long long)n0 + c * 32, r);
+      }
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync();  // both CTAs are done with the pair's TMEM and barriers
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
+struct PairLaunchInfo {
+  bool ready = false;
+  int max_clusters = 0;
+};
+
+template <int BN, bool OUT_BF16>
+int launch_pair_impl(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
+                     int num_sms, cudaStream_t s) {
+  using Cfg = PairCfg<BN>;
+  static PairLaunchInfo info[64];
+  static std::mutex mu;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  auto kernel = gemm_bf16_tc2_kernel<BN, OUT_BF16>;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (!info[dev].ready) {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!info[dev].ready) {
+      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           Cfg::SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+      // clusters that can be resident at once (GPCs with an odd number of
+      // free SMs leave one idle), so the persistent grid never has a tail
+      int n = 0;
+      cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+      e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+      if (e != cudaSuccess) return e;
+      info[dev].max_clusters = n > 0 ? n : 1;
+      info[dev].ready = true;
+    }
+  }
+  TcParams p;
+  p.a = a;
+  p.tiles_m = (a.M + BM - 1) / BM;
+  p.tiles_n = (a.N + BN - 1) / BN;
+  const long long tiles = (long long)p.tiles_m * p.tiles_n;
+  if (tiles <= 0) return cudaSuccess;
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  p.num_tiles = (int)tiles;
+  p.k_tiles = (a.K + BK - 1) / BK;
+  const int out_bytes = OUT_BF16 ? 2 : 4;
+  p.c_vec = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && ((a.ldc * out_bytes) % 16) == 0) ? 1 : 0;
+  const int clusters = (int)(tiles < info[dev].max_clusters ? tiles : info[dev].max_clusters);
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, *mapA, *mapB, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int launch_bf16_tc_pair(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB, int bn,
+                        int num_sms, cudaStream_t s) {
+  const bool bf16 = a.out == Elem::BF16;
+  if (bn == 256)
+    return bf16 ? launch_pair_impl<256, true>(a, mapA, mapB, num_sms, s)
+                : launch_pair_impl<256, false>(a, mapA, mapB, num_sms, s);
+  if (bn == 128)
+    return bf16 ? launch_pair_impl<128, true>(a, mapA, mapB, num_sms, s)
+                : launch_pair_impl<128, false>(a, mapA, mapB, num_sms, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace g3

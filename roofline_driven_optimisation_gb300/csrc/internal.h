@@ -31,6 +31,10 @@ enum WaitSite : int {
   kSiteTcMma = 11,
   kSiteTcEpilogue = 12,
   kSiteTcDrain = 13,
+  kSiteTc2Producer = 14,
+  kSiteTc2Mma = 15,
+  kSiteTc2Epilogue = 16,
+  kSiteTc2Drain = 17,
   kSiteSimtProducer = 20,
   kSiteSimtConsumer = 21,
   kSiteSimtDrain = 22,
@@ -52,9 +56,17 @@ constexpr int kSimtBM = 128, kSimtBN = 128, kSimtBK = 16;
 // BF16 tcgen05 kernel: TMA tiles of A (64 k x 128 m) and B (64 n x 64 k),
 // 128-byte swizzle; C tiles of 128 x bn with bn from choose_tc_bn().
 int choose_tc_bn(int M, int N, int num_sms);
+// Single CTA (pair = 1) or CTA pair (pair = 2) and the tile width.
+void choose_tc_config(int M, int N, int num_sms, int* pair, int* bn);
 int launch_bf16_tc(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB, int bn,
                    int num_sms, cudaStream_t s);
 constexpr int kTcBM = 128, kTcBK = 64;
+
+// The same GEMM on CTA pairs (clusters of two, cta_group::2): C tiles of
+// 256 x bn, bn in {128, 256}; each CTA loads 128 rows of A and bn/2 columns
+// of B with the same tensor maps as the single-CTA kernel.
+int launch_bf16_tc_pair(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB, int bn,
+                        int num_sms, cudaStream_t s);
 
 // Skinny (M <= 16) split-K kernel: TMA tiles of B (64 n x 64 k) and A
 // (64 k x 16 rows), 128-byte swizzle.

@@ -138,15 +138,83 @@ def test_bf16_tc_every_tile_width(cuda_lib, bn, M, N, K):
         g.force_tile_n(0)
 
 
+@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("M,N,K", [(17, 64, 64), (100, 304, 136), (256, 256, 64), (300, 1000, 200),
+                                   (520, 640, 1000), (1024, 2048, 256)])
+def test_bf16_tc_pair(cuda_lib, bn, M, N, K):
+    c = inputs.make("decode_m16_o", M=M, N=N, K=K)
+    g.force_tc_pair(2)
+    g.force_tile_n(bn)
+    try:
+        for out, alpha, beta in ((BF16, 1.0, 0.0), (F32, 1.5, 0.5)):
+            err, path = check(c.A, c.B, c.C0, alpha, beta, out)
+            assert path == g.PATH_BF16_TC and g.last_tc_pair() == 2 and g.last_tile_n() == bn
+    finally:
+        g.force_tc_pair(0)
+        g.force_tile_n(0)
+
+
+def test_bf16_tc_pair_deterministic_and_matches_single(cuda_lib):
+    c = inputs.make("bf16_4096", M=768, N=1024, K=512)
+    g.force_tc_pair(2)
+    try:
+        a = run_abi(c.A, c.B, None, 1.0, 0.0, F32)[0]
+        b = run_abi(c.A, c.B, None, 1.0, 0.0, F32)[0]
+    finally:
+        g.force_tc_pair(0)
+    assert torch.equal(a, b)
+    g.force_tc_pair(1)
+    try:
+        s1 = run_abi(c.A, c.B, None, 1.0, 0.0, F32)[0]
+    finally:
+        g.force_tc_pair(0)
+    # same products, same k order inside each 16-deep MMA step: agree to fp32 rounding
+    assert torch.allclose(a, s1, rtol=1e-5, atol=1e-6)
+
+
+def test_bf16_tc_pair_rejects_other_widths(cuda_lib):
+    c = inputs.make("bf16_4096", M=256, N=256, K=64)
+    g.force_tc_pair(2)
+    g.force_tile_n(192)
+    try:
+        with pytest.raises(g.GemmError) as e:
+            run_abi(c.A, c.B, None, 1.0, 0.0, BF16)
+        assert e.value.code == g.GEMM_ERR_UNSUPPORTED
+    finally:
+        g.force_tc_pair(0)
+        g.force_tile_n(0)
+    with pytest.raises(g.GemmError):
+        g.force_tc_pair(3)
+
+
+@pytest.mark.parametrize("out", [BF16, F32])
+def test_bf16_tc_pair_8192_sampled(cuda_lib, out):
+    c = inputs.make("bf16_8192")
+    A, B = c.A.cuda(), c.B.cuda()
+    C = torch.full((8192, 8192), float("nan"), dtype=out, device="cuda")
+    g.force_tc_pair(2)
+    try:
+        g.gemm(A, B, C, 1.0, 0.0)
+        torch.cuda.synchronize()
+        assert g.last_tc_pair() == 2
+    finally:
+        g.force_tc_pair(0)
+    gen = np.random.default_rng(7)
+    rows = np.sort(gen.choice(8192, 12, replace=False))
+    cols = np.sort(gen.choice(8192, 12, replace=False))
+    tol = oracle.TOL_BF16_OUT if out == BF16 else oracle.TOL_BF16_F32OUT
+    sampled_check(A, B, C, c.A, c.B, None, 1.0, 0.0, tol, rows, cols)
+
+
 def test_bf16_tc_tile_width_choice(cuda_lib):
-    # 8192^3 on 152 SMs: 256-wide tiles; 4096 x 4096: 128-wide tiles (7 waves
-    # of 128 cost less than 4 of 256 with the last one a third full)
+    # on 152 SMs: square 4096 and 8192 run on CTA pairs with 256 x 256 tiles;
+    # a 128-row GEMM runs on single CTAs (more tiles than pairs would give)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    for n, want in ((8192, 256), (4096, 128)):
-        c = inputs.make("bf16_4096", M=n, N=n, K=64)
+    for M, N, want in ((8192, 8192, (2, 256)), (4096, 4096, (2, 256)), (128, 4096, (1, 128))):
+        c = inputs.make("bf16_4096", M=M, N=N, K=64)
         check(c.A, c.B, None, 1.0, 0.0, BF16)
         if sms == 152:
-            assert g.last_tile_n() == want, (n, g.last_tile_n())
+            assert (g.last_tc_pair(), g.last_tile_n()) == want, (M, N)
     with pytest.raises(g.GemmError):
         g.force_tile_n(100)
 
