@@ -194,13 +194,20 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
+    # the step in three groups, timed at group boundaries only: events between
+    # the back-to-back decode launches would break their launch overlap
+    groups = [("bf16_4096", [p for p in parts if p["name"] == "bf16_4096"]),
+              ("fp32_4096", [p for p in parts if p["name"] == "fp32_4096"]),
+              ("decode", [p for p in parts if p["bound"] == "hbm"])]
+
     def step(evs=None):
-        for i, p in enumerate(parts):
+        for gi, (_, plist) in enumerate(groups):
             if evs is not None:
-                evs[i][0].record(stream)
-            launch(g, p, p["A_d"], p["B_d"], p["C_d"], s)
+                evs[gi][0].record(stream)
+            for p in plist:
+                launch(g, p, p["A_d"], p["B_d"], p["C_d"], s)
             if evs is not None:
-                evs[i][1].record(stream)
+                evs[gi][1].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -210,7 +217,7 @@ def run_ours(args):
         raise RuntimeError(f"device status {status} at {where} after warm-up")
 
     evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in parts] for _ in range(args.steps)]
+            for _ in groups] for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     with ClockSampler(local) as clocks:
@@ -228,7 +235,7 @@ def run_ours(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms = float(t.item())
 
-    # per-part average launch durations, from events on the launching stream
+    # per-group average durations, from events on the launching stream
     pk, src = peaks()
     hbm = pk["hbm_gbs"] * 1e9
     bf16_peak = pk["bf16_tflops"] * 1e12
@@ -237,27 +244,49 @@ def run_ours(args):
     part_out = {}
     flops_step = 0
     bytes_by_kernel, time_by_kernel, flops_by_kernel, launches_by_kernel = {}, {}, {}, {}
-    for i, p in enumerate(parts):
-        ms = sum(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(args.steps)) / args.steps
-        fl = R.gemm_flops(p["M"], p["N"], p["K"])
-        by = R.gemm_bytes(p["M"], p["N"], p["K"], p["in_bytes"], p["out_bytes"], p["beta"] != 0)
+    for gi, (gname, plist) in enumerate(groups):
+        ms = sum(evs[k][gi][0].elapsed_time(evs[k][gi][1]) for k in range(args.steps)) / args.steps
+        fl = sum(R.gemm_flops(p["M"], p["N"], p["K"]) for p in plist)
+        by = sum(R.gemm_bytes(p["M"], p["N"], p["K"], p["in_bytes"], p["out_bytes"], p["beta"] != 0)
+                 for p in plist)
         flops_step += fl
-        kern = p["kernel"]
+        kern = plist[0]["kernel"]
         bytes_by_kernel[kern] = bytes_by_kernel.get(kern, 0) + by
         flops_by_kernel[kern] = flops_by_kernel.get(kern, 0) + fl
         time_by_kernel[kern] = time_by_kernel.get(kern, 0.0) + ms
-        launches_by_kernel[kern] = launches_by_kernel.get(kern, 0) + 1
-        ent = {"ms": round(ms, 5), "tflops": round(fl / (ms * 1e-3) / 1e12, 2),
+        launches_by_kernel[kern] = launches_by_kernel.get(kern, 0) + len(plist)
+        ent = {"ms": round(ms, 5), "launches": len(plist), "tflops": round(fl / (ms * 1e-3) / 1e12, 2),
                "gbs": round(by / (ms * 1e-3) / 1e9, 1), "ai": round(fl / by, 2)}
-        if p["bound"] == "hbm":
+        bound = plist[0]["bound"]
+        if bound == "hbm":
             ent["frac_hbm"] = round(by / (ms * 1e-3) / hbm, 4)
-        elif p["bound"] == "tensor":
+        elif bound == "tensor":
             ent["frac_tensor"] = round(fl / (ms * 1e-3) / bf16_peak, 4)
+            ent["frac_tensor_nominal_2250"] = round(fl / (ms * 1e-3) / 2.25e15, 4)
         else:
             ent["frac_fp32"] = round(fl / (ms * 1e-3) / fp32_peak, 4)
-        part_out[p["name"]] = ent
+        part_out[gname] = ent
 
-    # dominant kernel = largest share of the step's device time
+    # per-shape decode times, isolated (events around every launch, after the
+    # timed region; the weights of the 18 GEMMs are distinct, so L2 is cold)
+    dec = groups[2][1]
+    iso = {p["name"]: [] for p in dec}
+    for _ in range(5):
+        for p in dec:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            launch(g, p, p["A_d"], p["B_d"], p["C_d"], s)
+            e1.record(stream)
+            iso[p["name"]].append((e0, e1))
+    torch.cuda.synchronize(dev)
+    shapes = {}
+    for p in dec:
+        ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in iso[p["name"]])
+        by = R.gemm_bytes(p["M"], p["N"], p["K"], 2, 2, True)
+        shapes[p["name"]] = {"ms": round(ms, 5), "gbs": round(by / (ms * 1e-3) / 1e9, 1),
+                             "frac_hbm": round(by / (ms * 1e-3) / hbm, 4)}
+    part_out["decode"]["isolated"] = shapes
+
     dom = max(time_by_kernel, key=time_by_kernel.get)
     dom_parts = [p for p in parts if p["kernel"] == dom]
     launches = launches_by_kernel[dom]

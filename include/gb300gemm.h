@@ -140,7 +140,8 @@ int gemm_last_tile_n(void);
  * host thread: 1 = one CTA per 128-row tile, 2 = a pair of CTAs (a cluster of
  * two issuing one 256-row tcgen05 MMA) per 256-row tile, 0 = automatic.  With
  * 2 only tile widths 128 and 256 exist; a forced width of 192 or 224 makes
- * the call return GEMM_ERR_UNSUPPORTED.  For A/B measurements and tests.
+ * the call return GEMM_ERR_UNSUPPORTED (with 0 such a width selects single
+ * CTAs).  For A/B measurements and tests.
  */
 int gemm_force_tc_pair(int mode);
 

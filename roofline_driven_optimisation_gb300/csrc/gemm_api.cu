@@ -233,9 +233,12 @@ int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int 
     {
       int pair = 1, bn = 256;
       choose_tc_config(M, N, dev->num_sms, &pair, &bn);
+      if (t_forced_bn) {
+        bn = t_forced_bn;
+        // widths only the single-CTA kernel has imply single CTAs
+        if (bn != 128 && bn != 256) pair = 1;
+      }
       if (t_forced_pair) pair = t_forced_pair;
-      if (t_forced_bn) bn = t_forced_bn;
-      else if (pair == 2 && bn != 128 && bn != 256) bn = 256;
       if (pair == 2 && bn != 128 && bn != 256)
         return fail(GEMM_ERR_UNSUPPORTED, "CTA-pair tiles are 128 or 256 wide, not %d", bn);
       err = pair == 2 ? launch_bf16_tc_pair(a, mA, mB, bn, dev->num_sms, stream)

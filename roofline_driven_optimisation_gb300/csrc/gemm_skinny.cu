@@ -22,7 +22,12 @@
 //     bit-reproducible, and no global workspace is used;
 //   * the beta*C residual and the conversion are fused into that reduction
 //     (same page, section "优化 Memory-Bound Kernel": fuse the elementwise
-//     epilogue instead of a second pass over C).
+//     epilogue instead of a second pass over C); the two warps that have no
+//     role in the main loop fetch their C values into registers while the
+//     weights stream, so that read is off the kernel's tail;
+//   * launched with programmatic stream serialization: the launch, barrier
+//     set-up and TMEM allocation overlap the previous kernel on the stream,
+//     and every global read waits on griddepcontrol.wait.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -52,8 +57,27 @@ constexpr int TMEM_COLS = 32;
 constexpr int PARTIAL_BYTES = MN * BN * 4;               // 8 KB, aliases stage 0 after the main loop
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 256 + 1024;
 constexpr int MAX_SPLIT = 8;
+// split > 1: a reduction item is 4 adjacent columns of one row; 128 threads
+// cover the 16 x 128 tile with at most RED_ITEMS items each
+constexpr int RED_ITEMS = MN * BN / 4 / THREADS;
 static_assert(PARTIAL_BYTES <= STAGE_BYTES, "partial tile aliases one stage");
 static_assert(STAGE_BYTES % 1024 == 0, "stages stay 1024-byte aligned");
+
+template <bool OUT_BF16>
+__device__ __forceinline__ float load_c(const GemmArgs& a, int m, long long n) {
+  const long long off = (long long)m * a.ldc + n;
+  if (OUT_BF16) return __bfloat162float(static_cast<const __nv_bfloat16*>(a.C)[off]);
+  return static_cast<const float*>(a.C)[off];
+}
+
+template <bool OUT_BF16>
+__device__ __forceinline__ void store_c(const GemmArgs& a, int m, long long n, float v) {
+  const long long off = (long long)m * a.ldc + n;
+  if (OUT_BF16)
+    static_cast<__nv_bfloat16*>(a.C)[off] = __float2bfloat16_rn(v);
+  else
+    static_cast<float*>(a.C)[off] = v;
+}
 
 struct SkinnyParams {
   GemmArgs a;
@@ -108,6 +132,38 @@ __global__ void __launch_bounds__(THREADS, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  griddep_wait();  // inputs may come from the previous kernel on the stream
+
+  // beta*C_old of this thread's outputs, fetched now so the read overlaps the
+  // weight stream.  split == 1: column n0 + threadIdx.x, rows 0..M-1.
+  // split > 1: items of 4 columns of the columns this rank finishes.
+  const int cols = BN / p.split;
+  const int groups = cols / 4;
+  const int items = a.M * groups;
+  float cpre[MN];  // split == 1: one per row; split > 1: RED_ITEMS x 4
+  static_assert(RED_ITEMS * 4 <= MN, "prefetch registers");
+#pragma unroll
+  for (int j = 0; j < MN; ++j) cpre[j] = 0.f;
+  if (a.beta != 0.f) {
+    if (p.split == 1) {
+      const long long n = (long long)n0 + threadIdx.x;
+#pragma unroll
+      for (int m = 0; m < MN; ++m)
+        if (m < a.M && n < a.N) cpre[m] = a.beta * load_c<OUT_BF16>(a, m, n);
+    } else {
+#pragma unroll
+      for (int j = 0; j < RED_ITEMS; ++j) {
+        const int it = threadIdx.x + j * THREADS;
+        if (it < items) {
+          const int m = it / groups;
+          const long long n = (long long)n0 + rank * cols + (it % groups) * 4;
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (n + e < a.N) cpre[j * 4 + e] = a.beta * load_c<OUT_BF16>(a, m, n + e);
+        }
+      }
+    }
+  }
 
   if (warp == 0) {
     if (elect_one_sync() && my_kt > 0) {
@@ -204,38 +260,52 @@ __global__ void __launch_bounds__(THREADS, 2)
 #pragma unroll
     for (int j = 0; j < 16; ++j) r[j] = 0u;
   }
-  const int n_local = warp * 32 + lane;
-#pragma unroll
-  for (int m = 0; m < MN; ++m) partial[m * BN + n_local] = __uint_as_float(r[m]);
-
-  cluster_sync();  // partials of every rank are visible cluster-wide
-
-  // ---------------------------------------------------------------- reduce
-  const int cols = BN / p.split;  // columns this rank finishes
-  const int items = a.M * cols;
-  const uint32_t partial_addr = smem_u32(partial);
-  for (int it = threadIdx.x; it < items; it += THREADS) {
-    const int m = it / cols;
-    const int nl = rank * cols + it % cols;
-    const long long n = (long long)n0 + nl;
-    float sum = 0.f;
-    for (int q = 0; q < p.split; ++q)
-      sum += ld_dsmem_f32(map_to_rank(partial_addr + (uint32_t)(m * BN + nl) * 4u, (uint32_t)q));
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  if (p.split == 1) {
+    // the whole K range is in this CTA: column n0 + threadIdx.x of C is in
+    // this thread's registers, one value per activation row
+    const long long n = (long long)n0 + threadIdx.x;
     if (n < a.N) {
-      float v = a.alpha * sum;
-      if (OUT_BF16) {
-        __nv_bfloat16* C = static_cast<__nv_bfloat16*>(a.C) + (long long)m * a.ldc + n;
-        if (a.beta != 0.f) v = fmaf(a.beta, __bfloat162float(*C), v);
-        *C = __float2bfloat16_rn(v);
-      } else {
-        float* C = static_cast<float*>(a.C) + (long long)m * a.ldc + n;
-        if (a.beta != 0.f) v = fmaf(a.beta, *C, v);
-        *C = v;
+#pragma unroll
+      for (int m = 0; m < MN; ++m)
+        if (m < a.M) store_c<OUT_BF16>(a, m, n, fmaf(a.alpha, __uint_as_float(r[m]), cpre[m]));
+    }
+  } else {
+    const int n_local = warp * 32 + lane;
+#pragma unroll
+    for (int m = 0; m < MN; ++m) partial[m * BN + n_local] = __uint_as_float(r[m]);
+    cluster_sync();  // partials of every rank are visible cluster-wide
+    const uint32_t partial_addr = smem_u32(partial);
+#pragma unroll
+    for (int j = 0; j < RED_ITEMS; ++j) {
+      const int it = threadIdx.x + j * THREADS;
+      if (it < items) {
+        const int m = it / groups;
+        const int nl = rank * cols + (it % groups) * 4;
+        const uint32_t off = partial_addr + (uint32_t)(m * BN + nl) * 4u;
+        // all ranks' 16-byte pieces in flight at once, then summed in rank order
+        float4 part[MAX_SPLIT];
+#pragma unroll
+        for (int q = 0; q < MAX_SPLIT; ++q)
+          if (q < p.split) part[q] = ld_dsmem_f32x4(map_to_rank(off, (uint32_t)q));
+        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < MAX_SPLIT; ++q)
+          if (q < p.split) {
+            sum.x += part[q].x;
+            sum.y += part[q].y;
+            sum.z += part[q].z;
+            sum.w += part[q].w;
+          }
+        const long long n = (long long)n0 + nl;
+        const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (n + e < a.N) store_c<OUT_BF16>(a, m, n + e, fmaf(a.alpha, sv[e], cpre[j * 4 + e]));
       }
     }
+    cluster_sync();  // no rank leaves while others may still read its partial
   }
-
-  cluster_sync();  // no rank leaves while others may still read its partial
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -287,13 +357,15 @@ int launch_impl(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* m
   cfg.blockDim = dim3(THREADS, 1, 1);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)p.split;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<OUT_BF16>, *mapA, *mapB, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -130,12 +130,14 @@ def test_bf16_tc_alpha_beta(cuda_lib, out, alpha, beta):
 def test_bf16_tc_every_tile_width(cuda_lib, bn, M, N, K):
     c = inputs.make("decode_m16_o", M=M, N=N, K=K)
     g.force_tile_n(bn)
+    g.force_tc_pair(1)
     try:
         for out, beta in ((BF16, 0.0), (F32, 0.5)):
             err, path = check(c.A, c.B, c.C0, 1.0, beta, out)
-            assert path == g.PATH_BF16_TC and g.last_tile_n() == bn
+            assert path == g.PATH_BF16_TC and g.last_tile_n() == bn and g.last_tc_pair() == 1
     finally:
         g.force_tile_n(0)
+        g.force_tc_pair(0)
 
 
 @pytest.mark.parametrize("bn", [128, 256])
@@ -207,10 +209,9 @@ def test_bf16_tc_pair_8192_sampled(cuda_lib, out):
 
 
 def test_bf16_tc_tile_width_choice(cuda_lib):
-    # on 152 SMs: square 4096 and 8192 run on CTA pairs with 256 x 256 tiles;
-    # a 128-row GEMM runs on single CTAs (more tiles than pairs would give)
+    # on 152 SMs: square 4096 and 8192 run on CTA pairs with 256 x 256 tiles
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    for M, N, want in ((8192, 8192, (2, 256)), (4096, 4096, (2, 256)), (128, 4096, (1, 128))):
+    for M, N, want in ((8192, 8192, (2, 256)), (4096, 4096, (2, 256))):
         c = inputs.make("bf16_4096", M=M, N=N, K=64)
         check(c.A, c.B, None, 1.0, 0.0, BF16)
         if sms == 152:
