@@ -47,9 +47,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per launch measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum)
 # for each kernel source file, valid only while the file hashes to `sha256`.
 NCU_TRAFFIC = {
-    # profiles/sgemm_tma_kernel_fp32_4096.md: 425.7 MB read + 56.4 MB written
-    "gemm_f32_simt.cu": {"sha256": "e2d4e4fff5d5e3707ad8cd3347fa0d420cd77d411fdf96feaedca8e614e039a7",
-                         "bytes_per_launch": 482115328},
+    # profiles/sgemm_tma_kernel_fp32_4096.md: 401.4 MB read + 54.9 MB written
+    "gemm_f32_simt.cu": {"sha256": "87ac9ecf4c07e6b29f5f32afd5b958500f4db663cf7b79b70258665ea1022c23",
+                         "bytes_per_launch": 456229376},
+    # profiles/gemm_bf16_tc2_kernel_bf16_8192.md, 4096^3 capture: 79.0 MB + 10.9 MB
+    "gemm_bf16_tc2.cu": {"sha256": "cb432567274a20e7291c74dff303f440d1294fe655ca5f252f55d519c9d6215c",
+                         "bytes_per_launch": 89855744},
 }
 
 
@@ -188,6 +191,17 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     s = stream.cuda_stream
     n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    # label each part with the kernel source the dispatcher actually runs
+    files = {g.PATH_F32_SIMT: "gemm_f32_simt.cu", g.PATH_SKINNY: "gemm_skinny.cu",
+             g.PATH_GENERIC: "gemm_generic.cu"}
+    for p in parts:
+        launch(g, p, p["A_d"], p["B_d"], p["C_d"], s)
+        path = g.last_path()
+        if path == g.PATH_BF16_TC:
+            p["kernel"] = "gemm_bf16_tc2.cu" if g.last_tc_pair() == 2 else "gemm_bf16_tc.cu"
+        else:
+            p["kernel"] = files[path]
+    torch.cuda.synchronize(dev)
 
     def barrier():
         if world > 1:
