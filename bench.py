@@ -171,6 +171,7 @@ def run_ours(args):
     import torch
     import torch.distributed as dist
     import roofline_driven_optimisation_gb300 as g
+    from roofline_driven_optimisation_gb300 import replicas
     from roofline_driven_optimisation_gb300 import roofline as R
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -244,10 +245,7 @@ def run_ours(args):
     status, where = g.device_status(s)
     if status != 0:
         raise RuntimeError(f"device status {status} at {where} in the timed region")
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = replicas.max_over_ranks(elapsed_ms, dist if world > 1 else None, device=dev)
 
     # per-group average durations, from events on the launching stream
     pk, src = peaks()
@@ -325,7 +323,7 @@ def run_ours(args):
                 "algorithmic_flops_per_launch": int(flops_by_kernel[dom] / launches)}
 
     ms_step = elapsed_ms / args.steps
-    value = world * flops_step / (ms_step * 1e-3) / 1e12
+    value = replicas.whole_job_rate(flops_step, world, ms_step * 1e-3) / 1e12
     e2e = run_e2e(args, g, torch, dev, parts, s, world)
 
     result = {
