@@ -145,9 +145,18 @@ int gemm_last_tile_n(void);
  */
 int gemm_force_tc_pair(int mode);
 
-/* 2 if the last tensor-core call on this host thread ran on CTA pairs, 1 if on
- * single CTAs, 0 if none. */
+/* For the last tensor-core call on this host thread: 1 if it ran on single
+ * CTAs, 2 on CTA pairs, 4 on CTA pairs with the tiles of the last partial
+ * wave split into half-width tiles, 0 if there was none. */
 int gemm_last_tc_pair(void);
+
+/*
+ * Allow (1, the default) or forbid (0), for later calls on this host thread,
+ * that the CTA-pair kernel runs the tiles of a partial last wave as two
+ * half-width tiles each, on otherwise idle pairs.  For A/B measurements and
+ * tests.
+ */
+int gemm_force_split_tiles(int enable);
 
 /*
  * Upper bound, in nanoseconds, on any single wait inside a kernel launched

@@ -38,7 +38,7 @@ PATH_NAMES = {PATH_AUTO: "none", PATH_GENERIC: "generic", PATH_F32_SIMT: "f32_si
 # every symbol the public header declares
 EXPORTS = ("gemm_f32", "gemm_bf16", "gemm_bf16_f32out", "gemm_get_last_error",
            "gemm_device_status", "gemm_force_path", "gemm_last_path", "gemm_force_tile_n",
-           "gemm_last_tile_n", "gemm_force_tc_pair", "gemm_last_tc_pair",
+           "gemm_last_tile_n", "gemm_force_tc_pair", "gemm_last_tc_pair", "gemm_force_split_tiles",
            "gemm_set_wait_timeout_ns", "gemm_selftest_wait_timeout")
 
 _lib = None
@@ -90,6 +90,8 @@ def load(path: str | None = None):
         lib.gemm_force_tc_pair.restype = i
         lib.gemm_last_tc_pair.argtypes = []
         lib.gemm_last_tc_pair.restype = i
+        lib.gemm_force_split_tiles.argtypes = [i]
+        lib.gemm_force_split_tiles.restype = i
         lib.gemm_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
         lib.gemm_set_wait_timeout_ns.restype = i
         lib.gemm_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
@@ -145,6 +147,10 @@ def force_tc_pair(mode: int):
 
 def last_tc_pair() -> int:
     return load().gemm_last_tc_pair()
+
+
+def force_split_tiles(enable: int):
+    _check(load().gemm_force_split_tiles(enable))
 
 
 def set_wait_timeout_ns(ns: int):

@@ -34,6 +34,7 @@ thread_local int t_forced_bn = 0;
 thread_local int t_last_bn = 0;
 thread_local int t_forced_pair = 0;
 thread_local int t_last_pair = 0;
+thread_local int t_split_tiles = 1;
 std::atomic<uint64_t> g_timeout_ns{1000000000ull};
 
 int fail(int code, const char* fmt, ...) {
@@ -241,11 +242,12 @@ int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int 
       if (t_forced_pair) pair = t_forced_pair;
       if (pair == 2 && bn != 128 && bn != 256)
         return fail(GEMM_ERR_UNSUPPORTED, "CTA-pair tiles are 128 or 256 wide, not %d", bn);
-      err = pair == 2 ? launch_bf16_tc_pair(a, mA, mB, bn, dev->num_sms, stream)
+      int schedule = 1;
+      err = pair == 2 ? launch_bf16_tc_pair(a, mA, mB, bn, dev->num_sms, stream, &schedule)
                       : launch_bf16_tc(a, mA, mB, bn, dev->num_sms, stream);
       if (err == cudaSuccess) {
         t_last_bn = bn;
-        t_last_pair = pair;
+        t_last_pair = schedule;
       }
     }
       break;
@@ -280,6 +282,9 @@ __global__ void selftest_wait_kernel(int* status, uint64_t timeout_ns) {
 }
 
 }  // namespace
+
+bool split_tiles_enabled() { return t_split_tiles != 0; }
+
 }  // namespace g3
 
 using g3::Elem;
@@ -348,6 +353,12 @@ int gemm_force_tc_pair(int mode) {
 }
 
 int gemm_last_tc_pair(void) { return g3::t_last_pair; }
+
+int gemm_force_split_tiles(int enable) {
+  if (enable != 0 && enable != 1) return g3::fail(GEMM_ERR_INVALID_ARG, "enable must be 0 or 1");
+  g3::t_split_tiles = enable;
+  return GEMM_OK;
+}
 
 int gemm_set_wait_timeout_ns(uint64_t timeout_ns) {
   g3::g_timeout_ns.store(timeout_ns == 0 ? 1000000000ull : timeout_ns);

@@ -18,6 +18,13 @@
 // CTA's 128 rows.  The leader's commits arrive on both CTAs' barriers
 // (multicast), and both CTAs' epilogues arrive on the leader's
 // accumulator-empty barrier.  Waits are bounded as in the single-CTA kernel.
+//
+// Persistent schedule: tiles [0, dp_tiles) go to the pairs in turn.  When the
+// last wave would be partial (R = tiles mod pairs) and 2R pairs exist, those R
+// tiles instead run as 2R half-width items (256 x BN/2) on 2R pairs: a
+// half-width tile costs about 0.58 of a full one (measured per-column costs
+// of the 128- and 256-wide pair tiles), so the last wave shrinks from a whole
+// tile-time to a bit over half of one, with nothing to reduce afterwards.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -96,8 +103,21 @@ __global__ void __launch_bounds__(THREADS, 1)
   const GemmArgs& a = p.a;
   const uint32_t rank = cluster_ctarank() & 1u;  // clusters hold exactly one pair
   const bool leader = rank == 0;
-  const int cluster_id = blockIdx.x >> 1;
-  const int num_clusters = gridDim.x >> 1;
+  const int pair_id = blockIdx.x >> 1;
+  const int num_pairs = gridDim.x >> 1;
+  // this pair's work items: whole tiles, then at most one half-width item
+  const int n_dp = pair_id < p.dp_tiles ? (p.dp_tiles - pair_id + num_pairs - 1) / num_pairs : 0;
+  const int n_items = n_dp + (pair_id < p.half_tiles ? 1 : 0);
+  auto item = [&](int i, int& m0, int& n0, int& bn) {
+    if (i < n_dp) {
+      pair_tile_coords<BN>(pair_id + i * num_pairs, p, m0, n0);
+      bn = BN;
+    } else {
+      pair_tile_coords<BN>(p.dp_tiles + pair_id / 2, p, m0, n0);
+      bn = BN / 2;
+      n0 += (pair_id & 1) * (BN / 2);
+    }
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -130,11 +150,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
-        int m0, n0;
-        pair_tile_coords<BN>(tile, p, m0, n0);
+      for (int i = 0; ok && i < n_items; ++i) {
+        int m0, n0, bn;
+        item(i, m0, n0, bn);
         const int a_row = m0 + (int)rank * BM_CTA;
-        const int b_col = n0 + (int)rank * (BN / 2);
+        const int b_col = n0 + (int)rank * (bn / 2);
+        const int b_boxes = bn / 2 / 64;
+        const uint32_t tx_bytes = 2u * (A_STAGE_BYTES + b_boxes * B_BOX_BYTES);
         for (int kt = 0; kt < p.k_tiles; ++kt) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, a.timeout_ns, abort_flag)) {
             if (!*abort_flag) report_status(a.status, 5, kSiteTc2Producer);
@@ -144,10 +166,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           // both CTAs' copies of this stage complete on the leader's barrier
           const uint32_t lead_full = map_to_rank(full_bar(stage), 0);
-          if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * STAGE_BYTES);
+          if (leader) mbar_arrive_expect_tx(full_bar(stage), tx_bytes);
           tma_load_2d_pair(a_tile(stage), &mapA, lead_full, kt * BK, a_row);
-#pragma unroll
-          for (int j = 0; j < Cfg::B_BOXES; ++j)
+          for (int j = 0; j < b_boxes; ++j)
             tma_load_2d_pair(b_tile(stage) + j * B_BOX_BYTES, &mapB, lead_full, b_col + j * 64,
                              kt * BK);
           issued |= 1u << stage;
@@ -176,13 +197,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ MMA issuer (leader)
     if (leader) {
       if (elect_one_sync()) {
-        constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, /*A K-major*/ 0, /*B MN-major*/ 1);
+        constexpr uint32_t idesc_full = idesc_bf16_f32(BM, BN, /*A K-major*/ 0, /*B MN-major*/ 1);
+        constexpr uint32_t idesc_half = idesc_bf16_f32(BM, BN / 2, 0, 1);
         int stage = 0;
         uint32_t phase = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true, issued_any = false;
-        for (int tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
+        for (int i = 0; ok && i < n_items; ++i) {
+          const uint32_t idesc = i < n_dp ? idesc_full : idesc_half;
           if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, a.timeout_ns, abort_flag)) {
             if (!*abort_flag) report_status(a.status, 5, kSiteTc2Mma);
             *abort_flag = 1;
@@ -232,9 +255,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t lead_tempty1 = map_to_rank(tempty_bar(1), 0);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = cluster_id; tile < p.num_tiles; tile += num_clusters) {
-      int m0, n0;
-      pair_tile_coords<BN>(tile, p, m0, n0);
+    for (int i = 0; i < n_items; ++i) {
+      int m0, n0, bn;
+      item(i, m0, n0, bn);
       if (!mbar_wait(tfull_bar(acc), acc_phase, a.timeout_ns, abort_flag)) {
         if (!*abort_flag) report_status(a.status, 5, kSiteTc2Epilogue);
         *abort_flag = 1;
@@ -244,11 +267,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       const long long m = (long long)m0 + rank * BM_CTA + quarter * 32 + lane;
       const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < bn / 32; ++c) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_row + c * 32, r);
         tc_wait_ld();
-        if (c == BN / 32 - 1) {
+        if (c == bn / 32 - 1) {
           tc_fence_before();
           mbar_arrive_remote(acc == 0 ? lead_tempty0 : lead_tempty1);
         }
@@ -276,7 +299,7 @@ struct PairLaunchInfo {
 
 template <int BN, bool OUT_BF16>
 int launch_pair_impl(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
-                     int num_sms, cudaStream_t s) {
+                     int num_sms, cudaStream_t s, int* schedule) {
   using Cfg = PairCfg<BN>;
   static PairLaunchInfo info[64];
   static std::mutex mu;
@@ -322,7 +345,20 @@ int launch_pair_impl(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorM
   p.k_tiles = (a.K + BK - 1) / BK;
   const int out_bytes = OUT_BF16 ? 2 : 4;
   p.c_vec = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && ((a.ldc * out_bytes) % 16) == 0) ? 1 : 0;
-  const int clusters = (int)(tiles < info[dev].max_clusters ? tiles : info[dev].max_clusters);
+  const int pairs = info[dev].max_clusters;
+  const long long rem = tiles % pairs;
+  int clusters;
+  if (BN == 256 && split_tiles_enabled() && rem > 0 && 2 * rem <= pairs) {
+    p.dp_tiles = (int)(tiles - rem);
+    p.half_tiles = (int)(2 * rem);
+    clusters = pairs;
+    *schedule = 4;
+  } else {
+    p.dp_tiles = p.num_tiles;
+    p.half_tiles = 0;
+    clusters = (int)(tiles < pairs ? tiles : pairs);
+    *schedule = 2;
+  }
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, *mapA, *mapB, p);
   if (e != cudaSuccess) return e;
@@ -332,14 +368,14 @@ int launch_pair_impl(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorM
 }  // namespace
 
 int launch_bf16_tc_pair(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB, int bn,
-                        int num_sms, cudaStream_t s) {
+                        int num_sms, cudaStream_t s, int* schedule) {
   const bool bf16 = a.out == Elem::BF16;
   if (bn == 256)
-    return bf16 ? launch_pair_impl<256, true>(a, mapA, mapB, num_sms, s)
-                : launch_pair_impl<256, false>(a, mapA, mapB, num_sms, s);
+    return bf16 ? launch_pair_impl<256, true>(a, mapA, mapB, num_sms, s, schedule)
+                : launch_pair_impl<256, false>(a, mapA, mapB, num_sms, s, schedule);
   if (bn == 128)
-    return bf16 ? launch_pair_impl<128, true>(a, mapA, mapB, num_sms, s)
-                : launch_pair_impl<128, false>(a, mapA, mapB, num_sms, s);
+    return bf16 ? launch_pair_impl<128, true>(a, mapA, mapB, num_sms, s, schedule)
+                : launch_pair_impl<128, false>(a, mapA, mapB, num_sms, s, schedule);
   return cudaErrorInvalidValue;
 }
 

@@ -65,8 +65,11 @@ constexpr int kTcBM = 128, kTcBK = 64;
 // The same GEMM on CTA pairs (clusters of two, cta_group::2): C tiles of
 // 256 x bn, bn in {128, 256}; each CTA loads 128 rows of A and bn/2 columns
 // of B with the same tensor maps as the single-CTA kernel.
+// *schedule receives 2 (whole tiles) or 4 (the tiles of a partial last wave
+// run as two half-width tiles each).
+bool split_tiles_enabled();
 int launch_bf16_tc_pair(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB, int bn,
-                        int num_sms, cudaStream_t s);
+                        int num_sms, cudaStream_t s, int* schedule);
 
 // Skinny (M <= 16) split-K kernel: TMA tiles of B (64 n x 64 k) and A
 // (64 k x 16 rows), 128-byte swizzle.

@@ -16,7 +16,11 @@ namespace {
 struct TcParams {
   GemmArgs a;
   int tiles_m, tiles_n, num_tiles, k_tiles;
-  int c_vec;  // C 16-byte aligned and ldc*sizeof(out) a multiple of 16
+  int c_vec;       // C 16-byte aligned and ldc*sizeof(out) a multiple of 16
+  // CTA-pair kernel: tiles [0, dp_tiles) run one per pair; the remaining
+  // tiles run as half_tiles items of half the width, one per pair
+  int dp_tiles;
+  int half_tiles;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

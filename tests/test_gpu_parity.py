@@ -150,7 +150,7 @@ def test_bf16_tc_pair(cuda_lib, bn, M, N, K):
     try:
         for out, alpha, beta in ((BF16, 1.0, 0.0), (F32, 1.5, 0.5)):
             err, path = check(c.A, c.B, c.C0, alpha, beta, out)
-            assert path == g.PATH_BF16_TC and g.last_tc_pair() == 2 and g.last_tile_n() == bn
+            assert path == g.PATH_BF16_TC and g.last_tc_pair() in (2, 4) and g.last_tile_n() == bn
     finally:
         g.force_tc_pair(0)
         g.force_tile_n(0)
@@ -172,6 +172,31 @@ def test_bf16_tc_pair_deterministic_and_matches_single(cuda_lib):
         g.force_tc_pair(0)
     # same products, same k order inside each 16-deep MMA step: agree to fp32 rounding
     assert torch.allclose(a, s1, rtol=1e-5, atol=1e-6)
+
+
+@pytest.mark.parametrize("M,N,K", [(2560, 2560, 1024), (1536, 1280, 1024), (1300, 1000, 520),
+                                   (1300, 800, 520), (300, 256, 136)])
+def test_bf16_tc_half_width_last_wave(cuda_lib, M, N, K):
+    # tile counts whose partial last wave runs as half-width tiles; (1300, 800):
+    # the second half of the last tile column lies entirely outside C;
+    # (1536, 1280) and (300, 256): fewer tiles than pairs, every tile halved
+    c = inputs.make("decode_m16_o", M=M, N=N, K=K)
+    g.force_tc_pair(2)
+    g.force_tile_n(256)
+    try:
+        for out, alpha, beta in ((BF16, 1.0, 0.0), (F32, 1.5, 0.5)):
+            err, path = check(c.A, c.B, c.C0, alpha, beta, out)
+            assert path == g.PATH_BF16_TC and g.last_tc_pair() == 4, g.last_tc_pair()
+        a1 = run_abi(c.A, c.B, None, 1.0, 0.0, F32)[0]
+        g.force_split_tiles(0)
+        b = run_abi(c.A, c.B, None, 1.0, 0.0, F32)[0]
+        assert g.last_tc_pair() == 2
+        # the same products in the same order: identical bits
+        assert torch.equal(a1, b)
+    finally:
+        g.force_split_tiles(1)
+        g.force_tc_pair(0)
+        g.force_tile_n(0)
 
 
 def test_bf16_tc_pair_rejects_other_widths(cuda_lib):
@@ -198,7 +223,7 @@ def test_bf16_tc_pair_8192_sampled(cuda_lib, out):
     try:
         g.gemm(A, B, C, 1.0, 0.0)
         torch.cuda.synchronize()
-        assert g.last_tc_pair() == 2
+        assert g.last_tc_pair() in (2, 4)
     finally:
         g.force_tc_pair(0)
     gen = np.random.default_rng(7)
@@ -215,7 +240,7 @@ def test_bf16_tc_tile_width_choice(cuda_lib):
         c = inputs.make("bf16_4096", M=M, N=N, K=64)
         check(c.A, c.B, None, 1.0, 0.0, BF16)
         if sms == 152:
-            assert (g.last_tc_pair(), g.last_tile_n()) == want, (M, N)
+            assert (min(g.last_tc_pair(), 2), g.last_tile_n()) == want, (M, N)
     with pytest.raises(g.GemmError):
         g.force_tile_n(100)
 
