@@ -47,12 +47,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per launch measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum)
 # for each kernel source file, valid only while the file hashes to `sha256`.
 NCU_TRAFFIC = {
-    # profiles/sgemm_tma_kernel_fp32_4096.md: 401.4 MB read + 54.9 MB written
-    "gemm_f32_simt.cu": {"sha256": "87ac9ecf4c07e6b29f5f32afd5b958500f4db663cf7b79b70258665ea1022c23",
-                         "bytes_per_launch": 456229376},
-    # profiles/gemm_bf16_tc2_kernel_bf16_8192.md, 4096^3 capture: 79.0 MB + 10.9 MB
-    "gemm_bf16_tc2.cu": {"sha256": "cb432567274a20e7291c74dff303f440d1294fe655ca5f252f55d519c9d6215c",
-                         "bytes_per_launch": 89855744},
+    # profiles/sgemm_tma_kernel_fp32_4096.md: 410.6 MB read + 54.0 MB written
+    "gemm_f32_simt.cu": {"sha256": "31bef2fda14d2f2bce126b0c4d3c86dbde56f170dd9a8ba320f2c93586c46560",
+                         "bytes_per_launch": 464635136},
+    # profiles/gemm_bf16_tc2_kernel_bf16_8192.md, 4096^3 capture: 78.1 MB + 11.1 MB
+    "gemm_bf16_tc2.cu": {"sha256": "754954bef5e8861ae8d1c13c9543fde47040cb59a70d799f831c19253668bf96",
+                         "bytes_per_launch": 89235968},
 }
 
 
