@@ -26,8 +26,9 @@
 //     role in the main loop fetch their C values into registers while the
 //     weights stream, so that read is off the kernel's tail;
 //   * launched with programmatic stream serialization: the launch, barrier
-//     set-up and TMEM allocation overlap the previous kernel on the stream,
-//     and every global read waits on griddepcontrol.wait.
+//     set-up, TMEM allocation and an L2 prefetch of the first weight stages
+//     overlap the previous kernel on the stream, and every read into the SM
+//     waits on griddepcontrol.wait.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -132,6 +133,16 @@ __global__ void __launch_bounds__(THREADS, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if (warp == 0 && lane == 0 && my_kt > 0) {
+    // While the previous kernel on the stream finishes, pull the first
+    // stages of this CTA's weights into L2 (a prefetch only: the real loads
+    // come after the wait and see whatever is in memory then).
+    tma_prefetch_desc(&mapB);
+    const int pre = my_kt < STAGES ? my_kt : STAGES;
+    for (int kt = kt_begin; kt < kt_begin + pre; ++kt)
+#pragma unroll
+      for (int j = 0; j < BN / 64; ++j) tma_prefetch_l2_2d(&mapB, n0 + j * 64, kt * BK);
+  }
   griddep_wait();  // inputs may come from the previous kernel on the stream
 
   // beta*C_old of this thread's outputs, fetched now so the read overlaps the
