@@ -64,11 +64,17 @@ constexpr int RED_ITEMS = MN * BN / 4 / THREADS;
 static_assert(PARTIAL_BYTES <= STAGE_BYTES, "partial tile aliases one stage");
 static_assert(STAGE_BYTES % 1024 == 0, "stages stay 1024-byte aligned");
 
+// The raw bits of C_old (bf16 zero-extended, or fp32): the load writes the
+// register directly, so nothing waits for it until raw_to_float() runs.
 template <bool OUT_BF16>
-__device__ __forceinline__ float load_c(const GemmArgs& a, int m, long long n) {
+__device__ __forceinline__ uint32_t load_c_raw(const GemmArgs& a, int m, long long n) {
   const long long off = (long long)m * a.ldc + n;
-  if (OUT_BF16) return __bfloat162float(static_cast<const __nv_bfloat16*>(a.C)[off]);
-  return static_cast<const float*>(a.C)[off];
+  if (OUT_BF16) return static_cast<const unsigned short*>(a.C)[off];
+  return __float_as_uint(static_cast<const float*>(a.C)[off]);
+}
+template <bool OUT_BF16>
+__device__ __forceinline__ float raw_to_float(uint32_t w) {
+  return OUT_BF16 ? __uint_as_float(w << 16) : __uint_as_float(w);
 }
 
 template <bool OUT_BF16>
@@ -145,22 +151,24 @@ __global__ void __launch_bounds__(THREADS, 2)
   }
   griddep_wait();  // inputs may come from the previous kernel on the stream
 
-  // beta*C_old of this thread's outputs, fetched now so the read overlaps the
-  // weight stream.  split == 1: column n0 + threadIdx.x, rows 0..M-1.
-  // split > 1: items of 4 columns of the columns this rank finishes.
+  // C_old of this thread's outputs, loaded now and not used until the
+  // epilogue, so the loads stay in flight while the weights stream (no
+  // thread -- in particular not the TMA producer -- waits for them here).
+  // split == 1: column n0 + threadIdx.x, rows 0..M-1.  split > 1: items of 4
+  // columns of the columns this rank finishes.
   const int cols = BN / p.split;
   const int groups = cols / 4;
   const int items = a.M * groups;
-  float cpre[MN];  // split == 1: one per row; split > 1: RED_ITEMS x 4
+  uint32_t cpre[MN];  // split == 1: one per row; split > 1: RED_ITEMS x 4
   static_assert(RED_ITEMS * 4 <= MN, "prefetch registers");
 #pragma unroll
-  for (int j = 0; j < MN; ++j) cpre[j] = 0.f;
+  for (int j = 0; j < MN; ++j) cpre[j] = 0u;
   if (a.beta != 0.f) {
     if (p.split == 1) {
       const long long n = (long long)n0 + threadIdx.x;
 #pragma unroll
       for (int m = 0; m < MN; ++m)
-        if (m < a.M && n < a.N) cpre[m] = a.beta * load_c<OUT_BF16>(a, m, n);
+        if (m < a.M && n < a.N) cpre[m] = load_c_raw<OUT_BF16>(a, m, n);
     } else {
 #pragma unroll
       for (int j = 0; j < RED_ITEMS; ++j) {
@@ -170,7 +178,7 @@ __global__ void __launch_bounds__(THREADS, 2)
           const long long n = (long long)n0 + rank * cols + (it % groups) * 4;
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            if (n + e < a.N) cpre[j * 4 + e] = a.beta * load_c<OUT_BF16>(a, m, n + e);
+            if (n + e < a.N) cpre[j * 4 + e] = load_c_raw<OUT_BF16>(a, m, n + e);
         }
       }
     }
@@ -279,7 +287,9 @@ __global__ void __launch_bounds__(THREADS, 2)
     if (n < a.N) {
 #pragma unroll
       for (int m = 0; m < MN; ++m)
-        if (m < a.M) store_c<OUT_BF16>(a, m, n, fmaf(a.alpha, __uint_as_float(r[m]), cpre[m]));
+        if (m < a.M)
+          store_c<OUT_BF16>(a, m, n,
+                            fmaf(a.alpha, __uint_as_float(r[m]), a.beta * raw_to_float<OUT_BF16>(cpre[m])));
     }
   } else {
     const int n_local = warp * 32 + lane;
@@ -312,7 +322,9 @@ __global__ void __launch_bounds__(THREADS, 2)
         const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          if (n + e < a.N) store_c<OUT_BF16>(a, m, n + e, fmaf(a.alpha, sv[e], cpre[j * 4 + e]));
+          if (n + e < a.N)
+            store_c<OUT_BF16>(a, m, n + e,
+                              fmaf(a.alpha, sv[e], a.beta * raw_to_float<OUT_BF16>(cpre[j * 4 + e])));
       }
     }
     cluster_sync();  // no rank leaves while others may still read its partial
