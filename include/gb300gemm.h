@@ -86,6 +86,37 @@ int gemm_bf16_f32out(int M, int N, int K, float alpha, const gemm_bf16_t* A, int
                      const gemm_bf16_t* B, int ldb, float beta, float* C, int ldc,
                      cudaStream_t stream);
 
+/* Activation applied last by the _ex entry points. */
+typedef enum {
+  GEMM_ACT_NONE = 0,
+  GEMM_ACT_RELU = 1, /* max(z, 0) */
+  GEMM_ACT_SILU = 2, /* z / (1 + exp(-z)) */
+  GEMM_ACT_GELU = 3  /* 0.5 z (1 + erf(z / sqrt(2))) */
+} gemm_activation;
+
+/*
+ * The three GEMMs with a fused elementwise epilogue ("Kernel 性能从何而来",
+ * section "优化 Memory-Bound Kernel": fuse the GEMM with its elementwise
+ * epilogue instead of a second pass over C):
+ *
+ *     z = alpha * A*B + beta * C + bias      (bias[n] added to every row m)
+ *     C = act(z)
+ *
+ * z and act(z) are evaluated in fp32 and rounded once to C's type.  `bias` is
+ * a DEVICE pointer to N floats (4-byte aligned) or NULL; `activation` is a
+ * gemm_activation.  Everything else is as for the plain entry points, which
+ * are these with bias = NULL and GEMM_ACT_NONE.
+ */
+int gemm_f32_ex(int M, int N, int K, float alpha, const float* A, int lda, const float* B, int ldb,
+                float beta, float* C, int ldc, const float* bias, int activation,
+                cudaStream_t stream);
+int gemm_bf16_ex(int M, int N, int K, float alpha, const gemm_bf16_t* A, int lda,
+                 const gemm_bf16_t* B, int ldb, float beta, gemm_bf16_t* C, int ldc,
+                 const float* bias, int activation, cudaStream_t stream);
+int gemm_bf16_f32out_ex(int M, int N, int K, float alpha, const gemm_bf16_t* A, int lda,
+                        const gemm_bf16_t* B, int ldb, float beta, float* C, int ldc,
+                        const float* bias, int activation, cudaStream_t stream);
+
 /*
  * Message for the last non-OK return on the calling host thread ("" if none).
  * The string is owned by the library and valid until the next call on this

@@ -13,6 +13,10 @@ package imports nothing from it.
   (:func:`abs_product_max`).  For alpha != 1 or beta != 0 the scale of the
   whole expression, ``max(|alpha| sum_k |A||B| + |beta| |C0|)``, is used
   (:func:`normwise_denominator`); it equals the former at alpha=1, beta=0.
+  For the fused epilogue act(z) the scale is that of z (with |bias|): the
+  activations have slope at most 1.13, so an error in z carries over at that
+  size.
+* ``oracle.epilogue`` holds the activations and the SwiGLU pair.
 * ``oracle.roofline_ref`` restates the FLOP, arithmetic-intensity and roofline
   formulas of the pages.
 
@@ -120,7 +124,7 @@ def abs_product_max(A, B, threads: int | None = None) -> float:
 
 
 def normwise_denominator(A, B, alpha: float = 1.0, beta: float = 0.0, C0=None,
-                         threads: int | None = None) -> float:
+                         threads: int | None = None, bias=None) -> float:
     """max_{m,n} (|alpha| sum_k |A[m,k]||B[k,n]| + |beta| |C0[m,n]|).
 
     The normwise scale of the whole expression alpha*A*B + beta*C0.  With
@@ -138,6 +142,9 @@ def normwise_denominator(A, B, alpha: float = 1.0, beta: float = 0.0, C0=None,
         P = gemm(A64, B64, abs(alpha), abs(beta), c0, threads)
     else:
         P = gemm(A64, B64, abs(alpha), 0.0, None, threads)
+    if bias is not None:
+        # the fused epilogue's bias is one more term of z = alpha*AB + beta*C0 + bias
+        P = P + np.abs(to_f64(bias)).reshape(1, -1)
     return float(P.max())
 
 

@@ -32,11 +32,13 @@ GEMM_ERR_CUDA = 4
 GEMM_ERR_DEVICE_TIMEOUT = 5
 
 PATH_AUTO, PATH_GENERIC, PATH_F32_SIMT, PATH_BF16_TC, PATH_SKINNY = range(5)
+ACT_NONE, ACT_RELU, ACT_SILU, ACT_GELU = range(4)
 PATH_NAMES = {PATH_AUTO: "none", PATH_GENERIC: "generic", PATH_F32_SIMT: "f32_simt",
               PATH_BF16_TC: "bf16_tc", PATH_SKINNY: "skinny"}
 
 # every symbol the public header declares
-EXPORTS = ("gemm_f32", "gemm_bf16", "gemm_bf16_f32out", "gemm_get_last_error",
+EXPORTS = ("gemm_f32", "gemm_bf16", "gemm_bf16_f32out", "gemm_f32_ex", "gemm_bf16_ex",
+           "gemm_bf16_f32out_ex", "gemm_get_last_error",
            "gemm_device_status", "gemm_force_path", "gemm_last_path", "gemm_force_tile_n",
            "gemm_last_tile_n", "gemm_force_tc_pair", "gemm_last_tc_pair", "gemm_force_split_tiles",
            "gemm_set_wait_timeout_ns", "gemm_selftest_wait_timeout")
@@ -73,6 +75,10 @@ def load(path: str | None = None):
         for name in ("gemm_f32", "gemm_bf16", "gemm_bf16_f32out"):
             fn = getattr(lib, name)
             fn.argtypes = [i, i, i, f, vp, i, vp, i, f, vp, i, vp]
+            fn.restype = i
+        for name in ("gemm_f32_ex", "gemm_bf16_ex", "gemm_bf16_f32out_ex"):
+            fn = getattr(lib, name)
+            fn.argtypes = [i, i, i, f, vp, i, vp, i, f, vp, i, vp, i, vp]
             fn.restype = i
         lib.gemm_get_last_error.argtypes = []
         lib.gemm_get_last_error.restype = ctypes.c_char_p
@@ -116,6 +122,19 @@ def gemm_bf16(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0):
 
 def gemm_bf16_f32out(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0):
     _check(load().gemm_bf16_f32out(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream))
+
+
+def gemm_f32_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias, act, stream=0):
+    _check(load().gemm_f32_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias, act, stream))
+
+
+def gemm_bf16_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias, act, stream=0):
+    _check(load().gemm_bf16_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias, act, stream))
+
+
+def gemm_bf16_f32out_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias, act, stream=0):
+    _check(load().gemm_bf16_f32out_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias, act,
+                                      stream))
 
 
 def device_status(stream=0) -> tuple[int, int]:
@@ -168,9 +187,11 @@ def _ld(t) -> int:
     return max(int(t.stride(0)), int(t.shape[1]), 1)
 
 
-def gemm(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
-    """C = alpha*A@B + beta*C for CUDA tensors (fp32/fp32/fp32, bf16/bf16/bf16
-    or bf16/bf16/fp32).  Argument marshalling only."""
+def gemm(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None, bias=None,
+         act: int = ACT_NONE):
+    """C = act(alpha*A@B + beta*C + bias) for CUDA tensors (fp32/fp32/fp32,
+    bf16/bf16/bf16 or bf16/bf16/fp32; bias: N fp32 values or None).
+    Argument marshalling only."""
     import torch
     M, K = A.shape
     K2, N = B.shape
@@ -180,13 +201,19 @@ def gemm(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
         raise ValueError("gemm() takes CUDA tensors")
     s = stream if stream is not None else torch.cuda.current_stream(A.device).cuda_stream
     args = (M, N, K, float(alpha), A.data_ptr(), _ld(A), B.data_ptr(), _ld(B), float(beta),
-            C.data_ptr(), _ld(C), s)
+            C.data_ptr(), _ld(C))
+    if bias is not None:
+        if bias.dtype != torch.float32 or not bias.is_cuda or bias.numel() != N or \
+                (bias.dim() == 1 and bias.stride(0) != 1):
+            raise ValueError("bias must be N contiguous fp32 values on the GPU")
+    plain = bias is None and act == ACT_NONE
+    ex = (bias.data_ptr() if bias is not None else None, int(act), s)
     if A.dtype == torch.float32 and B.dtype == torch.float32 and C.dtype == torch.float32:
-        gemm_f32(*args)
+        gemm_f32(*args, s) if plain else gemm_f32_ex(*args, *ex)
     elif A.dtype == torch.bfloat16 and B.dtype == torch.bfloat16 and C.dtype == torch.bfloat16:
-        gemm_bf16(*args)
+        gemm_bf16(*args, s) if plain else gemm_bf16_ex(*args, *ex)
     elif A.dtype == torch.bfloat16 and B.dtype == torch.bfloat16 and C.dtype == torch.float32:
-        gemm_bf16_f32out(*args)
+        gemm_bf16_f32out(*args, s) if plain else gemm_bf16_f32out_ex(*args, *ex)
     else:
         raise TypeError(f"unsupported dtypes {A.dtype}, {B.dtype} -> {C.dtype}")
     return C

@@ -165,7 +165,7 @@ int make_map(const void* ptr, uint64_t cols, uint64_t rows, uint64_t ld_bytes, u
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int lda, const void* B,
-        int ldb, float beta, void* C, int ldc, cudaStream_t stream) {
+        int ldb, float beta, void* C, int ldc, const float* bias, int act, cudaStream_t stream) {
   t_msg[0] = '\0';
   t_last_path = GEMM_PATH_AUTO;
   if (M < 0 || N < 0 || K < 0) return fail(GEMM_ERR_INVALID_ARG, "negative size M=%d N=%d K=%d", M, N, K);
@@ -179,6 +179,9 @@ int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int 
   if ((reinterpret_cast<uintptr_t>(A) % in_sz) || (reinterpret_cast<uintptr_t>(B) % in_sz) ||
       (reinterpret_cast<uintptr_t>(C) % out_sz))
     return fail(GEMM_ERR_MISALIGNED, "a matrix pointer is not aligned to its element size");
+  if (act < kActNone || act > kActGelu) return fail(GEMM_ERR_INVALID_ARG, "unknown activation %d", act);
+  if (reinterpret_cast<uintptr_t>(bias) % sizeof(float))
+    return fail(GEMM_ERR_MISALIGNED, "bias is not aligned to 4 bytes");
 
   DeviceInfo* dev = nullptr;
   int rc = device_info(&dev);
@@ -190,6 +193,8 @@ int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int 
   a.in = in; a.out = out;
   a.status = dev->status;
   a.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  a.bias = bias;
+  a.act = act;
 
   const bool tma_ok = K > 0 && aligned16(A) && aligned16(B) && ((size_t)lda * in_sz) % 16 == 0 &&
                       ((size_t)ldb * in_sz) % 16 == 0;
@@ -293,18 +298,42 @@ extern "C" {
 
 int gemm_f32(int M, int N, int K, float alpha, const float* A, int lda, const float* B, int ldb,
              float beta, float* C, int ldc, cudaStream_t stream) {
-  return g3::run(Elem::F32, Elem::F32, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+  return g3::run(Elem::F32, Elem::F32, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, nullptr,
+                 g3::kActNone, stream);
 }
 
 int gemm_bf16(int M, int N, int K, float alpha, const gemm_bf16_t* A, int lda, const gemm_bf16_t* B,
               int ldb, float beta, gemm_bf16_t* C, int ldc, cudaStream_t stream) {
-  return g3::run(Elem::BF16, Elem::BF16, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+  return g3::run(Elem::BF16, Elem::BF16, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, nullptr,
+                 g3::kActNone, stream);
 }
 
 int gemm_bf16_f32out(int M, int N, int K, float alpha, const gemm_bf16_t* A, int lda,
                      const gemm_bf16_t* B, int ldb, float beta, float* C, int ldc,
                      cudaStream_t stream) {
-  return g3::run(Elem::BF16, Elem::F32, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+  return g3::run(Elem::BF16, Elem::F32, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, nullptr,
+                 g3::kActNone, stream);
+}
+
+int gemm_f32_ex(int M, int N, int K, float alpha, const float* A, int lda, const float* B, int ldb,
+                float beta, float* C, int ldc, const float* bias, int activation,
+                cudaStream_t stream) {
+  return g3::run(Elem::F32, Elem::F32, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias,
+                 activation, stream);
+}
+
+int gemm_bf16_ex(int M, int N, int K, float alpha, const gemm_bf16_t* A, int lda,
+                 const gemm_bf16_t* B, int ldb, float beta, gemm_bf16_t* C, int ldc,
+                 const float* bias, int activation, cudaStream_t stream) {
+  return g3::run(Elem::BF16, Elem::BF16, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias,
+                 activation, stream);
+}
+
+int gemm_bf16_f32out_ex(int M, int N, int K, float alpha, const gemm_bf16_t* A, int lda,
+                        const gemm_bf16_t* B, int ldb, float beta, float* C, int ldc,
+                        const float* bias, int activation, cudaStream_t stream) {
+  return g3::run(Elem::BF16, Elem::F32, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias,
+                 activation, stream);
 }
 
 const char* gemm_get_last_error(void) { return g3::t_msg; }

@@ -25,6 +25,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "epilogue.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -210,6 +211,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     // ---------------------------------------------------------- epilogue
     float* C = static_cast<float*>(a.C);
     const bool beta_nz = a.beta != 0.f;
+    const bool epi = a.bias != nullptr || a.act != kActNone;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const long long m = (long long)m0 + wm * 64 + i * 8 + tm;
@@ -228,6 +230,10 @@ __global__ void __launch_bounds__(THREADS, 2)
             v[2] = fmaf(a.beta, c.z, v[2]);
             v[3] = fmaf(a.beta, c.w, v[3]);
           }
+          if (epi) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = finish(a, v[j], n + j);
+          }
           *reinterpret_cast<float4*>(cp) = make_float4(v[0], v[1], v[2], v[3]);
         } else {
 #pragma unroll
@@ -235,7 +241,7 @@ __global__ void __launch_bounds__(THREADS, 2)
             if (n + j < a.N) {
               float r = v[j];
               if (beta_nz) r = fmaf(a.beta, cp[j], r);
-              cp[j] = r;
+              cp[j] = finish(a, r, n + j);
             }
           }
         }

@@ -9,6 +9,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "epilogue.cuh"
 #include "internal.h"
 
 namespace g3 {
@@ -84,7 +85,7 @@ __global__ void __launch_bounds__(256) gemm_generic_kernel(GemmArgs a, int tiles
       if (n >= a.N) continue;
       float v = a.alpha * acc[i][j];
       if (a.beta != 0.f) v = fmaf(a.beta, to_f32<TO>(C[m * a.ldc + n]), v);
-      C[m * a.ldc + n] = from_f32<TO>(v);
+      C[m * a.ldc + n] = from_f32<TO>(finish(a, v, n));
     }
   }
 }

@@ -35,6 +35,7 @@
 
 #include <cstdlib>
 
+#include "epilogue.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -79,6 +80,7 @@ __device__ __forceinline__ float raw_to_float(uint32_t w) {
 
 template <bool OUT_BF16>
 __device__ __forceinline__ void store_c(const GemmArgs& a, int m, long long n, float v) {
+  v = finish(a, v, n);
   const long long off = (long long)m * a.ldc + n;
   if (OUT_BF16)
     static_cast<__nv_bfloat16*>(a.C)[off] = __float2bfloat16_rn(v);

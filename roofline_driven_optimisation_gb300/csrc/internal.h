@@ -9,6 +9,9 @@ namespace g3 {
 
 enum class Elem : int { F32 = 0, BF16 = 1 };
 
+// Activations of the fused epilogue (values of gemm_activation in the header).
+enum Act : int { kActNone = 0, kActRelu = 1, kActSilu = 2, kActGelu = 3 };
+
 // One GEMM call after validation: C = alpha*A*B + beta*C, row-major.
 struct GemmArgs {
   int M, N, K;
@@ -22,6 +25,8 @@ struct GemmArgs {
   Elem in, out;
   int* status;          // device status word (2 ints)
   uint64_t timeout_ns;  // bound on any single wait inside a kernel
+  const float* bias;    // N fp32 values added to every row of C, or null
+  int act;              // Act applied last
 };
 
 // Location codes recorded with a device timeout (status[1]).

@@ -8,6 +8,7 @@
 #include <cuda_bf16.h>
 #include <cstdint>
 
+#include "epilogue.cuh"
 #include "internal.h"
 
 namespace g3 {
@@ -38,6 +39,7 @@ __device__ __forceinline__ void store_row32(const TcParams& p, long long m, long
   for (int j = 0; j < 32; ++j) v[j] = a.alpha * __uint_as_float(r[j]);
   const bool beta_nz = a.beta != 0.f;
   const bool full = p.c_vec && (n + 32 <= a.N);
+  const bool epi = a.bias != nullptr || a.act != kActNone;
   if (OUT_BF16) {
     __nv_bfloat16* C = static_cast<__nv_bfloat16*>(a.C) + m * a.ldc + n;
     if (full) {
@@ -55,6 +57,10 @@ __device__ __forceinline__ void store_row32(const TcParams& p, long long m, long
           }
         }
       }
+      if (epi) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = finish(a, v[j], n + j);
+      }
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint4 o;
@@ -70,7 +76,7 @@ __device__ __forceinline__ void store_row32(const TcParams& p, long long m, long
         if (n + j < a.N) {
           float x = v[j];
           if (beta_nz) x = fmaf(a.beta, __bfloat162float(C[j]), x);
-          C[j] = __float2bfloat16_rn(x);
+          C[j] = __float2bfloat16_rn(finish(a, x, n + j));
         }
       }
     }
@@ -88,6 +94,12 @@ __device__ __forceinline__ void store_row32(const TcParams& p, long long m, long
           o.z = fmaf(a.beta, old.z, o.z);
           o.w = fmaf(a.beta, old.w, o.w);
         }
+        if (epi) {
+          o.x = finish(a, o.x, n + 4 * q);
+          o.y = finish(a, o.y, n + 4 * q + 1);
+          o.z = finish(a, o.z, n + 4 * q + 2);
+          o.w = finish(a, o.w, n + 4 * q + 3);
+        }
         c4[q] = o;
       }
     } else {
@@ -96,7 +108,7 @@ __device__ __forceinline__ void store_row32(const TcParams& p, long long m, long
         if (n + j < a.N) {
           float x = v[j];
           if (beta_nz) x = fmaf(a.beta, C[j], x);
-          C[j] = x;
+          C[j] = finish(a, x, n + j);
         }
       }
     }
