@@ -118,6 +118,26 @@ int gemm_bf16_f32out_ex(int M, int N, int K, float alpha, const gemm_bf16_t* A, 
                         const float* bias, int activation, cudaStream_t stream);
 
 /*
+ * The FFN gate/up pair of a LLaMA layer ("CUDA 算子工程 ch.10 朴素 GEMM 与
+ * Roofline 分析", section 10.1: FFN gate / up / down as separate GEMMs, SiLU
+ * among the small elementwise operators) fused into one kernel, as
+ * "Kernel 性能从何而来" section "优化 Memory-Bound Kernel" asks of a producer
+ * and its consumer (the intermediate stays in TMEM/registers):
+ *
+ *     C = silu(A * Bgate) .* (A * Bup),   silu(z) = z / (1 + exp(-z))
+ *
+ * A is M x K (lda), Bgate and Bup are K x N with the same leading dimension
+ * ldb, C is M x N (ldc); all bf16 DEVICE pointers owned by the caller.  Both
+ * products are accumulated in fp32, combined in fp32 and rounded once to
+ * bf16.  C is write-only.  K == 0 gives C = 0.  Bup may be NULL only when
+ * K == 0.  Alignment, paths, asynchrony, determinism and errors are as for
+ * gemm_bf16: M <= 16 runs on the decode kernel, larger M on CTA pairs with
+ * 256 x 128 C tiles, unaligned operands on the generic kernel.
+ */
+int gemm_bf16_swiglu(int M, int N, int K, const gemm_bf16_t* A, int lda, const gemm_bf16_t* Bgate,
+                     const gemm_bf16_t* Bup, int ldb, gemm_bf16_t* C, int ldc, cudaStream_t stream);
+
+/*
  * Message for the last non-OK return on the calling host thread ("" if none).
  * The string is owned by the library and valid until the next call on this
  * thread.

@@ -56,3 +56,27 @@ def swiglu(A, Bgate, Bup, threads=None):
     g = gemm(A, Bgate, 1.0, 0.0, None, threads)
     u = gemm(A, Bup, 1.0, 0.0, None, threads)
     return activate(g, SILU) * u
+
+
+# max over z of d/dz silu(z) = sigmoid(z) (1 + z (1 - sigmoid(z))), about
+# 1.0998 near z = 2.40; 1.1 bounds it
+SILU_SLOPE_BOUND = 1.1
+
+
+def swiglu_error_scale(A, Bgate, Bup, threads=None) -> float:
+    """Scale for the normwise error of a computed swiglu(A, Bgate, Bup).
+
+    With g = A@Bgate and u = A@Bup each accumulated with an error of at most
+    e * sum_k |A||B| (rounding of the products and sums), the first-order
+    error of silu(g) * u is at most
+        e * (SILU_SLOPE_BOUND |u| sum_k|A||Bgate| + |silu(g)| sum_k|A||Bup|),
+    and the final rounding of silu(g) * u is bounded by the same scale (since
+    |u| <= sum_k |A||Bup|).  Returns the max over elements of the bracket.
+    """
+    g = gemm(A, Bgate, 1.0, 0.0, None, threads)
+    u = gemm(A, Bup, 1.0, 0.0, None, threads)
+    Aa = np.abs(to_f64(A))
+    Sg = gemm(Aa, np.abs(to_f64(Bgate)), 1.0, 0.0, None, threads)
+    Su = gemm(Aa, np.abs(to_f64(Bup)), 1.0, 0.0, None, threads)
+    S = SILU_SLOPE_BOUND * np.abs(u) * Sg + np.abs(activate(g, SILU)) * Su
+    return float(S.max()) if S.size else 0.0

@@ -38,7 +38,7 @@ PATH_NAMES = {PATH_AUTO: "none", PATH_GENERIC: "generic", PATH_F32_SIMT: "f32_si
 
 # every symbol the public header declares
 EXPORTS = ("gemm_f32", "gemm_bf16", "gemm_bf16_f32out", "gemm_f32_ex", "gemm_bf16_ex",
-           "gemm_bf16_f32out_ex", "gemm_get_last_error",
+           "gemm_bf16_f32out_ex", "gemm_bf16_swiglu", "gemm_get_last_error",
            "gemm_device_status", "gemm_force_path", "gemm_last_path", "gemm_force_tile_n",
            "gemm_last_tile_n", "gemm_force_tc_pair", "gemm_last_tc_pair", "gemm_force_split_tiles",
            "gemm_set_wait_timeout_ns", "gemm_selftest_wait_timeout")
@@ -80,6 +80,8 @@ def load(path: str | None = None):
             fn = getattr(lib, name)
             fn.argtypes = [i, i, i, f, vp, i, vp, i, f, vp, i, vp, i, vp]
             fn.restype = i
+        lib.gemm_bf16_swiglu.argtypes = [i, i, i, vp, i, vp, vp, i, vp, i, vp]
+        lib.gemm_bf16_swiglu.restype = i
         lib.gemm_get_last_error.argtypes = []
         lib.gemm_get_last_error.restype = ctypes.c_char_p
         lib.gemm_device_status.argtypes = [vp, ctypes.POINTER(i)]
@@ -135,6 +137,10 @@ def gemm_bf16_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias, act, stream
 def gemm_bf16_f32out_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias, act, stream=0):
     _check(load().gemm_bf16_f32out_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias, act,
                                       stream))
+
+
+def gemm_bf16_swiglu(M, N, K, A, lda, Bgate, Bup, ldb, C, ldc, stream=0):
+    _check(load().gemm_bf16_swiglu(M, N, K, A, lda, Bgate, Bup, ldb, C, ldc, stream))
 
 
 def device_status(stream=0) -> tuple[int, int]:
@@ -216,4 +222,23 @@ def gemm(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None, bias=None,
         gemm_bf16_f32out(*args, s) if plain else gemm_bf16_f32out_ex(*args, *ex)
     else:
         raise TypeError(f"unsupported dtypes {A.dtype}, {B.dtype} -> {C.dtype}")
+    return C
+
+
+def swiglu(A, Bgate, Bup, C, stream=None):
+    """C = silu(A@Bgate) * (A@Bup) for bf16 CUDA tensors; Bgate and Bup share
+    one shape and leading dimension.  Argument marshalling only."""
+    import torch
+    M, K = A.shape
+    K2, N = Bgate.shape
+    if K2 != K or tuple(Bup.shape) != (K, N) or tuple(C.shape) != (M, N):
+        raise ValueError(f"shape mismatch {tuple(A.shape)} @ {tuple(Bgate.shape)}, "
+                         f"{tuple(Bup.shape)} -> {tuple(C.shape)}")
+    if _ld(Bgate) != _ld(Bup):
+        raise ValueError("Bgate and Bup must have the same leading dimension")
+    if not all(t.is_cuda and t.dtype == torch.bfloat16 for t in (A, Bgate, Bup, C)):
+        raise TypeError("swiglu() takes bf16 CUDA tensors")
+    s = stream if stream is not None else torch.cuda.current_stream(A.device).cuda_stream
+    gemm_bf16_swiglu(M, N, K, A.data_ptr(), _ld(A), Bgate.data_ptr(), Bup.data_ptr(), _ld(Bgate),
+                     C.data_ptr(), _ld(C), s)
     return C

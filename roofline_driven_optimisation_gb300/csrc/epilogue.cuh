@@ -27,6 +27,11 @@ __device__ __forceinline__ float activate(float z, int act) {
   }
 }
 
+// SwiGLU: silu(gate) * up
+__device__ __forceinline__ float swiglu_combine(float gate, float up) {
+  return gate / (1.f + expf(-gate)) * up;
+}
+
 // bias and activation of one value whose alpha/beta terms are already in v
 __device__ __forceinline__ float finish(const GemmArgs& a, float v, long long n) {
   if (a.bias != nullptr) v += a.bias[n];

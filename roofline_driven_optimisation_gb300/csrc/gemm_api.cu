@@ -164,8 +164,11 @@ int make_map(const void* ptr, uint64_t cols, uint64_t rows, uint64_t ld_bytes, u
 // ---------------------------------------------------------------- dispatch
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// swiglu: C = silu(A*B) * (A*B2), B2 with B's shape and leading dimension
+// (alpha 1, beta 0, no bias or activation).
 int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int lda, const void* B,
-        int ldb, float beta, void* C, int ldc, const float* bias, int act, cudaStream_t stream) {
+        int ldb, float beta, void* C, int ldc, const float* bias, int act, cudaStream_t stream,
+        bool swiglu = false, const void* B2 = nullptr) {
   t_msg[0] = '\0';
   t_last_path = GEMM_PATH_AUTO;
   if (M < 0 || N < 0 || K < 0) return fail(GEMM_ERR_INVALID_ARG, "negative size M=%d N=%d K=%d", M, N, K);
@@ -174,10 +177,11 @@ int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int 
                 lda, ldb, ldc, K, N);
   if (M == 0 || N == 0) return GEMM_OK;
   if (C == nullptr) return fail(GEMM_ERR_INVALID_ARG, "C is NULL");
-  if (K > 0 && (A == nullptr || B == nullptr)) return fail(GEMM_ERR_INVALID_ARG, "A or B is NULL");
+  if (K > 0 && (A == nullptr || B == nullptr || (swiglu && B2 == nullptr)))
+    return fail(GEMM_ERR_INVALID_ARG, "A or B is NULL");
   const size_t in_sz = in == Elem::F32 ? 4 : 2, out_sz = out == Elem::F32 ? 4 : 2;
   if ((reinterpret_cast<uintptr_t>(A) % in_sz) || (reinterpret_cast<uintptr_t>(B) % in_sz) ||
-      (reinterpret_cast<uintptr_t>(C) % out_sz))
+      (reinterpret_cast<uintptr_t>(B2) % in_sz) || (reinterpret_cast<uintptr_t>(C) % out_sz))
     return fail(GEMM_ERR_MISALIGNED, "a matrix pointer is not aligned to its element size");
   if (act < kActNone || act > kActGelu) return fail(GEMM_ERR_INVALID_ARG, "unknown activation %d", act);
   if (reinterpret_cast<uintptr_t>(bias) % sizeof(float))
@@ -195,9 +199,11 @@ int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int 
   a.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   a.bias = bias;
   a.act = act;
+  a.B2 = B2;
+  a.swiglu = swiglu ? 1 : 0;
 
-  const bool tma_ok = K > 0 && aligned16(A) && aligned16(B) && ((size_t)lda * in_sz) % 16 == 0 &&
-                      ((size_t)ldb * in_sz) % 16 == 0;
+  const bool tma_ok = K > 0 && aligned16(A) && aligned16(B) && (!swiglu || aligned16(B2)) &&
+                      ((size_t)lda * in_sz) % 16 == 0 && ((size_t)ldb * in_sz) % 16 == 0;
   int path;
   const int forced = t_forced_path;
   if (forced == GEMM_PATH_AUTO) {
@@ -208,14 +214,14 @@ int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int 
   } else {
     path = forced;
     const bool fits = forced == GEMM_PATH_GENERIC ||
-                      (tma_ok && ((forced == GEMM_PATH_F32_SIMT && in == Elem::F32) ||
+                      (tma_ok && ((forced == GEMM_PATH_F32_SIMT && in == Elem::F32 && !swiglu) ||
                                   (forced == GEMM_PATH_BF16_TC && in == Elem::BF16) ||
                                   (forced == GEMM_PATH_SKINNY && in == Elem::BF16 && M <= kSkMaxM)));
     if (!fits) return fail(GEMM_ERR_UNSUPPORTED, "forced path %d cannot run this call", forced);
   }
 
   int err = cudaSuccess;
-  const CUtensorMap *mA = nullptr, *mB = nullptr;
+  const CUtensorMap *mA = nullptr, *mB = nullptr, *mB2 = nullptr;
   switch (path) {
     case GEMM_PATH_GENERIC:
       err = launch_generic(a, stream);
@@ -236,6 +242,17 @@ int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int 
       if ((rc = make_map(B, N, K, (uint64_t)ldb * 2, 64, kTcBK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                          CU_TENSOR_MAP_SWIZZLE_128B, &mB)) != GEMM_OK)
         return rc;
+      if (swiglu) {
+        if ((rc = make_map(B2, N, K, (uint64_t)ldb * 2, 64, kTcBK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                           CU_TENSOR_MAP_SWIZZLE_128B, &mB2)) != GEMM_OK)
+          return rc;
+        err = launch_bf16_swiglu_pair(a, mA, mB, mB2, dev->num_sms, stream);
+        if (err == cudaSuccess) {
+          t_last_bn = 128;  // C columns per tile
+          t_last_pair = 2;
+        }
+        break;
+      }
     {
       int pair = 1, bn = 256;
       choose_tc_config(M, N, dev->num_sms, &pair, &bn);
@@ -263,7 +280,10 @@ int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int 
       if ((rc = make_map(B, N, K, (uint64_t)ldb * 2, 64, kSkBK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                          CU_TENSOR_MAP_SWIZZLE_128B, &mB)) != GEMM_OK)
         return rc;
-      err = launch_skinny(a, mA, mB, dev->num_sms, stream);
+      if (swiglu && (rc = make_map(B2, N, K, (uint64_t)ldb * 2, 64, kSkBK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                   CU_TENSOR_MAP_SWIZZLE_128B, &mB2)) != GEMM_OK)
+        return rc;
+      err = launch_skinny(a, mA, mB, mB2, dev->num_sms, stream);
       break;
     default:
       return fail(GEMM_ERR_INVALID_ARG, "unknown path %d", path);
@@ -313,6 +333,12 @@ int gemm_bf16_f32out(int M, int N, int K, float alpha, const gemm_bf16_t* A, int
                      cudaStream_t stream) {
   return g3::run(Elem::BF16, Elem::F32, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, nullptr,
                  g3::kActNone, stream);
+}
+
+int gemm_bf16_swiglu(int M, int N, int K, const gemm_bf16_t* A, int lda, const gemm_bf16_t* Bgate,
+                     const gemm_bf16_t* Bup, int ldb, gemm_bf16_t* C, int ldc, cudaStream_t stream) {
+  return g3::run(Elem::BF16, Elem::BF16, M, N, K, 1.f, A, lda, Bgate, ldb, 0.f, C, ldc, nullptr,
+                 g3::kActNone, stream, /*swiglu=*/true, Bup);
 }
 
 int gemm_f32_ex(int M, int N, int K, float alpha, const float* A, int lda, const float* B, int ldb,

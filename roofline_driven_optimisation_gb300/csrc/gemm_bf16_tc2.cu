@@ -25,6 +25,14 @@
 // half-width tile costs about 0.58 of a full one (measured per-column costs
 // of the 128- and 256-wide pair tiles), so the last wave shrinks from a whole
 // tile-time to a bit over half of one, with nothing to reduce afterwards.
+//
+// SwiGLU variant (SW, BN = 256): C = silu(A*Bgate) * (A*Bup) on C tiles of
+// 256 x 128.  Each CTA's half of the MMA's B operand is 64 columns of Bgate
+// (box 0) and the same 64 columns of Bup (box 1), so the MMA is the 256-wide
+// one above and accumulator column x holds output column
+// n0 + 64*(x / 128) + x % 64 of the gate (x % 128 < 64) or of the up
+// projection; the epilogue pairs them and applies silu(g) * u.  The
+// intermediate products never leave the chip and A is read once for both.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -74,10 +82,14 @@ __device__ __forceinline__ void pair_tile_coords(int tile, const TcParams& p, in
   n0 = (local / gsize) * BN;
 }
 
-template <int BN, bool OUT_BF16>
+// mapB2 is read only by the SwiGLU variant (the up-projection).
+template <int BN, bool OUT_BF16, bool SW>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_bf16_tc2_kernel(const __grid_constant__ CUtensorMap mapA,
-                         const __grid_constant__ CUtensorMap mapB, const TcParams p) {
+                         const __grid_constant__ CUtensorMap mapB,
+                         const __grid_constant__ CUtensorMap mapB2, const TcParams p) {
+  static_assert(!SW || (BN == 256 && OUT_BF16), "SwiGLU runs on the 256-wide bf16 instance");
+  constexpr int OUT_BN = SW ? BN / 2 : BN;  // C columns per tile
   using Cfg = PairCfg<BN>;
   constexpr int STAGES = Cfg::STAGES;
   constexpr int STAGE_BYTES = Cfg::STAGE_BYTES;
@@ -110,10 +122,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int n_items = n_dp + (pair_id < p.half_tiles ? 1 : 0);
   auto item = [&](int i, int& m0, int& n0, int& bn) {
     if (i < n_dp) {
-      pair_tile_coords<BN>(pair_id + i * num_pairs, p, m0, n0);
+      pair_tile_coords<OUT_BN>(pair_id + i * num_pairs, p, m0, n0);
       bn = BN;
     } else {
-      pair_tile_coords<BN>(p.dp_tiles + pair_id / 2, p, m0, n0);
+      pair_tile_coords<OUT_BN>(p.dp_tiles + pair_id / 2, p, m0, n0);
       bn = BN / 2;
       n0 += (pair_id & 1) * (BN / 2);
     }
@@ -146,6 +158,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (elect_one_sync()) {
       tma_prefetch_desc(&mapA);
       tma_prefetch_desc(&mapB);
+      if (SW) tma_prefetch_desc(&mapB2);
       uint32_t issued = 0, issued_par = 0;
       int stage = 0;
       uint32_t phase = 0;
@@ -154,7 +167,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         int m0, n0, bn;
         item(i, m0, n0, bn);
         const int a_row = m0 + (int)rank * BM_CTA;
-        const int b_col = n0 + (int)rank * (bn / 2);
+        const int b_col = n0 + (int)rank * (SW ? OUT_BN / 2 : bn / 2);
         const int b_boxes = bn / 2 / 64;
         const uint32_t tx_bytes = 2u * (A_STAGE_BYTES + b_boxes * B_BOX_BYTES);
         for (int kt = 0; kt < p.k_tiles; ++kt) {
@@ -169,8 +182,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (leader) mbar_arrive_expect_tx(full_bar(stage), tx_bytes);
           tma_load_2d_pair(a_tile(stage), &mapA, lead_full, kt * BK, a_row);
           for (int j = 0; j < b_boxes; ++j)
-            tma_load_2d_pair(b_tile(stage) + j * B_BOX_BYTES, &mapB, lead_full, b_col + j * 64,
-                             kt * BK);
+            tma_load_2d_pair(b_tile(stage) + j * B_BOX_BYTES, (SW && j == 1) ? &mapB2 : &mapB,
+                             lead_full, SW ? b_col : b_col + j * 64, kt * BK);
           issued |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -266,16 +279,37 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const long long m = (long long)m0 + rank * BM_CTA + quarter * 32 + lane;
       const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+      if constexpr (SW) {
 #pragma unroll 1
-      for (int c = 0; c < bn / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(t_row + c * 32, r);
-        tc_wait_ld();
-        if (c == bn / 32 - 1) {
-          tc_fence_before();
-          mbar_arrive_remote(acc == 0 ? lead_tempty0 : lead_tempty1);
+        for (int c = 0; c < OUT_BN / 32; ++c) {
+          // output columns n0 + 32c .. +32: gate at accumulator column
+          // 128*(c/2) + 32*(c%2), the up projection 64 columns further on
+          const uint32_t g_col = (uint32_t)(128 * (c / 2) + 32 * (c % 2));
+          uint32_t r[32], u[32];
+          tmem_ld_32x32b_x32(t_row + g_col, r);
+          tmem_ld_32x32b_x32(t_row + g_col + 64, u);
+          tc_wait_ld();
+          if (c == OUT_BN / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive_remote(acc == 0 ? lead_tempty0 : lead_tempty1);
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            r[j] = __float_as_uint(swiglu_combine(__uint_as_float(r[j]), __uint_as_float(u[j])));
+          if (m < a.M && n0 + c * 32 < a.N) store_row32<OUT_BF16>(p, m, (long long)n0 + c * 32, r);
         }
-        if (m < a.M && n0 + c * 32 < a.N) store_row32<OUT_BF16>(p, m, (long long)n0 + c * 32, r);
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < bn / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_row + c * 32, r);
+          tc_wait_ld();
+          if (c == bn / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive_remote(acc == 0 ? lead_tempty0 : lead_tempty1);
+          }
+          if (m < a.M && n0 + c * 32 < a.N) store_row32<OUT_BF16>(p, m, (long long)n0 + c * 32, r);
+        }
       }
       if (++acc == 2) {
         acc = 0;
@@ -297,16 +331,17 @@ struct PairLaunchInfo {
   int max_clusters = 0;
 };
 
-template <int BN, bool OUT_BF16>
+template <int BN, bool OUT_BF16, bool SW>
 int launch_pair_impl(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
-                     int num_sms, cudaStream_t s, int* schedule) {
+                     const CUtensorMap* mapB2, int num_sms, cudaStream_t s, int* schedule) {
+  constexpr int OUT_BN = SW ? BN / 2 : BN;
   using Cfg = PairCfg<BN>;
   static PairLaunchInfo info[64];
   static std::mutex mu;
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  auto kernel = gemm_bf16_tc2_kernel<BN, OUT_BF16>;
+  auto kernel = gemm_bf16_tc2_kernel<BN, OUT_BF16, SW>;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -337,7 +372,7 @@ int launch_pair_impl(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorM
   TcParams p;
   p.a = a;
   p.tiles_m = (a.M + BM - 1) / BM;
-  p.tiles_n = (a.N + BN - 1) / BN;
+  p.tiles_n = (a.N + OUT_BN - 1) / OUT_BN;
   const long long tiles = (long long)p.tiles_m * p.tiles_n;
   if (tiles <= 0) return cudaSuccess;
   if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
@@ -348,7 +383,7 @@ int launch_pair_impl(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorM
   const int pairs = info[dev].max_clusters;
   const long long rem = tiles % pairs;
   int clusters;
-  if (BN == 256 && split_tiles_enabled() && rem > 0 && 2 * rem <= pairs) {
+  if (!SW && BN == 256 && split_tiles_enabled() && rem > 0 && 2 * rem <= pairs) {
     p.dp_tiles = (int)(tiles - rem);
     p.half_tiles = (int)(2 * rem);
     clusters = pairs;
@@ -360,7 +395,7 @@ int launch_pair_impl(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorM
     *schedule = 2;
   }
   cfg.gridDim = dim3(2 * clusters, 1, 1);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, *mapA, *mapB, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, *mapA, *mapB, SW ? *mapB2 : *mapB, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -371,12 +406,19 @@ int launch_bf16_tc_pair(const GemmArgs& a, const CUtensorMap* mapA, const CUtens
                         int num_sms, cudaStream_t s, int* schedule) {
   const bool bf16 = a.out == Elem::BF16;
   if (bn == 256)
-    return bf16 ? launch_pair_impl<256, true>(a, mapA, mapB, num_sms, s, schedule)
-                : launch_pair_impl<256, false>(a, mapA, mapB, num_sms, s, schedule);
+    return bf16 ? launch_pair_impl<256, true, false>(a, mapA, mapB, nullptr, num_sms, s, schedule)
+                : launch_pair_impl<256, false, false>(a, mapA, mapB, nullptr, num_sms, s, schedule);
   if (bn == 128)
-    return bf16 ? launch_pair_impl<128, true>(a, mapA, mapB, num_sms, s, schedule)
-                : launch_pair_impl<128, false>(a, mapA, mapB, num_sms, s, schedule);
+    return bf16 ? launch_pair_impl<128, true, false>(a, mapA, mapB, nullptr, num_sms, s, schedule)
+                : launch_pair_impl<128, false, false>(a, mapA, mapB, nullptr, num_sms, s, schedule);
   return cudaErrorInvalidValue;
+}
+
+int launch_bf16_swiglu_pair(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
+                            const CUtensorMap* mapB2, int num_sms, cudaStream_t s) {
+  if (!a.swiglu || a.out != Elem::BF16 || mapB2 == nullptr) return cudaErrorInvalidValue;
+  int schedule = 0;
+  return launch_pair_impl<256, true, true>(a, mapA, mapB, mapB2, num_sms, s, &schedule);
 }
 
 }  // namespace g3

@@ -32,22 +32,31 @@ __device__ __forceinline__ float from_f32<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
 
-template <typename TI, typename TO>
+// SWIGLU: a second B (a.B2) and accumulator; C = silu(A*B) * (A*B2).
+template <typename TI, typename TO, bool SWIGLU>
 __global__ void __launch_bounds__(256) gemm_generic_kernel(GemmArgs a, int tiles_n) {
   __shared__ float As[GK][GT + 1];  // As[k][m]
   __shared__ float Bs[GK][GT + 1];  // Bs[k][n]
+  __shared__ float Bs2[SWIGLU ? GK : 1][GT + 1];
   const TI* A = static_cast<const TI*>(a.A);
   const TI* B = static_cast<const TI*>(a.B);
+  const TI* B2 = static_cast<const TI*>(a.B2);
   TO* C = static_cast<TO*>(a.C);
   const int tile = blockIdx.x;
   const long long m0 = (long long)(tile / tiles_n) * GT;
   const long long n0 = (long long)(tile % tiles_n) * GT;
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-  float acc[4][4];
+  float acc[4][4], acc2[SWIGLU ? 4 : 1][SWIGLU ? 4 : 1];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  if (SWIGLU) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc2[SWIGLU ? i : 0][SWIGLU ? j : 0] = 0.f;
+  }
 
   for (long long k0 = 0; k0 < a.K; k0 += GK) {
 #pragma unroll
@@ -59,6 +68,7 @@ __global__ void __launch_bounds__(256) gemm_generic_kernel(GemmArgs a, int tiles
       const int bk = idx / GT, bn = idx % GT;
       const long long hk = k0 + bk, hn = n0 + bn;
       Bs[bk][bn] = (hk < a.K && hn < a.N) ? to_f32<TI>(B[hk * a.ldb + hn]) : 0.f;
+      if (SWIGLU) Bs2[SWIGLU ? bk : 0][bn] = (hk < a.K && hn < a.N) ? to_f32<TI>(B2[hk * a.ldb + hn]) : 0.f;
     }
     __syncthreads();
 #pragma unroll
@@ -72,6 +82,16 @@ __global__ void __launch_bounds__(256) gemm_generic_kernel(GemmArgs a, int tiles
       for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+      if (SWIGLU) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) bv[j] = Bs2[SWIGLU ? kk : 0][tx + 16 * j];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            acc2[SWIGLU ? i : 0][SWIGLU ? j : 0] =
+                fmaf(av[i], bv[j], acc2[SWIGLU ? i : 0][SWIGLU ? j : 0]);
+      }
     }
     __syncthreads();
   }
@@ -83,6 +103,10 @@ __global__ void __launch_bounds__(256) gemm_generic_kernel(GemmArgs a, int tiles
     for (int j = 0; j < 4; ++j) {
       const long long n = n0 + tx + 16 * j;
       if (n >= a.N) continue;
+      if (SWIGLU) {
+        C[m * a.ldc + n] = from_f32<TO>(swiglu_combine(acc[i][j], acc2[SWIGLU ? i : 0][SWIGLU ? j : 0]));
+        continue;
+      }
       float v = a.alpha * acc[i][j];
       if (a.beta != 0.f) v = fmaf(a.beta, to_f32<TO>(C[m * a.ldc + n]), v);
       C[m * a.ldc + n] = from_f32<TO>(finish(a, v, n));
@@ -99,14 +123,20 @@ int launch_generic(const GemmArgs& a, cudaStream_t s) {
   if (tiles <= 0) return cudaSuccess;
   if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   dim3 grid((unsigned)tiles), block(256);
-  if (a.in == Elem::F32 && a.out == Elem::F32)
-    gemm_generic_kernel<float, float><<<grid, block, 0, s>>>(a, (int)tiles_n);
-  else if (a.in == Elem::BF16 && a.out == Elem::BF16)
-    gemm_generic_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, block, 0, s>>>(a, (int)tiles_n);
-  else if (a.in == Elem::BF16 && a.out == Elem::F32)
-    gemm_generic_kernel<__nv_bfloat16, float><<<grid, block, 0, s>>>(a, (int)tiles_n);
-  else
+  if (a.swiglu) {
+    if (a.in == Elem::BF16 && a.out == Elem::BF16)
+      gemm_generic_kernel<__nv_bfloat16, __nv_bfloat16, true><<<grid, block, 0, s>>>(a, (int)tiles_n);
+    else
+      return cudaErrorInvalidValue;
+  } else if (a.in == Elem::F32 && a.out == Elem::F32) {
+    gemm_generic_kernel<float, float, false><<<grid, block, 0, s>>>(a, (int)tiles_n);
+  } else if (a.in == Elem::BF16 && a.out == Elem::BF16) {
+    gemm_generic_kernel<__nv_bfloat16, __nv_bfloat16, false><<<grid, block, 0, s>>>(a, (int)tiles_n);
+  } else if (a.in == Elem::BF16 && a.out == Elem::F32) {
+    gemm_generic_kernel<__nv_bfloat16, float, false><<<grid, block, 0, s>>>(a, (int)tiles_n);
+  } else {
     return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 

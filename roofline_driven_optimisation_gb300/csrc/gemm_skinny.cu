@@ -29,6 +29,12 @@
 //     set-up, TMEM allocation and an L2 prefetch of the first weight stages
 //     overlap the previous kernel on the stream, and every read into the SM
 //     waits on griddepcontrol.wait.
+// SwiGLU variant (SW): C = silu(A*Bgate) * (A*Bup) for 64 output columns per
+// CTA.  The MMA's 128 rows are those 64 columns of Bgate followed by the
+// same 64 columns of Bup (one TMA box from each weight), so the stage size,
+// the MMA and the TMEM layout are unchanged; the two halves of the
+// accumulator meet in the reduction, which applies silu(g) * u before the
+// single rounding to bf16.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -78,6 +84,11 @@ __device__ __forceinline__ float raw_to_float(uint32_t w) {
   return OUT_BF16 ? __uint_as_float(w << 16) : __uint_as_float(w);
 }
 
+// SwiGLU output: silu(gate) * up rounded once to bf16
+__device__ __forceinline__ void store_swiglu(const GemmArgs& a, int m, long long n, float gate, float up) {
+  static_cast<__nv_bfloat16*>(a.C)[(long long)m * a.ldc + n] = __float2bfloat16_rn(swiglu_combine(gate, up));
+}
+
 template <bool OUT_BF16>
 __device__ __forceinline__ void store_c(const GemmArgs& a, int m, long long n, float v) {
   v = finish(a, v, n);
@@ -95,10 +106,34 @@ struct SkinnyParams {
   int c_vec;       // unused by the scalar stores; kept for symmetry
 };
 
-template <bool OUT_BF16>
+// Sum over the S ranks of the cluster, in rank order, of the 16-byte piece
+// at shared address `off` of each rank's partial tile; all S loads are in
+// flight before the first add.
+__device__ __forceinline__ float4 sum_ranks(uint32_t off, int split) {
+  float4 part[MAX_SPLIT];
+#pragma unroll
+  for (int q = 0; q < MAX_SPLIT; ++q)
+    if (q < split) part[q] = ld_dsmem_f32x4(map_to_rank(off, (uint32_t)q));
+  float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int q = 0; q < MAX_SPLIT; ++q)
+    if (q < split) {
+      sum.x += part[q].x;
+      sum.y += part[q].y;
+      sum.z += part[q].z;
+      sum.w += part[q].w;
+    }
+  return sum;
+}
+
+// mapB2 is read only by the SwiGLU variant (the up-projection).
+template <bool OUT_BF16, bool SW>
 __global__ void __launch_bounds__(THREADS, 2)
     gemm_skinny_kernel(const __grid_constant__ CUtensorMap mapA,
-                       const __grid_constant__ CUtensorMap mapB, const SkinnyParams p) {
+                       const __grid_constant__ CUtensorMap mapB,
+                       const __grid_constant__ CUtensorMap mapB2, const SkinnyParams p) {
+  static_assert(!SW || OUT_BF16, "the SwiGLU variant writes bf16");
+  constexpr int OUT_COLS = SW ? BN / 2 : BN;  // C columns per CTA
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -118,7 +153,10 @@ __global__ void __launch_bounds__(THREADS, 2)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const GemmArgs& a = p.a;
   const int rank = (int)cluster_ctarank();          // position along K inside the cluster
-  const int n0 = blockIdx.y * BN;
+  const int n0 = blockIdx.y * OUT_COLS;
+  // TMA box j of a stage: 64 columns of B (or, SwiGLU, of Bgate then Bup)
+  auto box_map = [&](int j) { return (SW && j == 1) ? &mapB2 : &mapB; };
+  auto box_col = [&](int j) { return SW ? n0 : n0 + j * 64; };
   const int kt_begin = (int)((long long)p.k_tiles * rank / p.split);
   const int kt_end = (int)((long long)p.k_tiles * (rank + 1) / p.split);
   const int my_kt = kt_end - kt_begin;
@@ -146,10 +184,11 @@ __global__ void __launch_bounds__(THREADS, 2)
     // stages of this CTA's weights into L2 (a prefetch only: the real loads
     // come after the wait and see whatever is in memory then).
     tma_prefetch_desc(&mapB);
+    if (SW) tma_prefetch_desc(&mapB2);
     const int pre = my_kt < STAGES ? my_kt : STAGES;
     for (int kt = kt_begin; kt < kt_begin + pre; ++kt)
 #pragma unroll
-      for (int j = 0; j < BN / 64; ++j) tma_prefetch_l2_2d(&mapB, n0 + j * 64, kt * BK);
+      for (int j = 0; j < BN / 64; ++j) tma_prefetch_l2_2d(box_map(j), box_col(j), kt * BK);
   }
   griddep_wait();  // inputs may come from the previous kernel on the stream
 
@@ -158,14 +197,14 @@ __global__ void __launch_bounds__(THREADS, 2)
   // thread -- in particular not the TMA producer -- waits for them here).
   // split == 1: column n0 + threadIdx.x, rows 0..M-1.  split > 1: items of 4
   // columns of the columns this rank finishes.
-  const int cols = BN / p.split;
+  const int cols = OUT_COLS / p.split;
   const int groups = cols / 4;
   const int items = a.M * groups;
   uint32_t cpre[MN];  // split == 1: one per row; split > 1: RED_ITEMS x 4
   static_assert(RED_ITEMS * 4 <= MN, "prefetch registers");
 #pragma unroll
   for (int j = 0; j < MN; ++j) cpre[j] = 0u;
-  if (a.beta != 0.f) {
+  if (!SW && a.beta != 0.f) {
     if (p.split == 1) {
       const long long n = (long long)n0 + threadIdx.x;
 #pragma unroll
@@ -190,6 +229,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     if (elect_one_sync() && my_kt > 0) {
       tma_prefetch_desc(&mapA);
       tma_prefetch_desc(&mapB);
+      if (SW) tma_prefetch_desc(&mapB2);
       const uint64_t stream_policy = l2_policy_evict_first();
       // bit s of `issued`: slot s has had a copy issued; bit s of
       // `issued_par`: the phase parity of its latest copy
@@ -205,7 +245,7 @@ __global__ void __launch_bounds__(THREADS, 2)
         mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
 #pragma unroll
         for (int j = 0; j < BN / 64; ++j)
-          tma_load_2d_hint(b_tile(stage) + j * B_BOX_BYTES, &mapB, full_bar(stage), n0 + j * 64,
+          tma_load_2d_hint(b_tile(stage) + j * B_BOX_BYTES, box_map(j), full_bar(stage), box_col(j),
                            kt * BK, stream_policy);
         tma_load_2d(a_tile(stage), &mapA, full_bar(stage), kt * BK, 0);
         issued |= 1u << stage;
@@ -282,7 +322,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     for (int j = 0; j < 16; ++j) r[j] = 0u;
   }
   if (threadIdx.x == 0) griddep_launch_dependents();
-  if (p.split == 1) {
+  if (!SW && p.split == 1) {
     // the whole K range is in this CTA: column n0 + threadIdx.x of C is in
     // this thread's registers, one value per activation row
     const long long n = (long long)n0 + threadIdx.x;
@@ -306,27 +346,23 @@ __global__ void __launch_bounds__(THREADS, 2)
         const int m = it / groups;
         const int nl = rank * cols + (it % groups) * 4;
         const uint32_t off = partial_addr + (uint32_t)(m * BN + nl) * 4u;
-        // all ranks' 16-byte pieces in flight at once, then summed in rank order
-        float4 part[MAX_SPLIT];
-#pragma unroll
-        for (int q = 0; q < MAX_SPLIT; ++q)
-          if (q < p.split) part[q] = ld_dsmem_f32x4(map_to_rank(off, (uint32_t)q));
-        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int q = 0; q < MAX_SPLIT; ++q)
-          if (q < p.split) {
-            sum.x += part[q].x;
-            sum.y += part[q].y;
-            sum.z += part[q].z;
-            sum.w += part[q].w;
-          }
         const long long n = (long long)n0 + nl;
+        const float4 sum = sum_ranks(off, p.split);
         const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
+        if (SW) {
+          // the up-projection of the same columns is 64 rows further down D^T
+          const float4 up = sum_ranks(off + (uint32_t)(BN / 2) * 4u, p.split);
+          const float uv[4] = {up.x, up.y, up.z, up.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (n + e < a.N)
-            store_c<OUT_BF16>(a, m, n + e,
-                              fmaf(a.alpha, sv[e], a.beta * raw_to_float<OUT_BF16>(cpre[j * 4 + e])));
+          for (int e = 0; e < 4; ++e)
+            if (n + e < a.N) store_swiglu(a, m, n + e, sv[e], uv[e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (n + e < a.N)
+              store_c<OUT_BF16>(a, m, n + e,
+                                fmaf(a.alpha, sv[e], a.beta * raw_to_float<OUT_BF16>(cpre[j * 4 + e])));
+        }
       }
     }
     cluster_sync();  // no rank leaves while others may still read its partial
@@ -356,14 +392,15 @@ int choose_split(int tiles_n, int k_tiles, int num_sms) {
   return s;
 }
 
-template <bool OUT_BF16>
-int launch_impl(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB, int num_sms,
-                cudaStream_t s) {
+template <bool OUT_BF16, bool SW>
+int launch_impl(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
+                const CUtensorMap* mapB2, int num_sms, cudaStream_t s) {
+  constexpr int OUT_COLS = SW ? BN / 2 : BN;
   static int attr_done_mask = 0;
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 31 && !(attr_done_mask & (1 << dev))) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_skinny_kernel<OUT_BF16>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_skinny_kernel<OUT_BF16, SW>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_done_mask |= (1 << dev);
@@ -371,7 +408,7 @@ int launch_impl(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* m
   SkinnyParams p;
   p.a = a;
   p.k_tiles = (a.K + BK - 1) / BK;
-  const int tiles_n = (a.N + BN - 1) / BN;
+  const int tiles_n = (a.N + OUT_COLS - 1) / OUT_COLS;
   if (tiles_n <= 0 || a.M <= 0) return cudaSuccess;
   if (tiles_n > 65535) return cudaErrorInvalidConfiguration;
   p.split = choose_split(tiles_n, p.k_tiles, num_sms);
@@ -391,17 +428,22 @@ int launch_impl(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* m
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<OUT_BF16>, *mapA, *mapB, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<OUT_BF16, SW>, *mapA, *mapB,
+                                     SW ? *mapB2 : *mapB, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 }  // namespace
 
-int launch_skinny(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB, int num_sms,
-                  cudaStream_t s) {
-  if (a.out == Elem::BF16) return launch_impl<true>(a, mapA, mapB, num_sms, s);
-  return launch_impl<false>(a, mapA, mapB, num_sms, s);
+int launch_skinny(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
+                  const CUtensorMap* mapB2, int num_sms, cudaStream_t s) {
+  if (a.swiglu) {
+    if (a.out != Elem::BF16 || mapB2 == nullptr) return cudaErrorInvalidValue;
+    return launch_impl<true, true>(a, mapA, mapB, mapB2, num_sms, s);
+  }
+  if (a.out == Elem::BF16) return launch_impl<true, false>(a, mapA, mapB, nullptr, num_sms, s);
+  return launch_impl<false, false>(a, mapA, mapB, nullptr, num_sms, s);
 }
 
 }  // namespace g3

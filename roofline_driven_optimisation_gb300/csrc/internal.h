@@ -27,6 +27,8 @@ struct GemmArgs {
   uint64_t timeout_ns;  // bound on any single wait inside a kernel
   const float* bias;    // N fp32 values added to every row of C, or null
   int act;              // Act applied last
+  const void* B2;       // SwiGLU: the up-projection (K x N, leading dimension ldb), else null
+  int swiglu;           // 1: C = silu(A*B) * (A*B2) (alpha 1, beta 0, no bias)
 };
 
 // Location codes recorded with a device timeout (status[1]).
@@ -75,11 +77,16 @@ constexpr int kTcBM = 128, kTcBK = 64;
 bool split_tiles_enabled();
 int launch_bf16_tc_pair(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB, int bn,
                         int num_sms, cudaStream_t s, int* schedule);
+// SwiGLU on CTA pairs (a.swiglu): C tiles of 256 x 128; each CTA's B operand
+// is 64 columns of Bgate (mapB) and the same 64 columns of Bup (mapB2).
+int launch_bf16_swiglu_pair(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
+                            const CUtensorMap* mapB2, int num_sms, cudaStream_t s);
 
 // Skinny (M <= 16) split-K kernel: TMA tiles of B (64 n x 64 k) and A
-// (64 k x 16 rows), 128-byte swizzle.
+// (64 k x 16 rows), 128-byte swizzle.  mapB2 (the up-projection) is used
+// when a.swiglu is set, and may be null otherwise.
 int launch_skinny(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
-                  int num_sms, cudaStream_t s);
+                  const CUtensorMap* mapB2, int num_sms, cudaStream_t s);
 constexpr int kSkMaxM = 16, kSkBN = 128, kSkBK = 64;
 
 int launch_selftest_wait(int* status, uint64_t timeout_ns, cudaStream_t s);

@@ -146,3 +146,22 @@ def random_matrix(rows: int, cols: int, seed: int, dtype: str = "f32",
     else:
         raise ValueError(dist)
     return round_to(x, dtype)
+
+
+@dataclasses.dataclass
+class SwigluCase:
+    A: torch.Tensor        # M x K activations, bf16, CPU
+    Bgate: torch.Tensor    # K x N gate projection, bf16
+    Bup: torch.Tensor      # K x N up projection, bf16
+
+
+def make_swiglu(M: int, N: int = LLAMA7B_WEIGHTS["gate"][1], K: int = LLAMA7B_WEIGHTS["gate"][0],
+                seed: int = 5) -> SwigluCase:
+    """Operands of the fused FFN gate/up pair: activations N(0,1), both
+    weights N(0, 0.02) (the LLaMA recipe of the other workloads), bf16."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    A = round_to(torch.randn((M, K), generator=gen, dtype=torch.float32), "bf16")
+    Bg = round_to(torch.randn((K, N), generator=gen, dtype=torch.float32) * 0.02, "bf16")
+    Bu = round_to(torch.randn((K, N), generator=gen, dtype=torch.float32) * 0.02, "bf16")
+    return SwigluCase(A, Bg, Bu)

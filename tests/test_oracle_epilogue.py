@@ -55,3 +55,53 @@ def test_swiglu_reduces_to_products():
     assert np.allclose(got, g / (1 + np.exp(-g)) * u, rtol=1e-15, atol=0)
     # a zero up-projection gives zero; an identity-like gate at large g gives g*u
     assert np.array_equal(E.swiglu(A, Bg, np.zeros_like(Bu)), np.zeros((4, 5)))
+
+
+def test_swiglu_worked_values():
+    # K = 1: g = 2, u = 3 gives silu(2) * 3 with sigmoid(2) = 0.8807970779778823;
+    # the gate, not the up projection, goes through silu (swapped: 5.7154...)
+    A = np.array([[2.0]])
+    got = E.swiglu(A, np.array([[1.0]]), np.array([[1.5]]))
+    assert abs(got[0, 0] - 2.0 * 0.8807970779778823 * 3.0) < 1e-14
+    # a very negative gate switches the output off whatever the up projection
+    assert abs(E.swiglu(A, np.array([[-30.0]]), np.array([[100.0]]))[0, 0]) < 1e-20
+
+
+def test_silu_slope_bound():
+    z = np.linspace(-20, 20, 400001)
+    s = 1.0 / (1.0 + np.exp(-z))
+    slope = s * (1.0 + z * (1.0 - s))
+    assert slope.max() <= E.SILU_SLOPE_BOUND
+    assert slope.max() > 1.09            # the bound is tight, not a loose guess
+    assert abs(z[slope.argmax()] - 2.40) < 0.01
+
+
+def test_swiglu_error_scale_closed_form():
+    # g = 1 - 1 = 0 with sum|A||Bg| = 2; u = 2 + 3 = 5 with sum|A||Bu| = 5:
+    # scale = 1.1 * 5 * 2 + silu(0) * 5 = 11 -- the gate term alone carries it
+    A = np.array([[1.0, 1.0]])
+    s = E.swiglu_error_scale(A, np.array([[1.0], [-1.0]]), np.array([[2.0], [3.0]]))
+    assert abs(s - 11.0) < 1e-12
+    # u = 0 exactly: only the up term remains, silu(2) * sum|A||Bu| = silu(2) * 2
+    s = E.swiglu_error_scale(A, np.array([[1.0], [1.0]]), np.array([[1.0], [-1.0]]))
+    assert abs(s - 2.0 * 0.8807970779778823 * 2.0) < 1e-12
+
+
+def test_swiglu_error_scale_bounds_perturbations():
+    # perturbing g and u by at most eps * sum|A||B| elementwise moves the
+    # output by at most eps * scale (first order), and |output| <= scale
+    rng = np.random.default_rng(11)
+    A = rng.standard_normal((6, 40))
+    Bg = rng.standard_normal((40, 7)) * 0.3
+    Bu = rng.standard_normal((40, 7)) * 0.3
+    scale = E.swiglu_error_scale(A, Bg, Bu)
+    g, u = A @ Bg, A @ Bu
+    Sg, Su = np.abs(A) @ np.abs(Bg), np.abs(A) @ np.abs(Bu)
+    out = E.activate(g, E.SILU) * u
+    assert np.abs(out).max() <= scale
+    eps = 1e-7
+    for _ in range(20):
+        dg = rng.uniform(-1, 1, g.shape) * eps * Sg
+        du = rng.uniform(-1, 1, u.shape) * eps * Su
+        moved = E.activate(g + dg, E.SILU) * (u + du) - out
+        assert np.abs(moved).max() <= eps * scale * (1 + 1e-6)
