@@ -47,12 +47,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per launch measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum)
 # for each kernel source file, valid only while the file hashes to `sha256`.
 NCU_TRAFFIC = {
-    # profiles/sgemm_tma_kernel_fp32_4096.md: 410.6 MB read + 54.0 MB written
-    "gemm_f32_simt.cu": {"sha256": "31bef2fda14d2f2bce126b0c4d3c86dbde56f170dd9a8ba320f2c93586c46560",
-                         "bytes_per_launch": 464635136},
-    # profiles/gemm_bf16_tc2_kernel_bf16_8192.md, 4096^3 capture: 78.1 MB + 11.1 MB
-    "gemm_bf16_tc2.cu": {"sha256": "754954bef5e8861ae8d1c13c9543fde47040cb59a70d799f831c19253668bf96",
-                         "bytes_per_launch": 89235968},
+    # profiles/sgemm_tma_kernel_fp32_4096.md: 414.2 MB read + 54.4 MB written
+    "gemm_f32_simt.cu": {"sha256": "0a11a053a88d77a0ccd9e81e5ccefb4122b4a71dadf7f74a22dc2ce80a278101",
+                         "bytes_per_launch": 468608000},
+    # profiles/gemm_bf16_tc2_kernel_bf16_8192.md, 4096^3 capture: 78.4 MB + 10.8 MB
+    "gemm_bf16_tc2.cu": {"sha256": "2b6a643cd4f8f8fb6f7abbdb20386e620f2d6405ed50541da379fcfbba57c7c7",
+                         "bytes_per_launch": 89199104},
 }
 
 
@@ -325,6 +325,8 @@ def run_ours(args):
     ms_step = elapsed_ms / args.steps
     value = replicas.whole_job_rate(flops_step, world, ms_step * 1e-3) / 1e12
     e2e = run_e2e(args, g, torch, dev, parts, s, world)
+    fused_ffn = measure_fused_ffn(g, torch, dev, s, hbm, bf16_peak) if rank == 0 else None
+    fma_probe = measure_fp32_fma(g, torch, dev, fp32_peak / 1e12) if rank == 0 else None
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -338,6 +340,8 @@ def run_ours(args):
                          "once per step"},
         "roofline": roofline,
         "parts": part_out,
+        "fused_ffn_swiglu": fused_ffn,
+        "fp32_fma_probe": fma_probe,
         "e2e": e2e,
         "gpu_launches": len(parts) * args.steps,
         "clocks": clocks.summary(),
@@ -391,6 +395,108 @@ def run_e2e(args, g, torch, dev, parts, s, world):
     return {"value": round(world * flops / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
             "ms_per_step": round(ms, 4), "steps": steps,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def measure_fp32_fma(g, torch, dev, formula_tflops, iters=16000, reps=3):
+    """Measured FP32 FMA rate with scalar and packed (f32x2) FMAs, against
+    the SMs x 128 lanes x 2 x clock peak the FP32 roofline uses."""
+    stream = torch.cuda.current_stream(dev)
+    sink = torch.zeros(1, dtype=torch.float32, device=dev)
+    out = {"formula_tflops": round(formula_tflops, 2)}
+    for name, packed in (("scalar", False), ("packed_f32x2", True)):
+        g.probe_fp32_fma(packed, iters, sink.data_ptr(), stream.cuda_stream)   # warm-up
+        best = 0.0
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            flops = g.probe_fp32_fma(packed, iters, sink.data_ptr(), stream.cuda_stream)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            best = max(best, flops / (e0.elapsed_time(e1) * 1e-3) / 1e12)
+        out[f"{name}_tflops"] = round(best, 2)
+        out[f"{name}_frac_of_formula"] = round(best / formula_tflops, 4)
+    return out
+
+
+def measure_fused_ffn(g, torch, dev, s, hbm, bf16_peak, reps=7):
+    """The fused FFN gate/up pair, C = silu(X Wg) * (X Wu) with the LLaMA-7B
+    shapes (K = 4096, N = 11008), against the two plain GEMMs it replaces
+    (which still leave the elementwise pass undone).  Timed with events
+    around each call, L2 flushed before every call by reading a buffer twice
+    its size (a read leaves only clean lines, so no write-back lands in the
+    timed call), median of `reps`.  Decode sizes are also timed back to back
+    over three distinct weight pairs (30 calls, events around the run), as a
+    decode loop launches them.  Not part of the step."""
+    from roofline_driven_optimisation_gb300 import inputs
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.ones(64 << 20, dtype=torch.float32, device=dev)   # 256 MB, 2x the L2
+    out = {}
+    for M in (1, 4, 16, 2048):
+        c = inputs.make_swiglu(M)
+        A, Bg, Bu = c.A.to(dev), c.Bgate.to(dev), c.Bup.to(dev)
+        K, N = A.shape[1], Bg.shape[1]
+        C, G, U = (torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(3))
+
+        def fused():
+            g.gemm_bf16_swiglu(M, N, K, A.data_ptr(), K, Bg.data_ptr(), Bu.data_ptr(), N,
+                               C.data_ptr(), N, s)
+
+        def two_gemms():
+            g.gemm_bf16(M, N, K, 1.0, A.data_ptr(), K, Bg.data_ptr(), N, 0.0, G.data_ptr(), N, s)
+            g.gemm_bf16(M, N, K, 1.0, A.data_ptr(), K, Bu.data_ptr(), N, 0.0, U.data_ptr(), N, s)
+
+        times = {"fused": [], "two": []}
+        for fn in (fused, two_gemms):
+            fn()
+        for _ in range(reps):
+            for key, fn in (("fused", fused), ("two", two_gemms)):
+                flush.sum()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                times[key].append((e0, e1))
+        torch.cuda.synchronize(dev)
+        status, where = g.device_status(s)
+        if status != 0:
+            raise RuntimeError(f"device status {status} at {where} in the fused FFN measurement")
+        ms = {k: statistics.median(a.elapsed_time(b) for a, b in v) for k, v in times.items()}
+        flops = 2 * 2 * M * N * K
+        by = 2 * M * K + 2 * 2 * K * N + 2 * M * N
+        ent = {"M": M, "N": N, "K": K, "fused_ms": round(ms["fused"], 5),
+               "two_gemms_ms": round(ms["two"], 5),
+               "speedup_vs_two_gemms": round(ms["two"] / ms["fused"], 3),
+               "fused_gbs": round(by / (ms["fused"] * 1e-3) / 1e9, 1),
+               "fused_tflops": round(flops / (ms["fused"] * 1e-3) / 1e12, 2)}
+        if M <= 16:
+            ent["frac_hbm"] = round(by / (ms["fused"] * 1e-3) / hbm, 4)
+            # back to back over three weight pairs (1.1 GB, beyond L2)
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(105)
+            copies = [(Bg, Bu)] + [tuple((torch.randn(w.shape, generator=gen, device=dev) * 0.02)
+                                         .to(w.dtype) for w in (Bg, Bu)) for _ in range(2)]
+            for wg, wu in copies:
+                g.gemm_bf16_swiglu(M, N, K, A.data_ptr(), K, wg.data_ptr(), wu.data_ptr(), N,
+                                   C.data_ptr(), N, s)
+            flush.sum()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(30):
+                wg, wu = copies[i % 3]
+                g.gemm_bf16_swiglu(M, N, K, A.data_ptr(), K, wg.data_ptr(), wu.data_ptr(), N,
+                                   C.data_ptr(), N, s)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            b2b = e0.elapsed_time(e1) / 30
+            ent["back_to_back_ms"] = round(b2b, 5)
+            ent["back_to_back_gbs"] = round(by / (b2b * 1e-3) / 1e9, 1)
+            ent["back_to_back_frac_hbm"] = round(by / (b2b * 1e-3) / hbm, 4)
+            del copies
+        else:
+            ent["frac_tensor"] = round(flops / (ms["fused"] * 1e-3) / bf16_peak, 4)
+        out[f"m{M}"] = ent
+        del A, Bg, Bu, C, G, U
+    return out
 
 
 # ----------------------------------------------------------------- CPU oracle

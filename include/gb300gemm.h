@@ -209,6 +209,10 @@ int gemm_last_tc_pair(void);
  */
 int gemm_force_split_tiles(int enable);
 
+/* For the last call on this host thread: the number of CTAs that shared the
+ * K range of one C tile (the decode kernel's cluster split), 1 if none did. */
+int gemm_last_k_split(void);
+
 /*
  * Upper bound, in nanoseconds, on any single wait inside a kernel launched
  * later by this process (default 1e9).  After it a kernel records

@@ -41,7 +41,8 @@ EXPORTS = ("gemm_f32", "gemm_bf16", "gemm_bf16_f32out", "gemm_f32_ex", "gemm_bf1
            "gemm_bf16_f32out_ex", "gemm_bf16_swiglu", "gemm_get_last_error",
            "gemm_device_status", "gemm_force_path", "gemm_last_path", "gemm_force_tile_n",
            "gemm_last_tile_n", "gemm_force_tc_pair", "gemm_last_tc_pair", "gemm_force_split_tiles",
-           "gemm_set_wait_timeout_ns", "gemm_selftest_wait_timeout")
+           "gemm_last_k_split", "gemm_set_wait_timeout_ns", "gemm_selftest_wait_timeout",
+           "gemm_probe_fp32_fma")
 
 _lib = None
 _lock = threading.Lock()
@@ -100,10 +101,14 @@ def load(path: str | None = None):
         lib.gemm_last_tc_pair.restype = i
         lib.gemm_force_split_tiles.argtypes = [i]
         lib.gemm_force_split_tiles.restype = i
+        lib.gemm_last_k_split.argtypes = []
+        lib.gemm_last_k_split.restype = i
         lib.gemm_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
         lib.gemm_set_wait_timeout_ns.restype = i
         lib.gemm_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
         lib.gemm_selftest_wait_timeout.restype = i
+        lib.gemm_probe_fp32_fma.argtypes = [i, i, vp, ctypes.POINTER(ctypes.c_double), vp]
+        lib.gemm_probe_fp32_fma.restype = i
         _lib = lib
         return lib
 
@@ -178,12 +183,26 @@ def force_split_tiles(enable: int):
     _check(load().gemm_force_split_tiles(enable))
 
 
+def last_k_split() -> int:
+    return load().gemm_last_k_split()
+
+
 def set_wait_timeout_ns(ns: int):
     _check(load().gemm_set_wait_timeout_ns(ns))
 
 
 def selftest_wait_timeout(ns: int, stream=0):
     _check(load().gemm_selftest_wait_timeout(ns, stream))
+
+
+def probe_fp32_fma(packed: bool, iters: int, sink_ptr: int, stream=0) -> float:
+    """Launch the FP32 FMA throughput probe; returns the launch's FLOPs."""
+    flops = ctypes.c_double(0.0)
+    rc = load().gemm_probe_fp32_fma(int(bool(packed)), int(iters), sink_ptr, ctypes.byref(flops),
+                                    stream)
+    if rc != 0:
+        raise GemmError(rc, "FMA probe launch failed")
+    return flops.value
 
 
 def _ld(t) -> int:

@@ -35,6 +35,7 @@ thread_local int t_last_bn = 0;
 thread_local int t_forced_pair = 0;
 thread_local int t_last_pair = 0;
 thread_local int t_split_tiles = 1;
+thread_local int t_last_k_split = 1;
 std::atomic<uint64_t> g_timeout_ns{1000000000ull};
 
 int fail(int code, const char* fmt, ...) {
@@ -171,6 +172,7 @@ int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int 
         bool swiglu = false, const void* B2 = nullptr) {
   t_msg[0] = '\0';
   t_last_path = GEMM_PATH_AUTO;
+  t_last_k_split = 1;
   if (M < 0 || N < 0 || K < 0) return fail(GEMM_ERR_INVALID_ARG, "negative size M=%d N=%d K=%d", M, N, K);
   if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
     return fail(GEMM_ERR_INVALID_ARG, "leading dimension too small (lda=%d ldb=%d ldc=%d, K=%d N=%d)",
@@ -283,7 +285,7 @@ int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int 
       if (swiglu && (rc = make_map(B2, N, K, (uint64_t)ldb * 2, 64, kSkBK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                                    CU_TENSOR_MAP_SWIZZLE_128B, &mB2)) != GEMM_OK)
         return rc;
-      err = launch_skinny(a, mA, mB, mB2, dev->num_sms, stream);
+      err = launch_skinny(a, mA, mB, mB2, dev->num_sms, stream, &t_last_k_split);
       break;
     default:
       return fail(GEMM_ERR_INVALID_ARG, "unknown path %d", path);
@@ -414,6 +416,8 @@ int gemm_force_split_tiles(int enable) {
   g3::t_split_tiles = enable;
   return GEMM_OK;
 }
+
+int gemm_last_k_split(void) { return g3::t_last_k_split; }
 
 int gemm_set_wait_timeout_ns(uint64_t timeout_ns) {
   g3::g_timeout_ns.store(timeout_ns == 0 ? 1000000000ull : timeout_ns);

@@ -12,8 +12,8 @@
 //     FMA pipe, not instruction issue, is the limit.
 // The K-slices stream through a 4-stage shared-memory ring filled by TMA
 // ("Kernel 性能从何而来", section "优化阶梯": TMA-backed loads are the first big
-// step), one producer warp issuing copies and eight compute warps consuming
-// them, handed over with mbarriers (same page, "通过重叠执行减少硬件空闲").
+// step); lane 0 of warp 0 issues the copies and the eight warps consume them,
+// handed over with mbarriers (same page, "通过重叠执行减少硬件空闲").
 //
 // Shared-memory bank conflicts ("CUDA 算子工程 ch.4 内存层级与代价表", sections
 // 4.3.1-4.3.4): the A tile is stored [m][k] (64 bytes per row) with the TMA
@@ -77,6 +77,9 @@ __device__ __forceinline__ float2 unpack2(uint64_t v) {
   return r;
 }
 
+// EPI: bias and/or activation present (the plain instance has no trace of
+// them, so the common case keeps the main loop's register allocation).
+template <bool EPI>
 __global__ void __launch_bounds__(THREADS, 2)
     sgemm_tma_kernel(const __grid_constant__ CUtensorMap mapA,
                      const __grid_constant__ CUtensorMap mapB, const SimtParams p) {
@@ -211,7 +214,6 @@ __global__ void __launch_bounds__(THREADS, 2)
     // ---------------------------------------------------------- epilogue
     float* C = static_cast<float*>(a.C);
     const bool beta_nz = a.beta != 0.f;
-    const bool epi = a.bias != nullptr || a.act != kActNone;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const long long m = (long long)m0 + wm * 64 + i * 8 + tm;
@@ -230,7 +232,7 @@ __global__ void __launch_bounds__(THREADS, 2)
             v[2] = fmaf(a.beta, c.z, v[2]);
             v[3] = fmaf(a.beta, c.w, v[3]);
           }
-          if (epi) {
+          if (EPI) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) v[j] = finish(a, v[j], n + j);
           }
@@ -241,7 +243,7 @@ __global__ void __launch_bounds__(THREADS, 2)
             if (n + j < a.N) {
               float r = v[j];
               if (beta_nz) r = fmaf(a.beta, cp[j], r);
-              cp[j] = finish(a, r, n + j);
+              cp[j] = EPI ? finish(a, r, n + j) : r;
             }
           }
         }
@@ -255,10 +257,13 @@ __global__ void __launch_bounds__(THREADS, 2)
 
 int launch_f32_simt(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
                     cudaStream_t s) {
-  static bool attr_done = false;  // idempotent; a race only repeats the call
+  static bool attr_done = false;  // idempotent; a race only repeats the calls
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(sgemm_tma_kernel,
+    cudaError_t e = cudaFuncSetAttribute(sgemm_tma_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(sgemm_tma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
@@ -269,7 +274,10 @@ int launch_f32_simt(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMa
   p.c_vec = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && (a.ldc % 4) == 0) ? 1 : 0;
   const long long tiles = (long long)p.tiles_m * p.tiles_n;
   if (tiles <= 0) return cudaSuccess;
-  sgemm_tma_kernel<<<(unsigned)tiles, THREADS, SMEM_BYTES, s>>>(*mapA, *mapB, p);
+  if (a.bias != nullptr || a.act != kActNone)
+    sgemm_tma_kernel<true><<<(unsigned)tiles, THREADS, SMEM_BYTES, s>>>(*mapA, *mapB, p);
+  else
+    sgemm_tma_kernel<false><<<(unsigned)tiles, THREADS, SMEM_BYTES, s>>>(*mapA, *mapB, p);
   return cudaGetLastError();
 }
 

@@ -394,7 +394,7 @@ int choose_split(int tiles_n, int k_tiles, int num_sms) {
 
 template <bool OUT_BF16, bool SW>
 int launch_impl(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
-                const CUtensorMap* mapB2, int num_sms, cudaStream_t s) {
+                const CUtensorMap* mapB2, int num_sms, cudaStream_t s, int* k_split) {
   constexpr int OUT_COLS = SW ? BN / 2 : BN;
   static int attr_done_mask = 0;
   int dev = 0;
@@ -412,6 +412,7 @@ int launch_impl(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* m
   if (tiles_n <= 0 || a.M <= 0) return cudaSuccess;
   if (tiles_n > 65535) return cudaErrorInvalidConfiguration;
   p.split = choose_split(tiles_n, p.k_tiles, num_sms);
+  *k_split = p.split;
   p.c_vec = 0;
 
   cudaLaunchConfig_t cfg = {};
@@ -437,13 +438,14 @@ int launch_impl(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* m
 }  // namespace
 
 int launch_skinny(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
-                  const CUtensorMap* mapB2, int num_sms, cudaStream_t s) {
+                  const CUtensorMap* mapB2, int num_sms, cudaStream_t s, int* k_split) {
+  *k_split = 1;
   if (a.swiglu) {
     if (a.out != Elem::BF16 || mapB2 == nullptr) return cudaErrorInvalidValue;
-    return launch_impl<true, true>(a, mapA, mapB, mapB2, num_sms, s);
+    return launch_impl<true, true>(a, mapA, mapB, mapB2, num_sms, s, k_split);
   }
-  if (a.out == Elem::BF16) return launch_impl<true, false>(a, mapA, mapB, nullptr, num_sms, s);
-  return launch_impl<false, false>(a, mapA, mapB, nullptr, num_sms, s);
+  if (a.out == Elem::BF16) return launch_impl<true, false>(a, mapA, mapB, nullptr, num_sms, s, k_split);
+  return launch_impl<false, false>(a, mapA, mapB, nullptr, num_sms, s, k_split);
 }
 
 }  // namespace g3

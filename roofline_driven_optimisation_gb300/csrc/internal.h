@@ -85,8 +85,9 @@ int launch_bf16_swiglu_pair(const GemmArgs& a, const CUtensorMap* mapA, const CU
 // Skinny (M <= 16) split-K kernel: TMA tiles of B (64 n x 64 k) and A
 // (64 k x 16 rows), 128-byte swizzle.  mapB2 (the up-projection) is used
 // when a.swiglu is set, and may be null otherwise.
+// *k_split receives the number of CTAs K was split over.
 int launch_skinny(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
-                  const CUtensorMap* mapB2, int num_sms, cudaStream_t s);
+                  const CUtensorMap* mapB2, int num_sms, cudaStream_t s, int* k_split);
 constexpr int kSkMaxM = 16, kSkBN = 128, kSkBK = 64;
 
 int launch_selftest_wait(int* status, uint64_t timeout_ns, cudaStream_t s);

@@ -2,6 +2,7 @@
 
     python -m roofline_driven_optimisation_gb300.run_case --case bf16_8192 --reps 3
     python -m roofline_driven_optimisation_gb300.run_case --case decode_m16_lm --out f32
+    python -m roofline_driven_optimisation_gb300.run_case --swiglu 16      (fused FFN gate/up)
 
 Prints the kernel family and the CUDA-event time of each call.  Workload
 names are those of ``roofline_driven_optimisation_gb300.inputs``.
@@ -23,15 +24,21 @@ def main():
     from roofline_driven_optimisation_gb300 import inputs
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("--case", required=True, choices=sorted(inputs.SPECS))
+    ap.add_argument("--case", choices=sorted(inputs.SPECS))
+    ap.add_argument("--swiglu", type=int, metavar="M",
+                    help="fused silu(X Wg) * (X Wu) with M rows and the LLaMA-7B gate/up shapes")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--out", default="auto", choices=["auto", "bf16", "f32"])
     ap.add_argument("--M", type=int)
     ap.add_argument("--N", type=int)
     ap.add_argument("--K", type=int)
     a = ap.parse_args()
+    if (a.case is None) == (a.swiglu is None):
+        ap.error("give exactly one of --case and --swiglu")
 
     g.load()
+    if a.swiglu is not None:
+        return run_swiglu(g, torch, inputs, a)
     c = inputs.make(a.case, M=a.M, N=a.N, K=a.K)
     sp = c.spec
     if sp.in_dtype == "f32":
@@ -49,6 +56,28 @@ def main():
         ms = e0.elapsed_time(e1)
         print(f"{a.case} M={sp.M} N={sp.N} K={sp.K} path={g.PATH_NAMES[g.last_path()]} "
               f"call {i}: {ms:.4f} ms, {2 * sp.M * sp.N * sp.K / ms / 1e9:.1f} TFLOP/s")
+    status, where = g.device_status()
+    if status != 0:
+        raise SystemExit(f"device status {status} at site {where}")
+
+
+def run_swiglu(g, torch, inputs, a):
+    kw = {k: v for k, v in (("N", a.N), ("K", a.K)) if v is not None}
+    c = inputs.make_swiglu(a.swiglu, **kw)
+    A, Bg, Bu = c.A.cuda(), c.Bgate.cuda(), c.Bup.cuda()
+    M, K = A.shape
+    N = Bg.shape[1]
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    for i in range(a.reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.swiglu(A, Bg, Bu, C)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        by = 2 * M * K + 4 * K * N + 2 * M * N
+        print(f"swiglu M={M} N={N} K={K} path={g.PATH_NAMES[g.last_path()]} call {i}: {ms:.4f} ms, "
+              f"{4 * M * N * K / ms / 1e9:.1f} TFLOP/s, {by / ms / 1e6:.1f} GB/s")
     status, where = g.device_status()
     if status != 0:
         raise SystemExit(f"device status {status} at site {where}")

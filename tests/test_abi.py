@@ -1,5 +1,6 @@
 """The C-ABI library builds, loads without a GPU, and exports every declared symbol."""
 import ctypes
+import glob
 import os
 import re
 import shutil
@@ -9,14 +10,17 @@ import pytest
 
 from conftest import ROOT
 
-HEADER = os.path.join(ROOT, "include", "gb300gemm.h")
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 
 def _declared_functions():
-    src = open(HEADER, encoding="utf-8").read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    names = re.findall(r"^\s*(?:const\s+)?\w[\w\s\*]*?\b(gemm_\w+)\s*\(", src, flags=re.M)
-    return sorted(set(names))
+    names = set()
+    for h in HEADERS:
+        src = open(h, encoding="utf-8").read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names |= set(re.findall(r"^\s*(?:const\s+)?\w[\w\s\*]*?\b(gemm_\w+)\s*\(", src,
+                                flags=re.M))
+    return sorted(names)
 
 
 @pytest.fixture(scope="module")
@@ -30,7 +34,7 @@ def lib_path():
 def test_header_declares_the_abi():
     names = _declared_functions()
     for want in ("gemm_f32", "gemm_bf16", "gemm_bf16_f32out", "gemm_get_last_error",
-                 "gemm_device_status"):
+                 "gemm_device_status", "gemm_bf16_swiglu", "gemm_probe_fp32_fma"):
         assert want in names
 
 
@@ -56,7 +60,8 @@ def test_header_is_valid_c(tmp_path):
     if shutil.which("gcc") is None:
         pytest.skip("gcc unavailable")
     src = tmp_path / "use.c"
-    src.write_text('#include "gb300gemm.h"\nint main(void){ return gemm_get_last_error() == 0; }\n')
+    src.write_text('#include "gb300gemm.h"\n#include "gb300gemm_probe.h"\n'
+                   'int main(void){ return gemm_get_last_error() == 0; }\n')
     r = subprocess.run(["gcc", "-std=c99", "-Wall", "-fsyntax-only",
                         "-I", os.path.join(ROOT, "include"), "-I", "/usr/local/cuda/include", str(src)],
                        capture_output=True, text=True)

@@ -62,11 +62,26 @@ def _check(c, **kw):
     return err, ran
 
 
+def _expected_split(N, K):
+    """K split of the decode kernel: the largest power of two <= 8 that keeps
+    the grid (64-column tiles x split) within two CTAs per SM, and no more
+    than the K stages of 64."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tiles_n, k_tiles = -(-N // 64), -(-K // 64)
+    s = 1
+    while s * 2 <= 8 and tiles_n * s * 2 <= 2 * sms:
+        s *= 2
+    while s > 1 and s > k_tiles:
+        s //= 2
+    return s
+
+
 # LLaMA-7B FFN gate/up (K = 4096, N = 11008) at the decode batch sizes
 @pytest.mark.parametrize("M", [1, 4, 16])
 def test_decode_llama_gate_up(cuda_lib, M):
     _, ran = _check(inputs.make_swiglu(M))
     assert ran == g.PATH_SKINNY
+    assert g.last_k_split() == _expected_split(11008, 4096)
 
 
 # tiles of 64 output columns: N = 4096 gives a K split of 4, N = 200 a ragged
@@ -75,6 +90,7 @@ def test_decode_llama_gate_up(cuda_lib, M):
 def test_decode_splits_and_tails(cuda_lib, M, N, K):
     _, ran = _check(inputs.make_swiglu(M, N, K, seed=M + N))
     assert ran == g.PATH_SKINNY
+    assert g.last_k_split() == _expected_split(N, K)
 
 
 @pytest.mark.parametrize("M,N,K", [(300, 520, 256), (17, 128, 64), (256, 11008, 64),
