@@ -10,10 +10,12 @@
 //     section 10.6 is the 4 x 4 version of the same idea), accumulated with
 //     the packed fma.rn.f32x2 (two IEEE fp32 FMAs per instruction), so the
 //     FMA pipe, not instruction issue, is the limit.
-// The K-slices stream through a 4-stage shared-memory ring filled by TMA
+// The K-slices stream through a 5-stage shared-memory ring filled by TMA
 // ("Kernel 性能从何而来", section "优化阶梯": TMA-backed loads are the first big
-// step); lane 0 of warp 0 issues the copies and the eight warps consume them,
-// handed over with mbarriers (same page, "通过重叠执行减少硬件空闲").
+// step).  A slot is handed to the eight warps by an mbarrier that the copy
+// completes, and handed back by a counter: the last warp to finish with a
+// slot issues its refill, so no warp ever waits for the others to release
+// one (same page, "通过重叠执行减少硬件空闲": keep every unit busy).
 //
 // Shared-memory bank conflicts ("CUDA 算子工程 ch.4 内存层级与代价表", sections
 // 4.3.1-4.3.4): the A tile is stored [m][k] (64 bytes per row) with the TMA
@@ -33,13 +35,14 @@ namespace g3 {
 namespace {
 
 constexpr int BM = kSimtBM, BN = kSimtBN, BK = kSimtBK;
-constexpr int STAGES = 4;
+constexpr int STAGES = 5;
 constexpr int A_STAGE_BYTES = BM * BK * 4;  // 8 KB
 constexpr int B_STAGE_BYTES = BK * BN * 4;  // 8 KB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int COMPUTE_WARPS = 8;
 constexpr int THREADS = COMPUTE_WARPS * 32;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+static_assert(STAGES * 8 + 16 + 2 * STAGES * 4 <= 256, "barrier area");
 
 struct SimtParams {
   GemmArgs a;
@@ -88,9 +91,11 @@ __global__ void __launch_bounds__(THREADS, 2)
   uint8_t* base_ptr = smem_raw + (base - smem_u32(smem_raw));
   const uint32_t bar_base = base + STAGES * STAGE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + STAGES * STAGE_BYTES);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + STAGES);
+  // per slot: warps done with it this round, and copies issued into it so far
+  uint32_t* done_cnt = reinterpret_cast<uint32_t*>(bars + STAGES) + 4;
+  uint32_t* issue_cnt = done_cnt + STAGES;
   auto full_bar = [&](int s) { return bar_base + 8u * s; };
-  auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
   auto a_tile = [&](int s) { return base + s * STAGE_BYTES; };
   auto b_tile = [&](int s) { return base + s * STAGE_BYTES + A_STAGE_BYTES; };
 
@@ -113,21 +118,18 @@ __global__ void __launch_bounds__(THREADS, 2)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), COMPUTE_WARPS);
+      done_cnt[s] = 0;
+      issue_cnt[s] = 0;
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
 
-  // Lane 0 of warp 0 also issues the TMA copies: the first STAGES K-slices up
-  // front, then each slot again as soon as all eight warps have released it.
-  // (A dedicated producer warp would put five warps on one scheduler at two
-  // CTAs per SM and cap registers at 96.)
+  // Thread 0 issues the first STAGES K-slices; every later copy is issued by
+  // the last warp to release its slot.  (A dedicated producer warp would put
+  // five warps on one scheduler at two CTAs per SM and cap registers at 96.)
   const bool producer = threadIdx.x == 0;
-  // slot s has a copy in flight when bit s of `issued` is set; its phase
-  // parity is bit s of `issued_par`
-  uint32_t issued = 0, issued_par = 0;
   if (producer) {
     tma_prefetch_desc(&mapA);
     tma_prefetch_desc(&mapB);
@@ -135,7 +137,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       mbar_arrive_expect_tx(full_bar(kt), STAGE_BYTES);
       tma_load_2d(a_tile(kt), &mapA, full_bar(kt), kt * BK, m0);
       tma_load_2d(b_tile(kt), &mapB, full_bar(kt), n0, kt * BK);
-      issued |= 1u << kt;
+      issue_cnt[kt] = 1;
     }
   }
 
@@ -163,7 +165,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
     const uint32_t at = a_tile(s) + a_row_off;
     const uint32_t bt = b_tile(s) + b_col_off;
-#pragma unroll 4
+#pragma unroll
     for (int kp = 0; kp < BK / 2; ++kp) {
       // rows i*8+tm, k = 2kp, 2kp+1: one 8-byte load per row inside the
       // swizzled 16-byte chunk that holds k = 4*(kp/2) .. 4*(kp/2)+3
@@ -185,28 +187,31 @@ __global__ void __launch_bounds__(THREADS, 2)
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty_bar(s));
-    if (producer && kt + STAGES < k_tiles) {
-      // refill slot s with K-slice kt+STAGES once every warp has released it
-      if (!mbar_wait(empty_bar(s), parity, a.timeout_ns, abort_flag)) {
-        if (!*abort_flag) report_status(a.status, 5, kSiteSimtProducer);
-        *abort_flag = 1;
-        ok = false;
-        break;
+    __syncwarp();  // every lane of this warp is done reading slot s
+    if (lane == 0) {
+      // the last of the eight warps to release slot s refills it with K-slice
+      // kt+STAGES; the slot's next round cannot start before that copy lands
+      __threadfence_block();
+      if (atomicAdd(&done_cnt[s], 1u) == COMPUTE_WARPS - 1) {
+        done_cnt[s] = 0;
+        __threadfence_block();
+        if (kt + STAGES < k_tiles && !*abort_flag) {
+          const int kn = kt + STAGES;
+          mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
+          tma_load_2d(a_tile(s), &mapA, full_bar(s), kn * BK, m0);
+          tma_load_2d(b_tile(s), &mapB, full_bar(s), n0, kn * BK);
+          atomicAdd(&issue_cnt[s], 1u);
+        }
       }
-      const int kn = kt + STAGES;
-      mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
-      tma_load_2d(a_tile(s), &mapA, full_bar(s), kn * BK, m0);
-      tma_load_2d(b_tile(s), &mapB, full_bar(s), n0, kn * BK);
-      issued_par = (issued_par & ~(1u << s)) | ((uint32_t)((kn / STAGES) & 1) << s);
     }
   }
+  __syncthreads();  // every warp has left the main loop
   if (producer && *abort_flag) {
-    // every copy already issued must land before shared memory is released
+    // every copy already issued must land before shared memory is released:
+    // the latest copy into slot s completes its phase issue_cnt[s] - 1
     for (int s = 0; s < STAGES; ++s)
-      if (((issued >> s) & 1u) &&
-          !mbar_wait(full_bar(s), (issued_par >> s) & 1u, a.timeout_ns, nullptr))
+      if (issue_cnt[s] > 0 &&
+          !mbar_wait(full_bar(s), (issue_cnt[s] - 1u) & 1u, a.timeout_ns, nullptr))
         report_status(a.status, 5, kSiteSimtDrain);
   }
 

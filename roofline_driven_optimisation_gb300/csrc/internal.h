@@ -42,7 +42,6 @@ enum WaitSite : int {
   kSiteTc2Mma = 15,
   kSiteTc2Epilogue = 16,
   kSiteTc2Drain = 17,
-  kSiteSimtProducer = 20,
   kSiteSimtConsumer = 21,
   kSiteSimtDrain = 22,
   kSiteSkinnyProducer = 30,
