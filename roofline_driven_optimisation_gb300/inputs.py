@@ -165,3 +165,37 @@ def make_swiglu(M: int, N: int = LLAMA7B_WEIGHTS["gate"][1], K: int = LLAMA7B_WE
     Bg = round_to(torch.randn((K, N), generator=gen, dtype=torch.float32) * 0.02, "bf16")
     Bu = round_to(torch.randn((K, N), generator=gen, dtype=torch.float32) * 0.02, "bf16")
     return SwigluCase(A, Bg, Bu)
+
+
+FP8_E4M3, FP8_E5M2 = 0, 1
+_FP8_DTYPES = {FP8_E4M3: "float8_e4m3fn", FP8_E5M2: "float8_e5m2"}
+
+
+@dataclasses.dataclass
+class Fp8Case:
+    A: torch.Tensor                # M x K FP8 codes (uint8), CPU
+    B: torch.Tensor                # K x N FP8 codes (uint8)
+    fmt_a: int
+    fmt_b: int
+    alpha: float                   # stands in for the product of per-tensor scales
+    beta: float
+    C0: Optional[torch.Tensor]     # M x N fp32 values, or None
+
+
+def fp8_codes(x: torch.Tensor, fmt: int) -> torch.Tensor:
+    """Round fp32 values to the nearest FP8 value of `fmt` (RNE) and return
+    the codes as uint8."""
+    return x.to(getattr(torch, _FP8_DTYPES[fmt])).view(torch.uint8).contiguous()
+
+
+def make_fp8(M: int, N: int, K: int, fmt_a: int = FP8_E4M3, fmt_b: int = FP8_E4M3,
+             seed: int = 6, beta: float = 0.0) -> Fp8Case:
+    """FP8 GEMM operands: A and B ~ N(0, 1) rounded to FP8, alpha = 1/sqrt(K)
+    (the per-tensor scales of a quantised layer fold into alpha, and this one
+    keeps C near N(0, 1)); C0 ~ N(0, 1) when beta != 0."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    A = fp8_codes(torch.randn((M, K), generator=gen, dtype=torch.float32), fmt_a)
+    B = fp8_codes(torch.randn((K, N), generator=gen, dtype=torch.float32), fmt_b)
+    C0 = torch.randn((M, N), generator=gen, dtype=torch.float32) if beta != 0.0 else None
+    return Fp8Case(A, B, fmt_a, fmt_b, 1.0 / math.sqrt(max(K, 1)), beta, C0)

@@ -1,6 +1,8 @@
 """The seeded input generators: determinism, shapes, and bf16 rounding."""
 import math
 
+import numpy as np
+
 import torch
 
 from roofline_driven_optimisation_gb300 import inputs
@@ -51,3 +53,16 @@ def test_workload_table():
     assert inputs.spec("prefill_lm").N == 32000
     assert inputs.spec("decode_m16_down").K == 11008
     assert {inputs.spec(f"decode_m{m}_qkv").M for m in (1, 4, 16)} == {1, 4, 16}
+
+
+def test_fp8_operands_are_seeded_codes():
+    from oracle import fp8
+    c1 = inputs.make_fp8(33, 40, 64, inputs.FP8_E4M3, inputs.FP8_E5M2, seed=3, beta=0.5)
+    c2 = inputs.make_fp8(33, 40, 64, inputs.FP8_E4M3, inputs.FP8_E5M2, seed=3, beta=0.5)
+    assert c1.A.dtype == torch.uint8 and c1.B.dtype == torch.uint8
+    assert torch.equal(c1.A, c2.A) and torch.equal(c1.B, c2.B) and torch.equal(c1.C0, c2.C0)
+    a = fp8.decode(c1.A, fp8.E4M3)
+    b = fp8.decode(c1.B, fp8.E5M2)
+    assert np.all(np.isfinite(a)) and np.all(np.isfinite(b))
+    assert 0.5 < a.std() < 1.5 and 0.5 < b.std() < 1.5
+    assert c1.alpha == 1 / 8
