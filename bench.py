@@ -47,12 +47,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per launch measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum)
 # for each kernel source file, valid only while the file hashes to `sha256`.
 NCU_TRAFFIC = {
-    # profiles/sgemm_tma_kernel_fp32_4096.md: 414.2 MB read + 54.4 MB written
-    "gemm_f32_simt.cu": {"sha256": "0a11a053a88d77a0ccd9e81e5ccefb4122b4a71dadf7f74a22dc2ce80a278101",
-                         "bytes_per_launch": 468608000},
-    # profiles/gemm_bf16_tc2_kernel_bf16_8192.md, 4096^3 capture: 78.4 MB + 10.8 MB
-    "gemm_bf16_tc2.cu": {"sha256": "2b6a643cd4f8f8fb6f7abbdb20386e620f2d6405ed50541da379fcfbba57c7c7",
-                         "bytes_per_launch": 89199104},
+    # profiles/sgemm_tma_kernel_fp32_4096.md: 406.1 MB read + 54.1 MB written
+    "gemm_f32_simt.cu": {"sha256": "a7d40a130b67d1ccc432d34a59d5b8e8f0bac0cc2ed7cdb9302bc58ff97a89d1",
+                         "bytes_per_launch": 460192768},
 }
 
 
@@ -327,6 +324,7 @@ def run_ours(args):
     e2e = run_e2e(args, g, torch, dev, parts, s, world)
     fused_ffn = measure_fused_ffn(g, torch, dev, s, hbm, bf16_peak) if rank == 0 else None
     fma_probe = measure_fp32_fma(g, torch, dev, fp32_peak / 1e12) if rank == 0 else None
+    fp8 = measure_fp8(g, torch, dev, pk["bf16_tflops"]) if rank == 0 else None
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -342,6 +340,7 @@ def run_ours(args):
         "parts": part_out,
         "fused_ffn_swiglu": fused_ffn,
         "fp32_fma_probe": fma_probe,
+        "fp8_gemm": fp8,
         "e2e": e2e,
         "gpu_launches": len(parts) * args.steps,
         "clocks": clocks.summary(),
@@ -415,6 +414,41 @@ def measure_fp32_fma(g, torch, dev, formula_tflops, iters=16000, reps=3):
             best = max(best, flops / (e0.elapsed_time(e1) * 1e-3) / 1e12)
         out[f"{name}_tflops"] = round(best, 2)
         out[f"{name}_frac_of_formula"] = round(best / formula_tflops, 4)
+    return out
+
+
+def measure_fp8(g, torch, dev, bf16_peak_tflops, reps=7):
+    """FP8 (E4M3) GEMM, bf16 C, at 4096^3 and 8192^3 against the FP8 dense
+    peak taken as the measured bf16 peak x 2 (the nominal FP8 : bf16 ratio,
+    4.5 : 2.25 PFLOP/s).  Events around each call, L2 flushed by a read pass
+    before every call, median of `reps`.  Not part of the step."""
+    from roofline_driven_optimisation_gb300 import inputs
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+    peak = 2.0 * bf16_peak_tflops
+    out = {"peak_tflops": round(peak, 1), "peak_source": "measured bf16 x 2 (nominal ratio)"}
+    for n in (4096, 8192):
+        c = inputs.make_fp8(n, n, n, inputs.FP8_E4M3, inputs.FP8_E4M3, seed=7)
+        A, B = c.A.to(dev), c.B.to(dev)
+        C = torch.empty((n, n), dtype=torch.bfloat16, device=dev)
+        g.gemm_fp8_tensors(A, 0, B, 0, C, c.alpha)
+        evs = []
+        for _ in range(reps):
+            flush.sum()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.gemm_fp8_tensors(A, 0, B, 0, C, c.alpha)
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+        tf = 2 * n ** 3 / (ms * 1e-3) / 1e12
+        out[f"e4m3_{n}"] = {"ms": round(ms, 5), "tflops": round(tf, 1), "frac": round(tf / peak, 4),
+                            "frac_nominal_4500": round(tf / 4500.0, 4)}
+        del A, B, C
+    status, where = g.device_status(stream.cuda_stream)
+    if status != 0:
+        raise RuntimeError(f"device status {status} at {where} in the FP8 measurement")
     return out
 
 

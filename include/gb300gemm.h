@@ -137,6 +137,35 @@ int gemm_bf16_f32out_ex(int M, int N, int K, float alpha, const gemm_bf16_t* A, 
 int gemm_bf16_swiglu(int M, int N, int K, const gemm_bf16_t* A, int lda, const gemm_bf16_t* Bgate,
                      const gemm_bf16_t* Bup, int ldb, gemm_bf16_t* C, int ldc, cudaStream_t stream);
 
+/* 8-bit floating-point formats of the FP8 entry points (the OCP FP8 formats). */
+typedef enum {
+  GEMM_FP8_E4M3 = 0, /* 4 exponent bits (bias 7), 3 mantissa bits, no inf, max 448 */
+  GEMM_FP8_E5M2 = 1  /* 5 exponent bits (bias 15), 2 mantissa bits, IEEE-like, max 57344 */
+} gemm_fp8_format;
+
+/*
+ * FP8 GEMM ("Kernel 性能从何而来", section "优化 Memory-Bound Kernel": fp8
+ * inputs move fewer bytes per FLOP than fp16 or fp32):
+ *
+ *     C = alpha * A * B + beta * C
+ *
+ * A is M x K and B is K x N, one byte per element, each in its own format
+ * (fmt_a, fmt_b: gemm_fp8_format), row-major with leading dimensions lda >= K
+ * and ldb >= N in elements (= bytes).  Per-tensor scale factors of a
+ * quantised layer fold into alpha.  The products are exact and accumulated
+ * in fp32, and the epilogue is that of gemm_bf16: bf16 C (gemm_fp8) or fp32 C
+ * (gemm_fp8_f32out).  The fast path runs on CTA pairs with 256 x 256 C tiles
+ * (tcgen05 kind::f8f6f4).  It needs 16-byte-aligned A and B, and lda and ldb
+ * multiples of 16.  Anything else runs on the generic kernel.  Conventions,
+ * errors and asynchrony are those of gemm_bf16.  An unknown format returns
+ * GEMM_ERR_INVALID_ARG.
+ */
+int gemm_fp8(int M, int N, int K, float alpha, const uint8_t* A, int fmt_a, int lda, const uint8_t* B,
+             int fmt_b, int ldb, float beta, gemm_bf16_t* C, int ldc, cudaStream_t stream);
+int gemm_fp8_f32out(int M, int N, int K, float alpha, const uint8_t* A, int fmt_a, int lda,
+                    const uint8_t* B, int fmt_b, int ldb, float beta, float* C, int ldc,
+                    cudaStream_t stream);
+
 /*
  * Message for the last non-OK return on the calling host thread ("" if none).
  * The string is owned by the library and valid until the next call on this
@@ -158,7 +187,7 @@ typedef enum {
   GEMM_PATH_AUTO = 0,     /* shape dispatcher (default) */
   GEMM_PATH_GENERIC = 1,  /* correctness-first tiled kernel, any alignment */
   GEMM_PATH_F32_SIMT = 2, /* register-tiled FP32 kernel */
-  GEMM_PATH_BF16_TC = 3,  /* tcgen05/TMEM/TMA warp-specialised kernel */
+  GEMM_PATH_BF16_TC = 3,  /* tcgen05/TMEM/TMA warp-specialised kernel (bf16 or FP8 inputs) */
   GEMM_PATH_SKINNY = 4    /* decode-shaped split-K kernel (bf16, M <= 16) */
 } gemm_path;
 

@@ -33,12 +33,14 @@ GEMM_ERR_DEVICE_TIMEOUT = 5
 
 PATH_AUTO, PATH_GENERIC, PATH_F32_SIMT, PATH_BF16_TC, PATH_SKINNY = range(5)
 ACT_NONE, ACT_RELU, ACT_SILU, ACT_GELU = range(4)
+FP8_E4M3, FP8_E5M2 = 0, 1
 PATH_NAMES = {PATH_AUTO: "none", PATH_GENERIC: "generic", PATH_F32_SIMT: "f32_simt",
               PATH_BF16_TC: "bf16_tc", PATH_SKINNY: "skinny"}
 
 # every symbol the public header declares
 EXPORTS = ("gemm_f32", "gemm_bf16", "gemm_bf16_f32out", "gemm_f32_ex", "gemm_bf16_ex",
-           "gemm_bf16_f32out_ex", "gemm_bf16_swiglu", "gemm_get_last_error",
+           "gemm_bf16_f32out_ex", "gemm_bf16_swiglu", "gemm_fp8", "gemm_fp8_f32out",
+           "gemm_get_last_error",
            "gemm_device_status", "gemm_force_path", "gemm_last_path", "gemm_force_tile_n",
            "gemm_last_tile_n", "gemm_force_tc_pair", "gemm_last_tc_pair", "gemm_force_split_tiles",
            "gemm_last_k_split", "gemm_set_wait_timeout_ns", "gemm_selftest_wait_timeout",
@@ -83,6 +85,10 @@ def load(path: str | None = None):
             fn.restype = i
         lib.gemm_bf16_swiglu.argtypes = [i, i, i, vp, i, vp, vp, i, vp, i, vp]
         lib.gemm_bf16_swiglu.restype = i
+        for name in ("gemm_fp8", "gemm_fp8_f32out"):
+            fn = getattr(lib, name)
+            fn.argtypes = [i, i, i, f, vp, i, i, vp, i, i, f, vp, i, vp]
+            fn.restype = i
         lib.gemm_get_last_error.argtypes = []
         lib.gemm_get_last_error.restype = ctypes.c_char_p
         lib.gemm_device_status.argtypes = [vp, ctypes.POINTER(i)]
@@ -146,6 +152,15 @@ def gemm_bf16_f32out_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias, act,
 
 def gemm_bf16_swiglu(M, N, K, A, lda, Bgate, Bup, ldb, C, ldc, stream=0):
     _check(load().gemm_bf16_swiglu(M, N, K, A, lda, Bgate, Bup, ldb, C, ldc, stream))
+
+
+def gemm_fp8(M, N, K, alpha, A, fmt_a, lda, B, fmt_b, ldb, beta, C, ldc, stream=0):
+    _check(load().gemm_fp8(M, N, K, alpha, A, fmt_a, lda, B, fmt_b, ldb, beta, C, ldc, stream))
+
+
+def gemm_fp8_f32out(M, N, K, alpha, A, fmt_a, lda, B, fmt_b, ldb, beta, C, ldc, stream=0):
+    _check(load().gemm_fp8_f32out(M, N, K, alpha, A, fmt_a, lda, B, fmt_b, ldb, beta, C, ldc,
+                                  stream))
 
 
 def device_status(stream=0) -> tuple[int, int]:
@@ -260,4 +275,27 @@ def swiglu(A, Bgate, Bup, C, stream=None):
     s = stream if stream is not None else torch.cuda.current_stream(A.device).cuda_stream
     gemm_bf16_swiglu(M, N, K, A.data_ptr(), _ld(A), Bgate.data_ptr(), Bup.data_ptr(), _ld(Bgate),
                      C.data_ptr(), _ld(C), s)
+    return C
+
+
+def gemm_fp8_tensors(A, fmt_a: int, B, fmt_b: int, C, alpha: float = 1.0, beta: float = 0.0,
+                     stream=None):
+    """C = alpha*dec(A)@dec(B) + beta*C for CUDA tensors of FP8 codes (uint8)
+    and a bf16 or fp32 C.  Argument marshalling only."""
+    import torch
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K or tuple(C.shape) != (M, N):
+        raise ValueError(f"shape mismatch {tuple(A.shape)} @ {tuple(B.shape)} -> {tuple(C.shape)}")
+    if A.dtype != torch.uint8 or B.dtype != torch.uint8 or not (A.is_cuda and B.is_cuda and C.is_cuda):
+        raise TypeError("gemm_fp8_tensors() takes uint8 FP8 codes on the GPU")
+    s = stream if stream is not None else torch.cuda.current_stream(A.device).cuda_stream
+    args = (M, N, K, float(alpha), A.data_ptr(), int(fmt_a), _ld(A), B.data_ptr(), int(fmt_b), _ld(B),
+            float(beta), C.data_ptr(), _ld(C), s)
+    if C.dtype == torch.bfloat16:
+        gemm_fp8(*args)
+    elif C.dtype == torch.float32:
+        gemm_fp8_f32out(*args)
+    else:
+        raise TypeError(f"unsupported output dtype {C.dtype}")
     return C

@@ -167,9 +167,10 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // swiglu: C = silu(A*B) * (A*B2), B2 with B's shape and leading dimension
 // (alpha 1, beta 0, no bias or activation).
+// in == FP8: fmt_a, fmt_b give the 8-bit formats of A and B.
 int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int lda, const void* B,
         int ldb, float beta, void* C, int ldc, const float* bias, int act, cudaStream_t stream,
-        bool swiglu = false, const void* B2 = nullptr) {
+        bool swiglu = false, const void* B2 = nullptr, int fmt_a = kE4M3, int fmt_b = kE4M3) {
   t_msg[0] = '\0';
   t_last_path = GEMM_PATH_AUTO;
   t_last_k_split = 1;
@@ -181,7 +182,10 @@ int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int 
   if (C == nullptr) return fail(GEMM_ERR_INVALID_ARG, "C is NULL");
   if (K > 0 && (A == nullptr || B == nullptr || (swiglu && B2 == nullptr)))
     return fail(GEMM_ERR_INVALID_ARG, "A or B is NULL");
-  const size_t in_sz = in == Elem::F32 ? 4 : 2, out_sz = out == Elem::F32 ? 4 : 2;
+  const size_t in_sz = in == Elem::F32 ? 4 : in == Elem::BF16 ? 2 : 1;
+  const size_t out_sz = out == Elem::F32 ? 4 : 2;
+  if (in == Elem::FP8 && (fmt_a < kE4M3 || fmt_a > kE5M2 || fmt_b < kE4M3 || fmt_b > kE5M2))
+    return fail(GEMM_ERR_INVALID_ARG, "unknown FP8 format (A %d, B %d)", fmt_a, fmt_b);
   if ((reinterpret_cast<uintptr_t>(A) % in_sz) || (reinterpret_cast<uintptr_t>(B) % in_sz) ||
       (reinterpret_cast<uintptr_t>(B2) % in_sz) || (reinterpret_cast<uintptr_t>(C) % out_sz))
     return fail(GEMM_ERR_MISALIGNED, "a matrix pointer is not aligned to its element size");
@@ -203,6 +207,8 @@ int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int 
   a.act = act;
   a.B2 = B2;
   a.swiglu = swiglu ? 1 : 0;
+  a.fmt_a = fmt_a;
+  a.fmt_b = fmt_b;
 
   const bool tma_ok = K > 0 && aligned16(A) && aligned16(B) && (!swiglu || aligned16(B2)) &&
                       ((size_t)lda * in_sz) % 16 == 0 && ((size_t)ldb * in_sz) % 16 == 0;
@@ -211,13 +217,14 @@ int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int 
   if (forced == GEMM_PATH_AUTO) {
     if (!tma_ok) path = GEMM_PATH_GENERIC;
     else if (in == Elem::F32) path = GEMM_PATH_F32_SIMT;
+    else if (in == Elem::FP8) path = GEMM_PATH_BF16_TC;
     else if (M <= kSkMaxM) path = GEMM_PATH_SKINNY;
     else path = GEMM_PATH_BF16_TC;
   } else {
     path = forced;
     const bool fits = forced == GEMM_PATH_GENERIC ||
                       (tma_ok && ((forced == GEMM_PATH_F32_SIMT && in == Elem::F32 && !swiglu) ||
-                                  (forced == GEMM_PATH_BF16_TC && in == Elem::BF16) ||
+                                  (forced == GEMM_PATH_BF16_TC && in != Elem::F32) ||
                                   (forced == GEMM_PATH_SKINNY && in == Elem::BF16 && M <= kSkMaxM)));
     if (!fits) return fail(GEMM_ERR_UNSUPPORTED, "forced path %d cannot run this call", forced);
   }
@@ -238,6 +245,20 @@ int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int 
       err = launch_f32_simt(a, mA, mB, stream);
       break;
     case GEMM_PATH_BF16_TC:
+      if (in == Elem::FP8) {
+        if ((rc = make_map(A, K, M, (uint64_t)lda, kF8BK, kTcBM, CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                           CU_TENSOR_MAP_SWIZZLE_128B, &mA)) != GEMM_OK)
+          return rc;
+        if ((rc = make_map(B, N, K, (uint64_t)ldb, 128, kF8BK, CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                           CU_TENSOR_MAP_SWIZZLE_128B, &mB)) != GEMM_OK)
+          return rc;
+        err = launch_fp8_tc_pair(a, mA, mB, dev->num_sms, stream);
+        if (err == cudaSuccess) {
+          t_last_bn = 256;
+          t_last_pair = 2;
+        }
+        break;
+      }
       if ((rc = make_map(A, K, M, (uint64_t)lda * 2, kTcBK, kTcBM, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                          CU_TENSOR_MAP_SWIZZLE_128B, &mA)) != GEMM_OK)
         return rc;
@@ -341,6 +362,19 @@ int gemm_bf16_swiglu(int M, int N, int K, const gemm_bf16_t* A, int lda, const g
                      const gemm_bf16_t* Bup, int ldb, gemm_bf16_t* C, int ldc, cudaStream_t stream) {
   return g3::run(Elem::BF16, Elem::BF16, M, N, K, 1.f, A, lda, Bgate, ldb, 0.f, C, ldc, nullptr,
                  g3::kActNone, stream, /*swiglu=*/true, Bup);
+}
+
+int gemm_fp8(int M, int N, int K, float alpha, const uint8_t* A, int fmt_a, int lda, const uint8_t* B,
+             int fmt_b, int ldb, float beta, gemm_bf16_t* C, int ldc, cudaStream_t stream) {
+  return g3::run(Elem::FP8, Elem::BF16, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, nullptr,
+                 g3::kActNone, stream, false, nullptr, fmt_a, fmt_b);
+}
+
+int gemm_fp8_f32out(int M, int N, int K, float alpha, const uint8_t* A, int fmt_a, int lda,
+                    const uint8_t* B, int fmt_b, int ldb, float beta, float* C, int ldc,
+                    cudaStream_t stream) {
+  return g3::run(Elem::FP8, Elem::F32, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, nullptr,
+                 g3::kActNone, stream, false, nullptr, fmt_a, fmt_b);
 }
 
 int gemm_f32_ex(int M, int N, int K, float alpha, const float* A, int lda, const float* B, int ldb,

@@ -33,6 +33,14 @@
 // n0 + 64*(x / 128) + x % 64 of the gate (x % 128 < 64) or of the up
 // projection; the epilogue pairs them and applies silu(g) * u.  The
 // intermediate products never leave the chip and A is read once for both.
+//
+// FP8 variant (F8, BN = 256): A and B hold 8-bit floats (E4M3 or E5M2 each,
+// "Kernel 性能从何而来", section "优化 Memory-Bound Kernel": a narrower type
+// moves fewer bytes per FLOP).  A K-stage is still one 128-byte swizzle row
+// per operand row, now 128 elements deep, so stage sizes, the pipeline and
+// the epilogue are the bf16 ones; each CTA loads one 128-column box of B, the
+// MMA is kind::f8f6f4 with K = 32 per instruction, and there is no
+// half-width tail (a half tile would need 64-column boxes).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -48,10 +56,6 @@ namespace {
 
 constexpr int BM_CTA = kTcBM;    // rows per CTA
 constexpr int BM = 2 * BM_CTA;   // rows per pair tile
-constexpr int BK = kTcBK;
-constexpr int UMMA_K = 16;
-constexpr int A_STAGE_BYTES = BM_CTA * BK * 2;   // 16 KB
-constexpr int B_BOX_BYTES = 64 * BK * 2;         // 8 KB (64 n x 64 k)
 constexpr int TMEM_COLS = 512;
 constexpr int NUM_EPI_WARPS = 4;
 constexpr int THREADS = 64 + NUM_EPI_WARPS * 32;
@@ -61,11 +65,28 @@ constexpr int RASTER_GROUP = 8;
 constexpr uint64_t kDrainGraceNs = 50000;        // after an abort, time for the peer's copies to land
 constexpr uint16_t kBothCtas = 0x3;
 
-template <int BN>
+// Stage geometry: every operand row of a K-stage is one 128-byte swizzle row
+// (64 bf16 or 128 FP8 elements of K); B boxes are 128 bytes wide in n.
+template <bool F8>
+struct Geom {
+  static constexpr int ESIZE = F8 ? 1 : 2;
+  static constexpr int BK = 128 / ESIZE;                 // K elements per stage
+  static constexpr int UMMA_K = F8 ? 32 : 16;           // K per MMA instruction
+  static constexpr int BOX_N = 128 / ESIZE;             // columns per B box
+  static constexpr int A_STAGE_BYTES = BM_CTA * 128;    // 16 KB
+  static constexpr int B_BOX_BYTES = BOX_N * BK * ESIZE;  // 8 KB bf16, 16 KB FP8
+  static constexpr int A_KSTEP = UMMA_K * ESIZE;        // bytes per MMA along a K-major row
+  static constexpr int B_KSTEP = UMMA_K * 128;          // bytes per MMA down N-major rows
+};
+static_assert(Geom<false>::BK == kTcBK && Geom<true>::BK == kF8BK, "K per stage");
+
+template <int BN, bool F8 = false>
 struct PairCfg {
-  static_assert(BN == 128 || BN == 256, "each CTA loads whole 64-column boxes of B");
-  static constexpr int B_BOXES = BN / 2 / 64;
-  static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_BOXES * B_BOX_BYTES;  // per CTA
+  using G = Geom<F8>;
+  static_assert(BN == 128 || BN == 256, "pair tiles are 128 or 256 wide");
+  static_assert(!F8 || BN == 256, "FP8 tiles load one whole 128-column box per CTA");
+  static constexpr int B_BOXES = BN / 2 / G::BOX_N;
+  static constexpr int STAGE_BYTES = G::A_STAGE_BYTES + B_BOXES * G::B_BOX_BYTES;  // per CTA
   static constexpr int STAGES_FIT = (SMEM_LIMIT - BAR_BYTES - 1024) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
@@ -83,14 +104,18 @@ __device__ __forceinline__ void pair_tile_coords(int tile, const TcParams& p, in
 }
 
 // mapB2 is read only by the SwiGLU variant (the up-projection).
-template <int BN, bool OUT_BF16, bool SW>
+template <int BN, bool OUT_BF16, bool SW, bool F8>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_bf16_tc2_kernel(const __grid_constant__ CUtensorMap mapA,
                          const __grid_constant__ CUtensorMap mapB,
                          const __grid_constant__ CUtensorMap mapB2, const TcParams p) {
-  static_assert(!SW || (BN == 256 && OUT_BF16), "SwiGLU runs on the 256-wide bf16 instance");
+  static_assert(!SW || (BN == 256 && OUT_BF16 && !F8), "SwiGLU runs on the 256-wide bf16 instance");
   constexpr int OUT_BN = SW ? BN / 2 : BN;  // C columns per tile
-  using Cfg = PairCfg<BN>;
+  using Cfg = PairCfg<BN, F8>;
+  using G = Geom<F8>;
+  constexpr int BK = G::BK;
+  constexpr int A_STAGE_BYTES = G::A_STAGE_BYTES;
+  constexpr int B_BOX_BYTES = G::B_BOX_BYTES;
   constexpr int STAGES = Cfg::STAGES;
   constexpr int STAGE_BYTES = Cfg::STAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
@@ -168,7 +193,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         item(i, m0, n0, bn);
         const int a_row = m0 + (int)rank * BM_CTA;
         const int b_col = n0 + (int)rank * (SW ? OUT_BN / 2 : bn / 2);
-        const int b_boxes = bn / 2 / 64;
+        const int b_boxes = bn / 2 / G::BOX_N;
         const uint32_t tx_bytes = 2u * (A_STAGE_BYTES + b_boxes * B_BOX_BYTES);
         for (int kt = 0; kt < p.k_tiles; ++kt) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, a.timeout_ns, abort_flag)) {
@@ -183,7 +208,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           tma_load_2d_pair(a_tile(stage), &mapA, lead_full, kt * BK, a_row);
           for (int j = 0; j < b_boxes; ++j)
             tma_load_2d_pair(b_tile(stage) + j * B_BOX_BYTES, (SW && j == 1) ? &mapB2 : &mapB,
-                             lead_full, SW ? b_col : b_col + j * 64, kt * BK);
+                             lead_full, SW ? b_col : b_col + j * G::BOX_N, kt * BK);
           issued |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -210,8 +235,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ MMA issuer (leader)
     if (leader) {
       if (elect_one_sync()) {
-        constexpr uint32_t idesc_full = idesc_bf16_f32(BM, BN, /*A K-major*/ 0, /*B MN-major*/ 1);
-        constexpr uint32_t idesc_half = idesc_bf16_f32(BM, BN / 2, 0, 1);
+        const uint32_t idesc_full =
+            F8 ? idesc_f8_f32(BM, BN, (uint32_t)a.fmt_a, (uint32_t)a.fmt_b, /*A K-major*/ 0, /*B MN-major*/ 1)
+               : idesc_bf16_f32(BM, BN, /*A K-major*/ 0, /*B MN-major*/ 1);
+        const uint32_t idesc_half = idesc_bf16_f32(BM, BN / 2, 0, 1);  // bf16 only
         int stage = 0;
         uint32_t phase = 0;
         int acc = 0;
@@ -235,11 +262,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-              const uint64_t adesc = smem_desc_sw128(a_tile(stage) + kk * UMMA_K * 2, 16, 1024);
+            for (int kk = 0; kk < BK / G::UMMA_K; ++kk) {
+              const uint64_t adesc = smem_desc_sw128(a_tile(stage) + kk * G::A_KSTEP, 16, 1024);
               const uint64_t bdesc =
-                  smem_desc_sw128(b_tile(stage) + kk * UMMA_K * 128, B_BOX_BYTES, 1024);
-              tc_mma_f16_pair(d_tmem, adesc, bdesc, idesc, (kt | kk) != 0 ? 1u : 0u);
+                  smem_desc_sw128(b_tile(stage) + kk * G::B_KSTEP, B_BOX_BYTES, 1024);
+              if constexpr (F8)
+                tc_mma_f8_pair(d_tmem, adesc, bdesc, idesc, (kt | kk) != 0 ? 1u : 0u);
+              else
+                tc_mma_f16_pair(d_tmem, adesc, bdesc, idesc, (kt | kk) != 0 ? 1u : 0u);
             }
             issued_any = true;
             tc_commit_pair_mc(empty_bar(stage), kBothCtas);  // frees the stage in both CTAs
@@ -331,17 +361,18 @@ struct PairLaunchInfo {
   int max_clusters = 0;
 };
 
-template <int BN, bool OUT_BF16, bool SW>
+template <int BN, bool OUT_BF16, bool SW, bool F8 = false>
 int launch_pair_impl(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
                      const CUtensorMap* mapB2, int num_sms, cudaStream_t s, int* schedule) {
   constexpr int OUT_BN = SW ? BN / 2 : BN;
-  using Cfg = PairCfg<BN>;
+  using Cfg = PairCfg<BN, F8>;
+  constexpr int BK = Geom<F8>::BK;
   static PairLaunchInfo info[64];
   static std::mutex mu;
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  auto kernel = gemm_bf16_tc2_kernel<BN, OUT_BF16, SW>;
+  auto kernel = gemm_bf16_tc2_kernel<BN, OUT_BF16, SW, F8>;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -383,7 +414,7 @@ int launch_pair_impl(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorM
   const int pairs = info[dev].max_clusters;
   const long long rem = tiles % pairs;
   int clusters;
-  if (!SW && BN == 256 && split_tiles_enabled() && rem > 0 && 2 * rem <= pairs) {
+  if (!SW && !F8 && BN == 256 && split_tiles_enabled() && rem > 0 && 2 * rem <= pairs) {
     p.dp_tiles = (int)(tiles - rem);
     p.half_tiles = (int)(2 * rem);
     clusters = pairs;
@@ -412,6 +443,15 @@ int launch_bf16_tc_pair(const GemmArgs& a, const CUtensorMap* mapA, const CUtens
     return bf16 ? launch_pair_impl<128, true, false>(a, mapA, mapB, nullptr, num_sms, s, schedule)
                 : launch_pair_impl<128, false, false>(a, mapA, mapB, nullptr, num_sms, s, schedule);
   return cudaErrorInvalidValue;
+}
+
+int launch_fp8_tc_pair(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
+                       int num_sms, cudaStream_t s) {
+  if (a.in != Elem::FP8 || a.swiglu) return cudaErrorInvalidValue;
+  int schedule = 0;
+  return a.out == Elem::BF16
+             ? launch_pair_impl<256, true, false, true>(a, mapA, mapB, nullptr, num_sms, s, &schedule)
+             : launch_pair_impl<256, false, false, true>(a, mapA, mapB, nullptr, num_sms, s, &schedule);
 }
 
 int launch_bf16_swiglu_pair(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,

@@ -7,7 +7,11 @@
 // guards of the thread-tile kernel in 10.6 do), and a 4 x 4 register tile per
 // thread.  Accumulation is fp32 for both input types.
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
+
+#include <cstdint>
+#include <type_traits>
 
 #include "epilogue.cuh"
 #include "internal.h"
@@ -24,6 +28,21 @@ template <>
 __device__ __forceinline__ float to_f32<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// FP8 element (uint8_t) in format fmt (Fp8Fmt): every E4M3 and E5M2 value
+// is exact in fp16, so the conversion through fp16 is exact
+__device__ __forceinline__ float fp8_to_f32(uint8_t v, int fmt) {
+  const __half_raw h = __nv_cvt_fp8_to_halfraw(v, fmt == kE5M2 ? __NV_E5M2 : __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+template <typename T>
+__device__ __forceinline__ float load_in(const T* p, long long i, int fmt) {
+  if constexpr (std::is_same<T, uint8_t>::value)
+    return fp8_to_f32(p[i], fmt);
+  else
+    return to_f32<T>(p[i]);
+}
 
 template <typename T>
 __device__ __forceinline__ T from_f32(float v);
@@ -64,11 +83,12 @@ __global__ void __launch_bounds__(256) gemm_generic_kernel(GemmArgs a, int tiles
       const int idx = threadIdx.x + r * 256;
       const int am = idx / GK, ak = idx % GK;
       const long long gm = m0 + am, gk = k0 + ak;
-      As[ak][am] = (gm < a.M && gk < a.K) ? to_f32<TI>(A[gm * a.lda + gk]) : 0.f;
+      As[ak][am] = (gm < a.M && gk < a.K) ? load_in<TI>(A, gm * a.lda + gk, a.fmt_a) : 0.f;
       const int bk = idx / GT, bn = idx % GT;
       const long long hk = k0 + bk, hn = n0 + bn;
-      Bs[bk][bn] = (hk < a.K && hn < a.N) ? to_f32<TI>(B[hk * a.ldb + hn]) : 0.f;
-      if (SWIGLU) Bs2[SWIGLU ? bk : 0][bn] = (hk < a.K && hn < a.N) ? to_f32<TI>(B2[hk * a.ldb + hn]) : 0.f;
+      Bs[bk][bn] = (hk < a.K && hn < a.N) ? load_in<TI>(B, hk * a.ldb + hn, a.fmt_b) : 0.f;
+      if (SWIGLU)
+        Bs2[SWIGLU ? bk : 0][bn] = (hk < a.K && hn < a.N) ? load_in<TI>(B2, hk * a.ldb + hn, 0) : 0.f;
     }
     __syncthreads();
 #pragma unroll
@@ -134,6 +154,10 @@ int launch_generic(const GemmArgs& a, cudaStream_t s) {
     gemm_generic_kernel<__nv_bfloat16, __nv_bfloat16, false><<<grid, block, 0, s>>>(a, (int)tiles_n);
   } else if (a.in == Elem::BF16 && a.out == Elem::F32) {
     gemm_generic_kernel<__nv_bfloat16, float, false><<<grid, block, 0, s>>>(a, (int)tiles_n);
+  } else if (a.in == Elem::FP8 && a.out == Elem::BF16) {
+    gemm_generic_kernel<uint8_t, __nv_bfloat16, false><<<grid, block, 0, s>>>(a, (int)tiles_n);
+  } else if (a.in == Elem::FP8 && a.out == Elem::F32) {
+    gemm_generic_kernel<uint8_t, float, false><<<grid, block, 0, s>>>(a, (int)tiles_n);
   } else {
     return cudaErrorInvalidValue;
   }

@@ -7,7 +7,10 @@
 
 namespace g3 {
 
-enum class Elem : int { F32 = 0, BF16 = 1 };
+enum class Elem : int { F32 = 0, BF16 = 1, FP8 = 2 };
+
+// FP8 formats (values of gemm_fp8_format in the header).
+enum Fp8Fmt : int { kE4M3 = 0, kE5M2 = 1 };
 
 // Activations of the fused epilogue (values of gemm_activation in the header).
 enum Act : int { kActNone = 0, kActRelu = 1, kActSilu = 2, kActGelu = 3 };
@@ -29,6 +32,7 @@ struct GemmArgs {
   int act;              // Act applied last
   const void* B2;       // SwiGLU: the up-projection (K x N, leading dimension ldb), else null
   int swiglu;           // 1: C = silu(A*B) * (A*B2) (alpha 1, beta 0, no bias)
+  int fmt_a, fmt_b;     // in == FP8: the formats of A and B (Fp8Fmt)
 };
 
 // Location codes recorded with a device timeout (status[1]).
@@ -78,6 +82,12 @@ int launch_bf16_tc_pair(const GemmArgs& a, const CUtensorMap* mapA, const CUtens
                         int num_sms, cudaStream_t s, int* schedule);
 // SwiGLU on CTA pairs (a.swiglu): C tiles of 256 x 128; each CTA's B operand
 // is 64 columns of Bgate (mapB) and the same 64 columns of Bup (mapB2).
+// FP8 inputs (in == FP8) on CTA pairs, 256 x 256 C tiles: TMA tiles of A
+// (128 k x 128 m bytes) and B (128 n x 128 k bytes), 128-byte swizzle.
+int launch_fp8_tc_pair(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
+                       int num_sms, cudaStream_t s);
+constexpr int kF8BK = 128;
+
 int launch_bf16_swiglu_pair(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
                             const CUtensorMap* mapB2, int num_sms, cudaStream_t s);
 

@@ -208,6 +208,16 @@ __device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t a_desc
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// The same MMA on 8-bit operands (E4M3 / E5M2, formats in the instruction
+// descriptor): K = 32 per instruction, fp32 accumulate.
+__device__ __forceinline__ void tc_mma_f8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrive once on the barrier at offset `bar` in every CTA of `cta_mask` when
 // the pair's tcgen05 ops issued so far by this thread are done.
 __device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {
@@ -252,6 +262,20 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, ui
   return (1u << 4)              // D format: f32
          | (1u << 7)            // A format: bf16
          | (1u << 10)           // B format: bf16
+         | (a_mn_major << 15)   // A major
+         | (b_mn_major << 16)   // B major
+         | ((N >> 3) << 17)     // N / 8
+         | ((M >> 4) << 24);    // M / 16
+}
+
+// Instruction descriptor of kind::f8f6f4 with fp32 accumulation: A and B
+// formats 0 = E4M3, 1 = E5M2 (same field positions as kind::f16).
+__host__ __device__ constexpr uint32_t idesc_f8_f32(uint32_t M, uint32_t N, uint32_t a_fmt,
+                                                    uint32_t b_fmt, uint32_t a_mn_major,
+                                                    uint32_t b_mn_major) {
+  return (1u << 4)              // D format: f32
+         | (a_fmt << 7)         // A format
+         | (b_fmt << 10)        // B format
          | (a_mn_major << 15)   // A major
          | (b_mn_major << 16)   // B major
          | ((N >> 3) << 17)     // N / 8
