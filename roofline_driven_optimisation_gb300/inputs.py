@@ -199,3 +199,32 @@ def make_fp8(M: int, N: int, K: int, fmt_a: int = FP8_E4M3, fmt_b: int = FP8_E4M
     B = fp8_codes(torch.randn((K, N), generator=gen, dtype=torch.float32), fmt_b)
     C0 = torch.randn((M, N), generator=gen, dtype=torch.float32) if beta != 0.0 else None
     return Fp8Case(A, B, fmt_a, fmt_b, 1.0 / math.sqrt(max(K, 1)), beta, C0)
+
+
+@dataclasses.dataclass
+class Int4Case:
+    q: torch.Tensor                # K x N/2 packed codes (uint8), low nibble = even column
+    scales: torch.Tensor           # ceil(K/G) x N bf16
+    N: int
+    group: int
+    zero: int
+
+
+def pack_int4(codes: torch.Tensor) -> torch.Tensor:
+    """K x N codes (0..15, N even) -> K x N/2 bytes, even column in the low nibble."""
+    c = codes.to(torch.uint8)
+    return (c[:, 0::2] | (c[:, 1::2] << 4)).contiguous()
+
+
+def make_int4(K: int, N: int, group: int = 128, zero: int = 8, seed: int = 8) -> Int4Case:
+    """A K x N INT4 weight: codes uniform on 0..15, per-group scales uniform on
+    [0.003, 0.006] (with zero point 8 the weights then have the N(0, 0.02)
+    spread of the bf16 LLaMA stand-ins), bf16."""
+    if N % 2:
+        raise ValueError("N must be even (two codes per byte)")
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    codes = torch.randint(0, 16, (K, N), generator=gen)
+    groups = (K + group - 1) // group
+    scales = (0.003 + 0.003 * torch.rand((groups, N), generator=gen)).to(torch.bfloat16)
+    return Int4Case(pack_int4(codes), scales, N, group, zero)

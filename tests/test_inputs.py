@@ -66,3 +66,15 @@ def test_fp8_operands_are_seeded_codes():
     assert np.all(np.isfinite(a)) and np.all(np.isfinite(b))
     assert 0.5 < a.std() < 1.5 and 0.5 < b.std() < 1.5
     assert c1.alpha == 1 / 8
+
+
+def test_int4_weights_pack_and_spread():
+    from oracle import int4
+    c = inputs.make_int4(256, 64, group=128, zero=8, seed=1)
+    assert c.q.shape == (256, 32) and c.q.dtype == torch.uint8
+    assert c.scales.shape == (2, 64) and c.scales.dtype == torch.bfloat16
+    codes = int4.unpack(c.q, 64)
+    assert codes.min() == 0 and codes.max() == 15
+    w = int4.dequant_exact(c.q, c.scales, 64, 128, 8)
+    assert 0.012 < w.std() < 0.03
+    assert torch.equal(inputs.make_int4(256, 64, seed=1).q, c.q)

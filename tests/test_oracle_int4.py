@@ -1,0 +1,47 @@
+"""Pins of the INT4 weight decoding: the nibble order of the pages' example,
+hand-computed values, zero points, groups, and the single bf16 rounding."""
+import numpy as np
+import torch
+
+from oracle import int4
+
+
+def test_nibble_order_low_first():
+    # byte 0xA3 holds 3 (first element, low nibble) then 10 (high nibble)
+    q = np.array([[0xA3, 0x0F]], dtype=np.uint8)
+    assert int4.unpack(q, 4).tolist() == [[3, 10, 15, 0]]
+    assert int4.unpack(q, 3).tolist() == [[3, 10, 15]]
+
+
+def test_hand_values_with_groups_and_zero_point():
+    q = np.array([[0x21], [0x43], [0xF0]], dtype=np.uint8)      # rows k=0,1,2; 2 columns
+    s = torch.tensor([[0.5, 2.0], [0.25, -1.0]], dtype=torch.bfloat16)   # G = 2
+    w = int4.dequant_exact(q, s, 2, group=2, zero=8)
+    # k=0: codes (1, 2); k=1: (3, 4) -> group 0; k=2: (0, 15) -> group 1
+    assert w.tolist() == [[0.5 * -7, 2.0 * -6], [0.5 * -5, 2.0 * -4], [0.25 * -8, -1.0 * 7]]
+    # zero point 0 is the pages' plain scale * code
+    assert int4.dequant_exact(q, s, 2, 2, 0)[2].tolist() == [0.0, -15.0]
+
+
+def test_bf16_rounding_is_single_and_nearest_even():
+    # scale 1 + 2^-7 (exact in bf16) times 15 = 15 + 15/128 needs 11 bits;
+    # bf16 keeps 8: 15.1171875 -> nearest bf16 is 15.125
+    s = torch.tensor([[1.0 + 2.0 ** -7]], dtype=torch.bfloat16)
+    q = np.array([[0x0F]], dtype=np.uint8)
+    assert int4.dequant_exact(q, s, 1, 1, 0)[0, 0] == 15.1171875
+    assert int4.dequant_bf16(q, s, 1, 1, 0)[0, 0].item() == 15.125
+    # every code times every power-of-two scale is exact
+    codes = np.arange(16, dtype=np.uint8).reshape(1, 16)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    s2 = torch.full((1, 16), 0.125, dtype=torch.bfloat16)
+    assert int4.dequant_bf16(packed, s2, 16, 1, 8).float().tolist() == [[(c - 8) / 8 for c in range(16)]]
+
+
+def test_gemm_w4_is_gemm_of_the_dequantised_weight():
+    rng = np.random.default_rng(2)
+    A = rng.integers(-3, 4, size=(3, 4)).astype(np.float64)
+    q = rng.integers(0, 256, size=(4, 3)).astype(np.uint8)
+    s = torch.tensor([[1.0, 0.5, 2.0, 4.0, 1.0, 0.25]] * 2, dtype=torch.bfloat16)
+    got = int4.gemm_w4(A, q, s, 6, group=2, zero=8)
+    W = int4.dequant_exact(q, s, 6, 2, 8)   # powers of two: the bf16 rounding is exact
+    assert np.array_equal(got, A @ W)
