@@ -325,6 +325,7 @@ def run_ours(args):
     fused_ffn = measure_fused_ffn(g, torch, dev, s, hbm, bf16_peak) if rank == 0 else None
     fma_probe = measure_fp32_fma(g, torch, dev, fp32_peak / 1e12) if rank == 0 else None
     fp8 = measure_fp8(g, torch, dev, pk["bf16_tflops"]) if rank == 0 else None
+    int4_dq = measure_int4_dequant(g, torch, dev, hbm) if rank == 0 else None
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -341,6 +342,7 @@ def run_ours(args):
         "fused_ffn_swiglu": fused_ffn,
         "fp32_fma_probe": fma_probe,
         "fp8_gemm": fp8,
+        "int4_dequant": int4_dq,
         "e2e": e2e,
         "gpu_launches": len(parts) * args.steps,
         "clocks": clocks.summary(),
@@ -449,6 +451,36 @@ def measure_fp8(g, torch, dev, bf16_peak_tflops, reps=7):
     status, where = g.device_status(stream.cuda_stream)
     if status != 0:
         raise RuntimeError(f"device status {status} at {where} in the FP8 measurement")
+    return out
+
+
+def measure_int4_dequant(g, torch, dev, hbm, reps=7):
+    """INT4 dequantisation of a 16384 x 16384 weight (group 128, zero point 8)
+    to bf16 and to fp32, in HBM GB/s of algorithmic bytes (codes read once,
+    scales once, output written once; more than L2, so no flush).  Not part of
+    the step."""
+    from roofline_driven_optimisation_gb300 import inputs
+    stream = torch.cuda.current_stream(dev)
+    n = 16384
+    c = inputs.make_int4(n, n, group=128, zero=8, seed=8)
+    q, sc = c.q.to(dev), c.scales.to(dev)
+    out = {}
+    for name, dt in (("bf16_out", torch.bfloat16), ("f32_out", torch.float32)):
+        W = torch.empty((n, n), dtype=dt, device=dev)
+        g.int4_dequant(q, sc, n, 128, 8, W)
+        evs = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.int4_dequant(q, sc, n, 128, 8, W)
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+        by = q.numel() + sc.numel() * 2 + W.numel() * W.element_size()
+        out[name] = {"ms": round(ms, 4), "gbs": round(by / (ms * 1e-3) / 1e9, 1),
+                     "frac_hbm": round(by / (ms * 1e-3) / hbm, 4), "bytes": int(by)}
+        del W
     return out
 
 

@@ -167,6 +167,29 @@ int gemm_fp8_f32out(int M, int N, int K, float alpha, const uint8_t* A, int fmt_
                     cudaStream_t stream);
 
 /*
+ * INT4 weight dequantisation ("CUDA 算子工程 ch.4 内存层级与代价表", section
+ * 4.5.3: two 4-bit codes per byte, the first in the low nibble, times a
+ * scale):
+ *
+ *     W[k][n] = scales[k / group][n] * (q[k][n] - zero)
+ *
+ * q is K x N codes (0..15) packed along n: byte j of row k (row stride ldq
+ * bytes, ldq >= ceil(N/2)) holds column 2j in bits 0-3 and column 2j+1 in
+ * bits 4-7.  scales is ceil(K/group) x N bf16 (row stride lds >= N elements).
+ * zero is one integer in 0..15, and group >= 1.  W is K x N (ldw >= N),
+ * written as bf16 by gemm_int4_dequant (the exact fp32 value rounded once,
+ * nearest even) or as fp32 by gemm_int4_dequant_f32 (exact).  All pointers
+ * are DEVICE pointers owned by the caller.  The fast kernel needs N a
+ * multiple of 32 and 16-byte-aligned rows of q, scales and W.  Other shapes
+ * run a per-byte kernel with the same results.  Errors and asynchrony are
+ * as for the GEMM entry points.
+ */
+int gemm_int4_dequant(const uint8_t* q, int K, int N, int ldq, const gemm_bf16_t* scales, int lds,
+                      int group, int zero, gemm_bf16_t* W, int ldw, cudaStream_t stream);
+int gemm_int4_dequant_f32(const uint8_t* q, int K, int N, int ldq, const gemm_bf16_t* scales,
+                          int lds, int group, int zero, float* W, int ldw, cudaStream_t stream);
+
+/*
  * Message for the last non-OK return on the calling host thread ("" if none).
  * The string is owned by the library and valid until the next call on this
  * thread.
@@ -188,7 +211,9 @@ typedef enum {
   GEMM_PATH_GENERIC = 1,  /* correctness-first tiled kernel, any alignment */
   GEMM_PATH_F32_SIMT = 2, /* register-tiled FP32 kernel */
   GEMM_PATH_BF16_TC = 3,  /* tcgen05/TMEM/TMA warp-specialised kernel (bf16 or FP8 inputs) */
-  GEMM_PATH_SKINNY = 4    /* decode-shaped split-K kernel (bf16, M <= 16) */
+  GEMM_PATH_SKINNY = 4,   /* decode-shaped split-K kernel (bf16, M <= 16) */
+  GEMM_PATH_INT4 = 5      /* INT4 dequantisation, 32 codes per thread (reported only;
+                             the per-byte fallback reports GEMM_PATH_GENERIC) */
 } gemm_path;
 
 /*

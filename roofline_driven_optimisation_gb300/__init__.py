@@ -31,16 +31,16 @@ GEMM_ERR_UNSUPPORTED = 3
 GEMM_ERR_CUDA = 4
 GEMM_ERR_DEVICE_TIMEOUT = 5
 
-PATH_AUTO, PATH_GENERIC, PATH_F32_SIMT, PATH_BF16_TC, PATH_SKINNY = range(5)
+PATH_AUTO, PATH_GENERIC, PATH_F32_SIMT, PATH_BF16_TC, PATH_SKINNY, PATH_INT4 = range(6)
 ACT_NONE, ACT_RELU, ACT_SILU, ACT_GELU = range(4)
 FP8_E4M3, FP8_E5M2 = 0, 1
 PATH_NAMES = {PATH_AUTO: "none", PATH_GENERIC: "generic", PATH_F32_SIMT: "f32_simt",
-              PATH_BF16_TC: "bf16_tc", PATH_SKINNY: "skinny"}
+              PATH_BF16_TC: "bf16_tc", PATH_SKINNY: "skinny", PATH_INT4: "int4"}
 
 # every symbol the public header declares
 EXPORTS = ("gemm_f32", "gemm_bf16", "gemm_bf16_f32out", "gemm_f32_ex", "gemm_bf16_ex",
            "gemm_bf16_f32out_ex", "gemm_bf16_swiglu", "gemm_fp8", "gemm_fp8_f32out",
-           "gemm_get_last_error",
+           "gemm_int4_dequant", "gemm_int4_dequant_f32", "gemm_get_last_error",
            "gemm_device_status", "gemm_force_path", "gemm_last_path", "gemm_force_tile_n",
            "gemm_last_tile_n", "gemm_force_tc_pair", "gemm_last_tc_pair", "gemm_force_split_tiles",
            "gemm_last_k_split", "gemm_set_wait_timeout_ns", "gemm_selftest_wait_timeout",
@@ -85,6 +85,10 @@ def load(path: str | None = None):
             fn.restype = i
         lib.gemm_bf16_swiglu.argtypes = [i, i, i, vp, i, vp, vp, i, vp, i, vp]
         lib.gemm_bf16_swiglu.restype = i
+        for name in ("gemm_int4_dequant", "gemm_int4_dequant_f32"):
+            fn = getattr(lib, name)
+            fn.argtypes = [vp, i, i, i, vp, i, i, i, vp, i, vp]
+            fn.restype = i
         for name in ("gemm_fp8", "gemm_fp8_f32out"):
             fn = getattr(lib, name)
             fn.argtypes = [i, i, i, f, vp, i, i, vp, i, i, f, vp, i, vp]
@@ -161,6 +165,14 @@ def gemm_fp8(M, N, K, alpha, A, fmt_a, lda, B, fmt_b, ldb, beta, C, ldc, stream=
 def gemm_fp8_f32out(M, N, K, alpha, A, fmt_a, lda, B, fmt_b, ldb, beta, C, ldc, stream=0):
     _check(load().gemm_fp8_f32out(M, N, K, alpha, A, fmt_a, lda, B, fmt_b, ldb, beta, C, ldc,
                                   stream))
+
+
+def gemm_int4_dequant(q, K, N, ldq, scales, lds, group, zero, W, ldw, stream=0):
+    _check(load().gemm_int4_dequant(q, K, N, ldq, scales, lds, group, zero, W, ldw, stream))
+
+
+def gemm_int4_dequant_f32(q, K, N, ldq, scales, lds, group, zero, W, ldw, stream=0):
+    _check(load().gemm_int4_dequant_f32(q, K, N, ldq, scales, lds, group, zero, W, ldw, stream))
 
 
 def device_status(stream=0) -> tuple[int, int]:
@@ -299,3 +311,22 @@ def gemm_fp8_tensors(A, fmt_a: int, B, fmt_b: int, C, alpha: float = 1.0, beta: 
     else:
         raise TypeError(f"unsupported output dtype {C.dtype}")
     return C
+
+
+def int4_dequant(q, scales, N: int, group: int, zero: int, W, stream=None):
+    """W = scales[k // group][n] * (q[k][n] - zero) for CUDA tensors: q K x ceil(N/2)
+    uint8 codes, scales bf16, W bf16 or fp32 (K x N).  Argument marshalling only."""
+    import torch
+    K = q.shape[0]
+    if W.shape[0] != K or W.shape[1] != N or q.dtype != torch.uint8 or scales.dtype != torch.bfloat16:
+        raise ValueError("int4_dequant(): shape or dtype mismatch")
+    s = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
+    args = (q.data_ptr(), K, N, _ld(q), scales.data_ptr(), _ld(scales), group, zero, W.data_ptr(),
+            _ld(W), s)
+    if W.dtype == torch.bfloat16:
+        gemm_int4_dequant(*args)
+    elif W.dtype == torch.float32:
+        gemm_int4_dequant_f32(*args)
+    else:
+        raise TypeError(f"unsupported output dtype {W.dtype}")
+    return W

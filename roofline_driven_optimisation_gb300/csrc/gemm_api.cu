@@ -317,6 +317,36 @@ int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int 
   return GEMM_OK;
 }
 
+int int4_dequant(const uint8_t* q, int K, int N, int ldq, const void* scales, int lds, int group,
+                int zero, void* W, int ldw, bool out_bf16, cudaStream_t stream) {
+  t_msg[0] = '\0';
+  t_last_path = GEMM_PATH_AUTO;
+  t_last_k_split = 1;
+  if (K < 0 || N < 0) return fail(GEMM_ERR_INVALID_ARG, "negative size K=%d N=%d", K, N);
+  if (group < 1) return fail(GEMM_ERR_INVALID_ARG, "group size %d < 1", group);
+  if (zero < 0 || zero > 15) return fail(GEMM_ERR_INVALID_ARG, "zero point %d outside 0..15", zero);
+  const int bytes_per_row = (N + 1) / 2;
+  if (ldq < (bytes_per_row > 1 ? bytes_per_row : 1) || lds < (N > 1 ? N : 1) || ldw < (N > 1 ? N : 1))
+    return fail(GEMM_ERR_INVALID_ARG, "leading dimension too small (ldq=%d lds=%d ldw=%d, N=%d)", ldq,
+                lds, ldw, N);
+  if (K == 0 || N == 0) return GEMM_OK;
+  if (q == nullptr || scales == nullptr || W == nullptr)
+    return fail(GEMM_ERR_INVALID_ARG, "q, scales or W is NULL");
+  if ((reinterpret_cast<uintptr_t>(scales) & 1u) ||
+      (reinterpret_cast<uintptr_t>(W) & (out_bf16 ? 1u : 3u)))
+    return fail(GEMM_ERR_MISALIGNED, "scales or W is not aligned to its element size");
+  DeviceInfo* dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc != GEMM_OK) return rc;
+  int vec = 0;
+  const int err = launch_int4_dequant(q, K, N, ldq, scales, lds, group, zero, W, ldw, out_bf16,
+                                      dev->num_sms, stream, &vec);
+  if (err != cudaSuccess)
+    return fail(GEMM_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString((cudaError_t)err));
+  t_last_path = vec ? GEMM_PATH_INT4 : GEMM_PATH_GENERIC;
+  return GEMM_OK;
+}
+
 __global__ void selftest_wait_kernel(int* status, uint64_t timeout_ns) {
   __shared__ uint64_t bar;
   if (threadIdx.x == 0) {
@@ -375,6 +405,16 @@ int gemm_fp8_f32out(int M, int N, int K, float alpha, const uint8_t* A, int fmt_
                     cudaStream_t stream) {
   return g3::run(Elem::FP8, Elem::F32, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, nullptr,
                  g3::kActNone, stream, false, nullptr, fmt_a, fmt_b);
+}
+
+int gemm_int4_dequant(const uint8_t* q, int K, int N, int ldq, const gemm_bf16_t* scales, int lds,
+                      int group, int zero, gemm_bf16_t* W, int ldw, cudaStream_t stream) {
+  return g3::int4_dequant(q, K, N, ldq, scales, lds, group, zero, W, ldw, true, stream);
+}
+
+int gemm_int4_dequant_f32(const uint8_t* q, int K, int N, int ldq, const gemm_bf16_t* scales,
+                          int lds, int group, int zero, float* W, int ldw, cudaStream_t stream) {
+  return g3::int4_dequant(q, K, N, ldq, scales, lds, group, zero, W, ldw, false, stream);
 }
 
 int gemm_f32_ex(int M, int N, int K, float alpha, const float* A, int lda, const float* B, int ldb,

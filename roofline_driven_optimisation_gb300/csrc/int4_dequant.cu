@@ -1,0 +1,152 @@
+// INT4 weight dequantisation: W[k][n] = s[k / G][n] * (q[k][n] - z), written
+// as bf16 (one rounding of the exact fp32 value) or as fp32 (exact).
+//
+// "CUDA 算子工程 ch.4 内存层级与代价表", section 4.5.3, measures this kernel:
+// reading one packed byte per thread is instruction-bound (256 GB/s on its
+// GPU), reading 16 bytes (32 codes) per thread and expanding them in
+// registers with vector stores reaches 2.1 TB/s.  Here each thread takes
+// items of 32 codes of one row (one 16-byte load of codes, the 32 scales of
+// those columns from L1/L2, four or eight 16-byte stores), keeps four items'
+// loads in flight, and the grid covers every SM at full occupancy, so the
+// kernel runs at the HBM roofline: about 2.5 bytes per weight (0.5 of codes,
+// 2 of bf16 output) and a few ALU operations.  Calls the vector path cannot
+// take (N not a multiple of 32, unaligned rows) run a per-byte kernel.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+
+namespace g3 {
+namespace {
+
+constexpr int THREADS = 256;
+constexpr int UNROLL = 4;
+
+// fp32 (code - zero) for the two codes of a byte, exact: the magic-number
+// float 2^23 + c has c in its low mantissa bits
+__device__ __forceinline__ float code_lo(uint32_t word, int byte) {
+  return __uint_as_float(0x4B000000u | ((word >> (8 * byte)) & 0xFu)) - 8388608.f;
+}
+__device__ __forceinline__ float code_hi(uint32_t word, int byte) {
+  return __uint_as_float(0x4B000000u | ((word >> (8 * byte + 4)) & 0xFu)) - 8388608.f;
+}
+
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(THREADS) int4_dequant_vec(const uint8_t* __restrict__ q, long long ldq,
+                                                            const __nv_bfloat16* __restrict__ s,
+                                                            long long lds, int group, int zero,
+                                                            void* __restrict__ w, long long ldw,
+                                                            int chunks, long long items) {
+  const long long stride = (long long)gridDim.x * THREADS;
+  const float fz = (float)zero;
+  for (long long base = (long long)blockIdx.x * THREADS + threadIdx.x; base < items;
+       base += stride * UNROLL) {
+    uint4 pk[UNROLL];
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const long long it = base + u * stride;
+      if (it < items) {
+        const long long k = it / chunks, c = it % chunks;
+        pk[u] = __ldcs(reinterpret_cast<const uint4*>(q + k * ldq + c * 16));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const long long it = base + u * stride;
+      if (it >= items) break;
+      const long long k = it / chunks, c = it % chunks;
+      const uint4* sp = reinterpret_cast<const uint4*>(s + (k / group) * lds + c * 32);
+      const uint32_t words[4] = {pk[u].x, pk[u].y, pk[u].z, pk[u].w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {          // 8 columns per word of codes
+        const uint4 sv = __ldg(sp + h);       // their 8 scales
+        const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+        float v[8];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const float s0 = __uint_as_float(sw[b] << 16), s1 = __uint_as_float(sw[b] & 0xFFFF0000u);
+          v[2 * b] = s0 * (code_lo(words[h], b) - fz);
+          v[2 * b + 1] = s1 * (code_hi(words[h], b) - fz);
+        }
+        if (OUT_BF16) {
+          uint4 o;
+          o.x = pack2_bf16(v[0], v[1]);
+          o.y = pack2_bf16(v[2], v[3]);
+          o.z = pack2_bf16(v[4], v[5]);
+          o.w = pack2_bf16(v[6], v[7]);
+          __stcs(reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(w) + k * ldw + c * 32 + h * 8), o);
+        } else {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(w) + k * ldw + c * 32 + h * 8);
+          __stcs(dst, make_float4(v[0], v[1], v[2], v[3]));
+          __stcs(dst + 1, make_float4(v[4], v[5], v[6], v[7]));
+        }
+      }
+    }
+  }
+}
+
+// one byte (two columns; the high nibble of a last odd column is padding)
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(THREADS) int4_dequant_bytes(const uint8_t* __restrict__ q, long long ldq,
+                                                              const __nv_bfloat16* __restrict__ s,
+                                                              long long lds, int group, int zero,
+                                                              void* __restrict__ w, long long ldw, int N,
+                                                              int bytes_per_row, long long items) {
+  const long long stride = (long long)gridDim.x * THREADS;
+  for (long long it = (long long)blockIdx.x * THREADS + threadIdx.x; it < items; it += stride) {
+    const long long k = it / bytes_per_row, j = it % bytes_per_row;
+    const uint32_t b = q[k * ldq + j];
+    const __nv_bfloat16* srow = s + (k / group) * lds;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const long long n = 2 * j + e;
+      if (n >= N) break;
+      const float code = (float)((b >> (4 * e)) & 0xFu);
+      const float v = __bfloat162float(srow[n]) * (code - (float)zero);
+      if (OUT_BF16)
+        static_cast<__nv_bfloat16*>(w)[k * ldw + n] = __float2bfloat16_rn(v);
+      else
+        static_cast<float*>(w)[k * ldw + n] = v;
+    }
+  }
+}
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+int launch_int4_dequant(const uint8_t* q, int K, int N, int ldq, const void* scales, int lds,
+                        int group, int zero, void* w, int ldw, bool out_bf16, int num_sms,
+                        cudaStream_t st, int* vector_path) {
+  const auto* s = static_cast<const __nv_bfloat16*>(scales);
+  const int osz = out_bf16 ? 2 : 4;
+  const bool vec = N % 32 == 0 && al16(q) && ldq % 16 == 0 && al16(s) && lds % 8 == 0 && al16(w) &&
+                   ((long long)ldw * osz) % 16 == 0;
+  *vector_path = vec ? 1 : 0;
+  const unsigned grid = (unsigned)num_sms * (2048 / THREADS);
+  if (vec) {
+    const int chunks = N / 32;
+    const long long items = (long long)K * chunks;
+    if (out_bf16)
+      int4_dequant_vec<true><<<grid, THREADS, 0, st>>>(q, ldq, s, lds, group, zero, w, ldw, chunks, items);
+    else
+      int4_dequant_vec<false><<<grid, THREADS, 0, st>>>(q, ldq, s, lds, group, zero, w, ldw, chunks, items);
+  } else {
+    const int bpr = (N + 1) / 2;
+    const long long items = (long long)K * bpr;
+    if (out_bf16)
+      int4_dequant_bytes<true><<<grid, THREADS, 0, st>>>(q, ldq, s, lds, group, zero, w, ldw, N, bpr, items);
+    else
+      int4_dequant_bytes<false><<<grid, THREADS, 0, st>>>(q, ldq, s, lds, group, zero, w, ldw, N, bpr, items);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace g3

@@ -99,6 +99,12 @@ int launch_skinny(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap*
                   const CUtensorMap* mapB2, int num_sms, cudaStream_t s, int* k_split);
 constexpr int kSkMaxM = 16, kSkBN = 128, kSkBK = 64;
 
+// INT4 dequantisation W = s[k / G][n] * (q - z) (bf16 or fp32 W);
+// *vector_path = 1 when the 32-codes-per-thread kernel ran.
+int launch_int4_dequant(const uint8_t* q, int K, int N, int ldq, const void* scales, int lds,
+                        int group, int zero, void* w, int ldw, bool out_bf16, int num_sms,
+                        cudaStream_t st, int* vector_path);
+
 int launch_selftest_wait(int* status, uint64_t timeout_ns, cudaStream_t s);
 
 }  // namespace g3
