@@ -457,8 +457,11 @@ def measure_fp8(g, torch, dev, bf16_peak_tflops, reps=7):
 def measure_int4_dequant(g, torch, dev, hbm, reps=7):
     """INT4 dequantisation of a 16384 x 16384 weight (group 128, zero point 8)
     to bf16 and to fp32, in HBM GB/s of algorithmic bytes (codes read once,
-    scales once, output written once; more than L2, so no flush).  Not part of
-    the step."""
+    scales once, output written once; more than L2, so no flush).  The output
+    is 80-89 % of the bytes and HBM writes alone run slower than a copy, so
+    the write rate of a plain fill of the same buffer is measured too and the
+    kernel is also scored against max(bytes / copy peak, written bytes / fill
+    rate).  Not part of the step."""
     from roofline_driven_optimisation_gb300 import inputs
     stream = torch.cuda.current_stream(dev)
     n = 16384
@@ -477,9 +480,22 @@ def measure_int4_dequant(g, torch, dev, hbm, reps=7):
             evs.append((e0, e1))
         torch.cuda.synchronize(dev)
         ms = statistics.median(a.elapsed_time(b) for a, b in evs)
-        by = q.numel() + sc.numel() * 2 + W.numel() * W.element_size()
+        fills = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            W.fill_(1.5)   # a non-zero value: zero fills can take a special memset path
+            e1.record(stream)
+            fills.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        wby = W.numel() * W.element_size()
+        fill_gbs = wby / (statistics.median(a.elapsed_time(b) for a, b in fills) * 1e-3) / 1e9
+        by = q.numel() + sc.numel() * 2 + wby
+        bound_ms = max(by / hbm, wby / (fill_gbs * 1e9)) * 1e3
         out[name] = {"ms": round(ms, 4), "gbs": round(by / (ms * 1e-3) / 1e9, 1),
-                     "frac_hbm": round(by / (ms * 1e-3) / hbm, 4), "bytes": int(by)}
+                     "frac_hbm": round(by / (ms * 1e-3) / hbm, 4), "bytes": int(by),
+                     "fill_gbs": round(fill_gbs, 1), "write_aware_bound_ms": round(bound_ms, 4),
+                     "frac_write_aware_bound": round(bound_ms / ms, 4)}
         del W
     return out
 

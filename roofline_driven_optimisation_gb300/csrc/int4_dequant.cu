@@ -6,11 +6,13 @@
 // GPU), reading 16 bytes (32 codes) per thread and expanding them in
 // registers with vector stores reaches 2.1 TB/s.  Here each thread takes
 // items of 32 codes of one row (one 16-byte load of codes, the 32 scales of
-// those columns from L1/L2, four or eight 16-byte stores), keeps four items'
-// loads in flight, and the grid covers every SM at full occupancy, so the
-// kernel runs at the HBM roofline: about 2.5 bytes per weight (0.5 of codes,
-// 2 of bf16 output) and a few ALU operations.  Calls the vector path cannot
-// take (N not a multiple of 32, unaligned rows) run a per-byte kernel.
+// those columns from L1/L2, four 16-byte bf16 stores), keeps four items'
+// loads in flight, and the grid covers every SM at full occupancy.  With
+// fp32 output the kernel is bound by HBM writes (4 bytes per weight), and
+// one thread per 8 columns makes every warp store 1 KB of contiguous
+// memory, which keeps the write stream at the device's fill rate.  Calls the
+// vector paths cannot take (unaligned rows, N not a multiple of 32 for bf16
+// or 8 for fp32) run a per-byte kernel.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -92,6 +94,59 @@ __global__ void __launch_bounds__(THREADS) int4_dequant_vec(const uint8_t* __res
   }
 }
 
+// One octet = 8 consecutive columns of one row: 4 bytes of codes, 8 scales
+// (16 bytes), 16 or 32 bytes of output.  Consecutive threads take
+// consecutive octets, so a warp reads 128 contiguous bytes of codes and
+// writes 512 (bf16) or 1024 (fp32) contiguous bytes per instruction.
+template <bool OUT_BF16, int UNR>
+__global__ void __launch_bounds__(THREADS) int4_dequant_octets(const uint8_t* __restrict__ q, long long ldq,
+                                                            const __nv_bfloat16* __restrict__ s,
+                                                            long long lds, int group, int zero,
+                                                            void* __restrict__ w, long long ldw,
+                                                            int octets, long long items) {
+  const long long stride = (long long)gridDim.x * THREADS;
+  const float fz = (float)zero;
+  for (long long base = (long long)blockIdx.x * THREADS + threadIdx.x; base < items;
+       base += stride * UNR) {
+    uint32_t pk[UNR];
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const long long it = base + u * stride;
+      if (it < items) {
+        const long long k = it / octets, o = it % octets;
+        pk[u] = __ldcs(reinterpret_cast<const unsigned int*>(q + k * ldq + o * 4));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const long long it = base + u * stride;
+      if (it >= items) break;
+      const long long k = it / octets, o = it % octets;
+      const uint4 sv = __ldg(reinterpret_cast<const uint4*>(s + (k / group) * lds + o * 8));
+      const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+      float v[8];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const float s0 = __uint_as_float(sw[b] << 16), s1 = __uint_as_float(sw[b] & 0xFFFF0000u);
+        v[2 * b] = s0 * (code_lo(pk[u], b) - fz);
+        v[2 * b + 1] = s1 * (code_hi(pk[u], b) - fz);
+      }
+      if (OUT_BF16) {
+        uint4 ov;
+        ov.x = pack2_bf16(v[0], v[1]);
+        ov.y = pack2_bf16(v[2], v[3]);
+        ov.z = pack2_bf16(v[4], v[5]);
+        ov.w = pack2_bf16(v[6], v[7]);
+        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(w) + k * ldw + o * 8) = ov;
+      } else {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(w) + k * ldw + o * 8);
+        dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+        dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+      }
+    }
+  }
+}
+
 // one byte (two columns; the high nibble of a last odd column is padding)
 template <bool OUT_BF16>
 __global__ void __launch_bounds__(THREADS) int4_dequant_bytes(const uint8_t* __restrict__ q, long long ldq,
@@ -127,17 +182,21 @@ int launch_int4_dequant(const uint8_t* q, int K, int N, int ldq, const void* sca
                         cudaStream_t st, int* vector_path) {
   const auto* s = static_cast<const __nv_bfloat16*>(scales);
   const int osz = out_bf16 ? 2 : 4;
-  const bool vec = N % 32 == 0 && al16(q) && ldq % 16 == 0 && al16(s) && lds % 8 == 0 && al16(w) &&
-                   ((long long)ldw * osz) % 16 == 0;
+  const bool w_ok = al16(s) && lds % 8 == 0 && al16(w) && ((long long)ldw * osz) % 16 == 0;
+  const bool vec = out_bf16 ? (w_ok && N % 32 == 0 && al16(q) && ldq % 16 == 0)
+                            : (w_ok && N % 8 == 0 && (reinterpret_cast<uintptr_t>(q) & 3u) == 0 &&
+                               ldq % 4 == 0);
   *vector_path = vec ? 1 : 0;
   const unsigned grid = (unsigned)num_sms * (2048 / THREADS);
-  if (vec) {
+  if (vec && out_bf16) {
     const int chunks = N / 32;
     const long long items = (long long)K * chunks;
-    if (out_bf16)
-      int4_dequant_vec<true><<<grid, THREADS, 0, st>>>(q, ldq, s, lds, group, zero, w, ldw, chunks, items);
-    else
-      int4_dequant_vec<false><<<grid, THREADS, 0, st>>>(q, ldq, s, lds, group, zero, w, ldw, chunks, items);
+    int4_dequant_vec<true><<<grid, THREADS, 0, st>>>(q, ldq, s, lds, group, zero, w, ldw, chunks, items);
+  } else if (vec) {
+    const int octets = N / 8;
+    const long long items = (long long)K * octets;
+    int4_dequant_octets<false, 8><<<grid, THREADS, 0, st>>>(q, ldq, s, lds, group, zero, w, ldw, octets,
+                                                            items);
   } else {
     const int bpr = (N + 1) / 2;
     const long long items = (long long)K * bpr;
