@@ -53,3 +53,32 @@ def gemm_w4(A, q_bytes, scales, N: int, group: int, zero: int, alpha=1.0, beta=0
     """fp64 alpha * A @ W + beta * C0 with W the bf16 dequantised weight."""
     W = dequant_bf16(q_bytes, scales, N, group, zero)
     return gemm(A, W, alpha, beta, None if C0 is None else to_f64(C0), threads)
+
+
+def gemm_w4_exact(A, q_bytes, scales, N: int, group: int, zero: int, alpha=1.0, beta=0.0, C0=None,
+                  threads=None) -> np.ndarray:
+    """fp64 alpha * A @ W + beta * C0 with W = s * (q - z) exact (the INT4 GEMM
+    that never rounds the weight: the integers q - z enter the products and
+    each group's sum is scaled)."""
+    W = dequant_exact(q_bytes, scales, N, group, zero)
+    return gemm(A, W, alpha, beta, None if C0 is None else to_f64(C0), threads)
+
+
+# Order of the eight codes of one 32-bit word in the K-packed layout: slot s
+# (bits 4s..4s+3) holds the code of k = 8j + SLOT_K[s], so that bits 0-3 and
+# 16-19 of (word >> 4i) are the codes of k = 8j + 2i and 8j + 2i + 1.
+SLOT_K = (0, 2, 4, 6, 1, 3, 5, 7)
+
+
+def repack_kmajor(q_bytes, K: int, N: int) -> np.ndarray:
+    """K-packed layout of a K x N weight: row n holds ceil(K/8) little-endian
+    32-bit words, word j packing the codes of k = 8j..8j+7 in the slot order
+    SLOT_K (codes past K are 0).  Returns N x 4*ceil(K/8) bytes."""
+    codes = unpack(q_bytes, N)                   # K x N
+    words = (K + 7) // 8
+    padded = np.zeros((words * 8, N), dtype=np.int64)
+    padded[:K] = codes
+    out = np.zeros((N, words), dtype=np.uint64)
+    for s, dk in enumerate(SLOT_K):
+        out |= (padded[dk::8].T.astype(np.uint64) << np.uint64(4 * s))
+    return out.astype("<u4").view(np.uint8).reshape(N, 4 * words)

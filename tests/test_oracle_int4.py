@@ -45,3 +45,46 @@ def test_gemm_w4_is_gemm_of_the_dequantised_weight():
     got = int4.gemm_w4(A, q, s, 6, group=2, zero=8)
     W = int4.dequant_exact(q, s, 6, 2, 8)   # powers of two: the bf16 rounding is exact
     assert np.array_equal(got, A @ W)
+
+
+def test_kmajor_repack_slot_order():
+    # column 0 holds k = 0..7 -> codes 1..8; column 1 holds 15 everywhere
+    K, N = 8, 2
+    codes = np.stack([np.arange(1, 9), np.full(8, 15)], axis=1)
+    q = (codes[:, 0] | (codes[:, 1] << 4)).astype(np.uint8).reshape(K, 1)
+    r = int4.repack_kmajor(q, K, N)
+    assert r.shape == (2, 4)
+    w0 = int.from_bytes(r[0].tobytes(), "little")
+    # slots 0..7 hold k = 0,2,4,6,1,3,5,7 -> codes 1,3,5,7,2,4,6,8
+    assert [(w0 >> (4 * s)) & 0xF for s in range(8)] == [1, 3, 5, 7, 2, 4, 6, 8]
+    # bits 0-3 and 16-19 of (word >> 4i) are k = 2i and 2i + 1
+    for i in range(4):
+        assert ((w0 >> (4 * i)) & 0xF, (w0 >> (4 * i + 16)) & 0xF) == (2 * i + 1, 2 * i + 2)
+    assert int.from_bytes(r[1].tobytes(), "little") == 0xFFFFFFFF
+
+
+def test_kmajor_repack_round_trip_and_padding():
+    rng = np.random.default_rng(9)
+    K, N = 21, 6
+    codes = rng.integers(0, 16, size=(K, N))
+    q = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    r = int4.repack_kmajor(q, K, N)
+    assert r.shape == (N, 12)
+    words = r.view("<u4").reshape(N, 3)
+    back = np.zeros((24, N), dtype=np.int64)
+    for s, dk in enumerate(int4.SLOT_K):
+        back[dk::8] = ((words >> (4 * s)) & 0xF).T
+    assert np.array_equal(back[:K], codes) and not back[K:].any()
+
+
+def test_exact_w4_gemm_differs_from_rounded_only_by_the_rounding():
+    rng = np.random.default_rng(4)
+    A = rng.standard_normal((3, 64))
+    q = rng.integers(0, 256, size=(64, 4)).astype(np.uint8)
+    s = torch.tensor(rng.uniform(0.003, 0.006, size=(1, 8)), dtype=torch.bfloat16)
+    exact = int4.gemm_w4_exact(A, q, s, 8, 64, 8)
+    W = int4.dequant_exact(q, s, 8, 64, 8)
+    assert np.allclose(exact, A @ W, rtol=1e-13, atol=1e-15)
+    rounded = int4.gemm_w4(A, q, s, 8, 64, 8)
+    scale = np.abs(A) @ np.abs(W)
+    assert np.max(np.abs(rounded - exact) / scale.max()) <= 2.0 ** -9
