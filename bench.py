@@ -326,6 +326,7 @@ def run_ours(args):
     fma_probe = measure_fp32_fma(g, torch, dev, fp32_peak / 1e12) if rank == 0 else None
     fp8 = measure_fp8(g, torch, dev, pk["bf16_tflops"]) if rank == 0 else None
     int4_dq = measure_int4_dequant(g, torch, dev, hbm) if rank == 0 else None
+    w4 = measure_w4_decode(g, torch, dev, hbm) if rank == 0 else None
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -343,6 +344,7 @@ def run_ours(args):
         "fp32_fma_probe": fma_probe,
         "fp8_gemm": fp8,
         "int4_dequant": int4_dq,
+        "w4a16_decode": w4,
         "e2e": e2e,
         "gpu_launches": len(parts) * args.steps,
         "clocks": clocks.summary(),
@@ -457,11 +459,8 @@ def measure_fp8(g, torch, dev, bf16_peak_tflops, reps=7):
 def measure_int4_dequant(g, torch, dev, hbm, reps=7):
     """INT4 dequantisation of a 16384 x 16384 weight (group 128, zero point 8)
     to bf16 and to fp32, in HBM GB/s of algorithmic bytes (codes read once,
-    scales once, output written once; more than L2, so no flush).  The output
-    is 80-89 % of the bytes and HBM writes alone run slower than a copy, so
-    the write rate of a plain fill of the same buffer is measured too and the
-    kernel is also scored against max(bytes / copy peak, written bytes / fill
-    rate).  Not part of the step."""
+    scales once, output written once; more than L2, so no flush).  Not part
+    of the step."""
     from roofline_driven_optimisation_gb300 import inputs
     stream = torch.cuda.current_stream(dev)
     n = 16384
@@ -480,24 +479,58 @@ def measure_int4_dequant(g, torch, dev, hbm, reps=7):
             evs.append((e0, e1))
         torch.cuda.synchronize(dev)
         ms = statistics.median(a.elapsed_time(b) for a, b in evs)
-        fills = []
-        for _ in range(reps):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            W.fill_(1.5)   # a non-zero value: zero fills can take a special memset path
-            e1.record(stream)
-            fills.append((e0, e1))
-        torch.cuda.synchronize(dev)
-        wby = W.numel() * W.element_size()
-        fill_gbs = wby / (statistics.median(a.elapsed_time(b) for a, b in fills) * 1e-3) / 1e9
-        by = q.numel() + sc.numel() * 2 + wby
-        bound_ms = max(by / hbm, wby / (fill_gbs * 1e9)) * 1e3
+        by = q.numel() + sc.numel() * 2 + W.numel() * W.element_size()
         out[name] = {"ms": round(ms, 4), "gbs": round(by / (ms * 1e-3) / 1e9, 1),
-                     "frac_hbm": round(by / (ms * 1e-3) / hbm, 4), "bytes": int(by),
-                     "fill_gbs": round(fill_gbs, 1), "write_aware_bound_ms": round(bound_ms, 4),
-                     "frac_write_aware_bound": round(bound_ms / ms, 4)}
+                     "frac_hbm": round(by / (ms * 1e-3) / hbm, 4), "bytes": int(by)}
         del W
     return out
+
+
+def measure_w4_decode(g, torch, dev, hbm, iters=20):
+    """INT4-weight decode GEMMs (group 128, zero point 8, bf16 X and C, beta 1)
+    on the six LLaMA-7B weight shapes at M = 1, 4, 16: the 18 calls back to
+    back, events around the run, median of `iters`.  Algorithmic bytes: codes
+    (K*N/2) and scales once, X, C read and written.  Not part of the step."""
+    from roofline_driven_optimisation_gb300 import inputs
+    stream = torch.cuda.current_stream(dev)
+    s = stream.cuda_stream
+    weights = {}
+    for w in WEIGHTS:
+        K, N = inputs.LLAMA7B_WEIGHTS[w]
+        c = inputs.make_int4(K, N, group=128, zero=8, seed=20 + len(weights))
+        weights[w] = (K, N, g.int4_repack(c.q.to(dev), K, N), c.scales.to(dev))
+    gen = torch.Generator().manual_seed(21)
+    calls, by = [], 0
+    for m in DECODE_MS:
+        for w in WEIGHTS:
+            K, N, qk, sc = weights[w]
+            X = torch.randn((m, K), generator=gen).to(torch.bfloat16).to(dev)
+            C = torch.randn((m, N), generator=gen).to(torch.bfloat16).to(dev)
+            calls.append((m, N, K, X, qk, sc, C))
+            by += K * N // 2 + sc.numel() * 2 + 2 * m * K + 4 * m * N
+
+    def run():
+        for m, N, K, X, qk, sc, C in calls:
+            g.gemm_w4a16(m, N, K, 1.0, X.data_ptr(), K, qk.data_ptr(), sc.data_ptr(), N, 128, 8, 1.0,
+                         C.data_ptr(), N, s)
+
+    for _ in range(3):
+        run()
+    evs = []
+    for _ in range(iters):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run()
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize(dev)
+    status, where = g.device_status(s)
+    if status != 0:
+        raise RuntimeError(f"device status {status} at {where} in the INT4 decode measurement")
+    ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+    return {"launches": len(calls), "ms": round(ms, 5), "bytes": int(by),
+            "gbs": round(by / (ms * 1e-3) / 1e9, 1), "frac_hbm": round(by / (ms * 1e-3) / hbm, 4),
+            "flops": int(sum(2 * m * N * K for m, N, K, *_ in calls))}
 
 
 def measure_fused_ffn(g, torch, dev, s, hbm, bf16_peak, reps=7):

@@ -190,6 +190,46 @@ int gemm_int4_dequant_f32(const uint8_t* q, int K, int N, int ldq, const gemm_bf
                           int lds, int group, int zero, float* W, int ldw, cudaStream_t stream);
 
 /*
+ * INT4 weight-only decode GEMM ("CUDA 算子工程 ch.4 内存层级与代价表",
+ * section 4.5.3, dequantisation fused into its consumer as "Kernel 性能从何而来"
+ * section "优化 Memory-Bound Kernel" asks):
+ *
+ *     C = alpha * X * W + beta * C,   W[k][n] = scales[k / group][n] * (q[k][n] - zero)
+ *
+ * X is M x K bf16 (ldx >= K), C is M x N (ldc >= N), bf16 (gemm_w4a16) or
+ * fp32 (gemm_w4a16_f32out), scales and zero as for gemm_int4_dequant.  The
+ * weight is the exact value: the products take the integers q - zero and each
+ * group's fp32 sum is multiplied by its scale, so W is never rounded.  qk holds
+ * the codes in the tiled layout that gemm_int4_repack writes
+ * (gemm_w4_packed_bytes(K, N) bytes, 16-byte aligned).  beta == 0 never reads
+ * C.  The fast path is the tcgen05 decode kernel.  It needs 1 <= M <= 16,
+ * group a multiple of 64 or group >= K, and X 16-byte aligned with ldx a
+ * multiple of 8.  Any other call runs a one-thread-per-element kernel.
+ * Conventions, errors, determinism and asynchrony are those of the GEMM entry
+ * points.
+ */
+int gemm_w4a16(int M, int N, int K, float alpha, const gemm_bf16_t* X, int ldx, const uint8_t* qk,
+               const gemm_bf16_t* scales, int lds, int group, int zero, float beta, gemm_bf16_t* C,
+               int ldc, cudaStream_t stream);
+int gemm_w4a16_f32out(int M, int N, int K, float alpha, const gemm_bf16_t* X, int ldx,
+                      const uint8_t* qk, const gemm_bf16_t* scales, int lds, int group, int zero,
+                      float beta, float* C, int ldc, cudaStream_t stream);
+
+/*
+ * The tiled INT4 layout of gemm_w4a16.  W is cut into tiles of 128 columns
+ * by 64 rows of K, 4 KB each, stored column tiles outer and K tiles inner.
+ * Inside a tile, column n has 32 bytes: eight little-endian 32-bit words, word j
+ * packing the codes of k = 8j + 0, 2, 4, 6, 1, 3, 5, 7 in its nibbles 0..7.
+ * Tiles and codes past N or K are 0.  gemm_w4_packed_bytes gives the size,
+ * ceil(N/128) * ceil(K/64) * 4096 bytes (0 for an empty weight).
+ * gemm_int4_repack writes it from the codes of gemm_int4_dequant (K x N,
+ * packed along n, ldq bytes per row) into qk (16-byte aligned DEVICE
+ * memory of that size).  Done once per weight.
+ */
+size_t gemm_w4_packed_bytes(int K, int N);
+int gemm_int4_repack(const uint8_t* q, int K, int N, int ldq, uint8_t* qk, cudaStream_t stream);
+
+/*
  * Message for the last non-OK return on the calling host thread ("" if none).
  * The string is owned by the library and valid until the next call on this
  * thread.
@@ -212,8 +252,10 @@ typedef enum {
   GEMM_PATH_F32_SIMT = 2, /* register-tiled FP32 kernel */
   GEMM_PATH_BF16_TC = 3,  /* tcgen05/TMEM/TMA warp-specialised kernel (bf16 or FP8 inputs) */
   GEMM_PATH_SKINNY = 4,   /* decode-shaped split-K kernel (bf16, M <= 16) */
-  GEMM_PATH_INT4 = 5      /* INT4 dequantisation, 32 codes per thread (reported only;
+  GEMM_PATH_INT4 = 5,     /* INT4 dequantisation, vector kernel (reported only;
                              the per-byte fallback reports GEMM_PATH_GENERIC) */
+  GEMM_PATH_W4 = 6        /* INT4-weight decode GEMM, tcgen05 kernel (reported only;
+                             its one-thread-per-element fallback reports GEMM_PATH_GENERIC) */
 } gemm_path;
 
 /*

@@ -82,3 +82,24 @@ def repack_kmajor(q_bytes, K: int, N: int) -> np.ndarray:
     for s, dk in enumerate(SLOT_K):
         out |= (padded[dk::8].T.astype(np.uint64) << np.uint64(4 * s))
     return out.astype("<u4").view(np.uint8).reshape(N, 4 * words)
+
+
+# Tiled K-packed layout: W is cut into tiles of TILE_N columns by TILE_K rows
+# of K, stored one after another (column tiles outer, K tiles inner), each
+# tile TILE_N x TILE_K/2 bytes with column n's codes for its TILE_K rows of K
+# as TILE_K/8 words in the SLOT_K order.  Tiles past N or K are zero-filled.
+TILE_N, TILE_K = 128, 64
+
+
+def tiled_bytes(K: int, N: int) -> int:
+    return -(-N // TILE_N) * -(-K // TILE_K) * TILE_N * TILE_K // 2
+
+
+def repack_tiled(q_bytes, K: int, N: int) -> np.ndarray:
+    """The tiled K-packed layout as a flat uint8 array of tiled_bytes(K, N)."""
+    tn, tk = -(-N // TILE_N), -(-K // TILE_K)
+    rows = repack_kmajor(q_bytes, K, N)                         # N x 4*ceil(K/8)
+    full = np.zeros((tn * TILE_N, tk * TILE_K // 2), dtype=np.uint8)
+    full[:N, : rows.shape[1]] = rows
+    tiles = full.reshape(tn, TILE_N, tk, TILE_K // 2).transpose(0, 2, 1, 3)
+    return np.ascontiguousarray(tiles).reshape(-1)

@@ -31,16 +31,17 @@ GEMM_ERR_UNSUPPORTED = 3
 GEMM_ERR_CUDA = 4
 GEMM_ERR_DEVICE_TIMEOUT = 5
 
-PATH_AUTO, PATH_GENERIC, PATH_F32_SIMT, PATH_BF16_TC, PATH_SKINNY, PATH_INT4 = range(6)
+PATH_AUTO, PATH_GENERIC, PATH_F32_SIMT, PATH_BF16_TC, PATH_SKINNY, PATH_INT4, PATH_W4 = range(7)
 ACT_NONE, ACT_RELU, ACT_SILU, ACT_GELU = range(4)
 FP8_E4M3, FP8_E5M2 = 0, 1
 PATH_NAMES = {PATH_AUTO: "none", PATH_GENERIC: "generic", PATH_F32_SIMT: "f32_simt",
-              PATH_BF16_TC: "bf16_tc", PATH_SKINNY: "skinny", PATH_INT4: "int4"}
+              PATH_BF16_TC: "bf16_tc", PATH_SKINNY: "skinny", PATH_INT4: "int4", PATH_W4: "w4"}
 
 # every symbol the public header declares
 EXPORTS = ("gemm_f32", "gemm_bf16", "gemm_bf16_f32out", "gemm_f32_ex", "gemm_bf16_ex",
            "gemm_bf16_f32out_ex", "gemm_bf16_swiglu", "gemm_fp8", "gemm_fp8_f32out",
-           "gemm_int4_dequant", "gemm_int4_dequant_f32", "gemm_get_last_error",
+           "gemm_int4_dequant", "gemm_int4_dequant_f32", "gemm_w4a16", "gemm_w4a16_f32out",
+           "gemm_int4_repack", "gemm_w4_packed_bytes", "gemm_get_last_error",
            "gemm_device_status", "gemm_force_path", "gemm_last_path", "gemm_force_tile_n",
            "gemm_last_tile_n", "gemm_force_tc_pair", "gemm_last_tc_pair", "gemm_force_split_tiles",
            "gemm_last_k_split", "gemm_set_wait_timeout_ns", "gemm_selftest_wait_timeout",
@@ -89,6 +90,14 @@ def load(path: str | None = None):
             fn = getattr(lib, name)
             fn.argtypes = [vp, i, i, i, vp, i, i, i, vp, i, vp]
             fn.restype = i
+        for name in ("gemm_w4a16", "gemm_w4a16_f32out"):
+            fn = getattr(lib, name)
+            fn.argtypes = [i, i, i, f, vp, i, vp, vp, i, i, i, f, vp, i, vp]
+            fn.restype = i
+        lib.gemm_int4_repack.argtypes = [vp, i, i, i, vp, vp]
+        lib.gemm_int4_repack.restype = i
+        lib.gemm_w4_packed_bytes.argtypes = [i, i]
+        lib.gemm_w4_packed_bytes.restype = ctypes.c_size_t
         for name in ("gemm_fp8", "gemm_fp8_f32out"):
             fn = getattr(lib, name)
             fn.argtypes = [i, i, i, f, vp, i, i, vp, i, i, f, vp, i, vp]
@@ -173,6 +182,24 @@ def gemm_int4_dequant(q, K, N, ldq, scales, lds, group, zero, W, ldw, stream=0):
 
 def gemm_int4_dequant_f32(q, K, N, ldq, scales, lds, group, zero, W, ldw, stream=0):
     _check(load().gemm_int4_dequant_f32(q, K, N, ldq, scales, lds, group, zero, W, ldw, stream))
+
+
+def gemm_w4a16(M, N, K, alpha, X, ldx, qk, scales, lds, group, zero, beta, C, ldc, stream=0):
+    _check(load().gemm_w4a16(M, N, K, alpha, X, ldx, qk, scales, lds, group, zero, beta, C, ldc,
+                             stream))
+
+
+def gemm_w4a16_f32out(M, N, K, alpha, X, ldx, qk, scales, lds, group, zero, beta, C, ldc, stream=0):
+    _check(load().gemm_w4a16_f32out(M, N, K, alpha, X, ldx, qk, scales, lds, group, zero, beta, C, ldc,
+                                    stream))
+
+
+def gemm_w4_packed_bytes(K, N) -> int:
+    return int(load().gemm_w4_packed_bytes(K, N))
+
+
+def gemm_int4_repack(q, K, N, ldq, qk, stream=0):
+    _check(load().gemm_int4_repack(q, K, N, ldq, qk, stream))
 
 
 def device_status(stream=0) -> tuple[int, int]:
@@ -330,3 +357,37 @@ def int4_dequant(q, scales, N: int, group: int, zero: int, W, stream=None):
     else:
         raise TypeError(f"unsupported output dtype {W.dtype}")
     return W
+
+
+
+def int4_repack(q, K: int, N: int, stream=None):
+    """Tiled copy (a new flat CUDA uint8 tensor of gemm_w4_packed_bytes(K, N))
+    of INT4 codes q (K x ceil(N/2) bytes, packed along n).  Argument
+    marshalling only."""
+    import torch
+    qk = torch.empty((max(gemm_w4_packed_bytes(K, N), 16),), dtype=torch.uint8, device=q.device)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
+    gemm_int4_repack(q.data_ptr(), K, N, _ld(q), qk.data_ptr(), s)
+    return qk
+
+
+def w4a16(X, qk, scales, group: int, zero: int, C, alpha: float = 1.0, beta: float = 0.0,
+          stream=None):
+    """C = alpha * X @ W + beta * C with W = scales[k // group] * (q - zero) given
+    as K-packed codes qk (from int4_repack); X bf16, C bf16 or fp32.  Argument
+    marshalling only."""
+    import torch
+    M, K = X.shape
+    N = C.shape[1]
+    if C.shape[0] != M or qk.numel() < gemm_w4_packed_bytes(K, N) or X.dtype != torch.bfloat16:
+        raise ValueError("w4a16(): shape or dtype mismatch")
+    s = stream if stream is not None else torch.cuda.current_stream(X.device).cuda_stream
+    args = (M, N, K, float(alpha), X.data_ptr(), _ld(X), qk.data_ptr(), scales.data_ptr(),
+            _ld(scales), int(group), int(zero), float(beta), C.data_ptr(), _ld(C), s)
+    if C.dtype == torch.bfloat16:
+        gemm_w4a16(*args)
+    elif C.dtype == torch.float32:
+        gemm_w4a16_f32out(*args)
+    else:
+        raise TypeError(f"unsupported output dtype {C.dtype}")
+    return C

@@ -347,6 +347,70 @@ int int4_dequant(const uint8_t* q, int K, int N, int ldq, const void* scales, in
   return GEMM_OK;
 }
 
+int int4_repack(const uint8_t* q, int K, int N, int ldq, uint8_t* qk, cudaStream_t stream) {
+  t_msg[0] = '\0';
+  t_last_path = GEMM_PATH_AUTO;
+  t_last_k_split = 1;
+  if (K < 0 || N < 0) return fail(GEMM_ERR_INVALID_ARG, "negative size K=%d N=%d", K, N);
+  const int bpr = (N + 1) / 2;
+  if (ldq < (bpr > 1 ? bpr : 1))
+    return fail(GEMM_ERR_INVALID_ARG, "leading dimension too small (ldq=%d, N=%d)", ldq, N);
+  if (K == 0 || N == 0) return GEMM_OK;
+  if (q == nullptr || qk == nullptr) return fail(GEMM_ERR_INVALID_ARG, "q or qk is NULL");
+  if (reinterpret_cast<uintptr_t>(qk) & 15u) return fail(GEMM_ERR_MISALIGNED, "qk is not 16-byte aligned");
+  DeviceInfo* dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc != GEMM_OK) return rc;
+  const int err = launch_int4_repack(q, ldq, qk, K, N, dev->num_sms, stream);
+  if (err != cudaSuccess)
+    return fail(GEMM_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString((cudaError_t)err));
+  return GEMM_OK;
+}
+
+int w4a16(int M, int N, int K, float alpha, const void* X, int ldx, const uint8_t* qk,
+          const void* scales, int lds, int group, int zero, float beta, void* C, int ldc, Elem out,
+          cudaStream_t stream) {
+  t_msg[0] = '\0';
+  t_last_path = GEMM_PATH_AUTO;
+  t_last_k_split = 1;
+  if (M < 0 || N < 0 || K < 0) return fail(GEMM_ERR_INVALID_ARG, "negative size M=%d N=%d K=%d", M, N, K);
+  if (group < 1) return fail(GEMM_ERR_INVALID_ARG, "group size %d < 1", group);
+  if (zero < 0 || zero > 15) return fail(GEMM_ERR_INVALID_ARG, "zero point %d outside 0..15", zero);
+  if (ldx < (K > 1 ? K : 1) || lds < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
+    return fail(GEMM_ERR_INVALID_ARG, "leading dimension too small (ldx=%d lds=%d ldc=%d)", ldx, lds, ldc);
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (C == nullptr) return fail(GEMM_ERR_INVALID_ARG, "C is NULL");
+  if (K > 0 && (X == nullptr || qk == nullptr || scales == nullptr))
+    return fail(GEMM_ERR_INVALID_ARG, "X, qk or scales is NULL");
+  const size_t out_sz = out == Elem::F32 ? 4 : 2;
+  if ((reinterpret_cast<uintptr_t>(X) & 1u) || (reinterpret_cast<uintptr_t>(scales) & 1u) ||
+      (reinterpret_cast<uintptr_t>(C) % out_sz))
+    return fail(GEMM_ERR_MISALIGNED, "X, scales or C is not aligned to its element size");
+  if (reinterpret_cast<uintptr_t>(qk) & 15u) return fail(GEMM_ERR_MISALIGNED, "qk is not 16-byte aligned");
+  DeviceInfo* dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc != GEMM_OK) return rc;
+  GemmArgs a{};
+  a.M = M; a.N = N; a.K = K; a.alpha = alpha; a.beta = beta;
+  a.A = X; a.lda = ldx; a.B = qk; a.ldb = 0; a.C = C; a.ldc = ldc;
+  a.in = Elem::BF16; a.out = out;
+  a.status = dev->status;
+  a.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  a.bias = nullptr; a.act = kActNone; a.B2 = nullptr; a.swiglu = 0; a.fmt_a = 0; a.fmt_b = 0;
+  const bool fast = w4_fast_ok(M, K, group) && aligned16(X) && ((size_t)ldx * 2) % 16 == 0 &&
+                    t_forced_path != GEMM_PATH_GENERIC;
+  const CUtensorMap* mX = nullptr;
+  if (fast && (rc = make_map(X, K, M, (uint64_t)ldx * 2, kSkBK, kSkMaxM, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                             CU_TENSOR_MAP_SWIZZLE_128B, &mX)) != GEMM_OK)
+    return rc;
+  const int err = launch_w4_decode(a, scales, lds, group, zero, mX, qk, fast, dev->num_sms, stream,
+                                   &t_last_k_split);
+  if (err != cudaSuccess)
+    return fail(GEMM_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString((cudaError_t)err));
+  t_last_path = fast ? GEMM_PATH_W4 : GEMM_PATH_GENERIC;
+  return GEMM_OK;
+}
+
 __global__ void selftest_wait_kernel(int* status, uint64_t timeout_ns) {
   __shared__ uint64_t bar;
   if (threadIdx.x == 0) {
@@ -415,6 +479,26 @@ int gemm_int4_dequant(const uint8_t* q, int K, int N, int ldq, const gemm_bf16_t
 int gemm_int4_dequant_f32(const uint8_t* q, int K, int N, int ldq, const gemm_bf16_t* scales,
                           int lds, int group, int zero, float* W, int ldw, cudaStream_t stream) {
   return g3::int4_dequant(q, K, N, ldq, scales, lds, group, zero, W, ldw, false, stream);
+}
+
+size_t gemm_w4_packed_bytes(int K, int N) { return g3::w4_packed_bytes(K, N); }
+
+int gemm_int4_repack(const uint8_t* q, int K, int N, int ldq, uint8_t* qk, cudaStream_t stream) {
+  return g3::int4_repack(q, K, N, ldq, qk, stream);
+}
+
+int gemm_w4a16(int M, int N, int K, float alpha, const gemm_bf16_t* X, int ldx, const uint8_t* qk,
+               const gemm_bf16_t* scales, int lds, int group, int zero, float beta, gemm_bf16_t* C,
+               int ldc, cudaStream_t stream) {
+  return g3::w4a16(M, N, K, alpha, X, ldx, qk, scales, lds, group, zero, beta, C, ldc, Elem::BF16,
+                   stream);
+}
+
+int gemm_w4a16_f32out(int M, int N, int K, float alpha, const gemm_bf16_t* X, int ldx,
+                      const uint8_t* qk, const gemm_bf16_t* scales, int lds, int group, int zero,
+                      float beta, float* C, int ldc, cudaStream_t stream) {
+  return g3::w4a16(M, N, K, alpha, X, ldx, qk, scales, lds, group, zero, beta, C, ldc, Elem::F32,
+                   stream);
 }
 
 int gemm_f32_ex(int M, int N, int K, float alpha, const float* A, int lda, const float* B, int ldb,

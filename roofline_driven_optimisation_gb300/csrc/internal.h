@@ -52,6 +52,10 @@ enum WaitSite : int {
   kSiteSkinnyMma = 31,
   kSiteSkinnyEpilogue = 32,
   kSiteSkinnyDrain = 33,
+  kSiteW4Producer = 40,
+  kSiteW4Mma = 41,
+  kSiteW4Epilogue = 42,
+  kSiteW4Drain = 43,
 };
 
 // Each launcher returns a cudaError_t (as int) from the launch.
@@ -104,6 +108,21 @@ constexpr int kSkMaxM = 16, kSkBN = 128, kSkBK = 64;
 int launch_int4_dequant(const uint8_t* q, int K, int N, int ldq, const void* scales, int lds,
                         int group, int zero, void* w, int ldw, bool out_bf16, int num_sms,
                         cudaStream_t st, int* vector_path);
+
+// INT4 weight-only decode GEMM (bf16 X, M <= 16; codes in the tiled layout
+// of 4 KB tiles, 128 columns x 64 rows of K): TMA tiles of X (64 k x 16 rows,
+// 128-byte swizzle), bulk copies of the code tiles.  fast = the tcgen05
+// kernel (w4_fast_ok and the alignment rules), else a one-thread-per-element
+// kernel.
+constexpr int kW4BN = 128, kW4BK = 64;
+bool w4_fast_ok(int M, int K, int group);
+size_t w4_packed_bytes(int K, int N);
+int launch_w4_decode(const GemmArgs& a, const void* scales, long long lds, int group, int zero,
+                     const CUtensorMap* mapX, const uint8_t* qk, bool fast, int num_sms,
+                     cudaStream_t s, int* k_split);
+// natural INT4 layout (packed along n) -> tiled layout (w4_packed_bytes)
+int launch_int4_repack(const uint8_t* q, long long ldq, uint8_t* qk, int K, int N, int num_sms,
+                       cudaStream_t s);
 
 int launch_selftest_wait(int* status, uint64_t timeout_ns, cudaStream_t s);
 

@@ -88,3 +88,22 @@ def test_exact_w4_gemm_differs_from_rounded_only_by_the_rounding():
     rounded = int4.gemm_w4(A, q, s, 8, 64, 8)
     scale = np.abs(A) @ np.abs(W)
     assert np.max(np.abs(rounded - exact) / scale.max()) <= 2.0 ** -9
+
+
+def test_tiled_layout_places_each_tile_contiguously():
+    rng = np.random.default_rng(12)
+    K, N = 130, 200                       # 3 K tiles (last partial), 2 column tiles
+    codes = rng.integers(0, 16, size=(K, N))
+    q = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    t = int4.repack_tiled(q, K, N)
+    assert t.size == int4.tiled_bytes(K, N) == 2 * 3 * 4096
+    rows = int4.repack_kmajor(q, K, N)    # N x 68
+    for n in (0, 127, 128, 199):
+        for kt in range(3):
+            blk = ((n // 128) * 3 + kt) * 4096 + (n % 128) * 32
+            want = np.zeros(32, dtype=np.uint8)
+            seg = rows[n, kt * 32:(kt + 1) * 32]
+            want[: seg.size] = seg
+            assert np.array_equal(t[blk:blk + 32], want)
+    # the padding columns of the last tile are zero
+    assert not t[(1 * 3 + 0) * 4096 + 72 * 32:(1 * 3 + 1) * 4096].any()
