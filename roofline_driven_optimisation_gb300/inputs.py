@@ -228,3 +228,22 @@ def make_int4(K: int, N: int, group: int = 128, zero: int = 8, seed: int = 8) ->
     groups = (K + group - 1) // group
     scales = (0.003 + 0.003 * torch.rand((groups, N), generator=gen)).to(torch.bfloat16)
     return Int4Case(pack_int4(codes), scales, N, group, zero)
+
+
+@dataclasses.dataclass
+class AttentionCase:
+    Q: torch.Tensor    # [B][Hq][Sq][D] bf16
+    K: torch.Tensor    # [B][Hkv][Sk][D] bf16
+    V: torch.Tensor    # [B][Hkv][Sk][D] bf16
+
+
+def make_attention(B: int = 1, Hq: int = 32, Hkv: int = 32, Sq: int = 2048, Sk: int = 2048,
+                   D: int = 128, seed: int = 9) -> AttentionCase:
+    """Attention operands, N(0, 1) rounded to bf16; the defaults are one
+    LLaMA-7B layer's prefill of a 2048-token context (32 heads of 128)."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    Q = torch.randn((B, Hq, Sq, D), generator=gen).to(torch.bfloat16)
+    K = torch.randn((B, Hkv, Sk, D), generator=gen).to(torch.bfloat16)
+    V = torch.randn((B, Hkv, Sk, D), generator=gen).to(torch.bfloat16)
+    return AttentionCase(Q, K, V)
