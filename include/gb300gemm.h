@@ -230,6 +230,27 @@ size_t gemm_w4_packed_bytes(int K, int N);
 int gemm_int4_repack(const uint8_t* q, int K, int N, int ldq, uint8_t* qk, cudaStream_t stream);
 
 /*
+ * Attention forward ("从模型计算到 GPU 执行：读懂算子、Kernel 与 GPU 性能", section
+ * 1.2: S = Q K^T, S = S / sqrt(d), P = softmax(S), O = P V), with S and P
+ * kept on chip ("Kernel 性能从何而来", section on attention):
+ *
+ *     O = softmax(Q K^T * scale) V,   per batch b and query head h
+ *
+ * Q and O are [B][Hq][Sq][D] and K, V are [B][Hkv][Sk][D], all contiguous bf16
+ * DEVICE tensors owned by the caller.  Hq must be a multiple of Hkv: query
+ * head h reads key/value head h / (Hq / Hkv).  scale == 0 means 1/sqrt(D).
+ * causal != 0 lets query i see key j only when j <= i + (Sk - Sq).  Masked
+ * scores are -inf, and a row with no visible key gives O = 0.  The softmax
+ * is in fp32 (running maximum and sum), P is rounded to bf16 for the second
+ * product, and O is rounded once to bf16.  The fast path (tcgen05) needs
+ * D = 64 or 128 and 16-byte-aligned tensors.  Other calls run a
+ * one-block-per-row kernel, for Sk up to about 58,000.  Errors and
+ * asynchrony are as for the GEMM entry points.
+ */
+int gemm_attention(int B, int Hq, int Hkv, int Sq, int Sk, int D, const gemm_bf16_t* Q, const gemm_bf16_t* K,
+                   const gemm_bf16_t* V, gemm_bf16_t* O, float scale, int causal, cudaStream_t stream);
+
+/*
  * Message for the last non-OK return on the calling host thread ("" if none).
  * The string is owned by the library and valid until the next call on this
  * thread.
@@ -254,8 +275,10 @@ typedef enum {
   GEMM_PATH_SKINNY = 4,   /* decode-shaped split-K kernel (bf16, M <= 16) */
   GEMM_PATH_INT4 = 5,     /* INT4 dequantisation, vector kernel (reported only;
                              the per-byte fallback reports GEMM_PATH_GENERIC) */
-  GEMM_PATH_W4 = 6        /* INT4-weight decode GEMM, tcgen05 kernel (reported only;
+  GEMM_PATH_W4 = 6,       /* INT4-weight decode GEMM, tcgen05 kernel (reported only;
                              its one-thread-per-element fallback reports GEMM_PATH_GENERIC) */
+  GEMM_PATH_ATTN = 7      /* attention, tcgen05 kernel (reported only; its
+                             one-block-per-row fallback reports GEMM_PATH_GENERIC) */
 } gemm_path;
 
 /*

@@ -31,17 +31,18 @@ GEMM_ERR_UNSUPPORTED = 3
 GEMM_ERR_CUDA = 4
 GEMM_ERR_DEVICE_TIMEOUT = 5
 
-PATH_AUTO, PATH_GENERIC, PATH_F32_SIMT, PATH_BF16_TC, PATH_SKINNY, PATH_INT4, PATH_W4 = range(7)
+PATH_AUTO, PATH_GENERIC, PATH_F32_SIMT, PATH_BF16_TC, PATH_SKINNY, PATH_INT4, PATH_W4, PATH_ATTN = range(8)
 ACT_NONE, ACT_RELU, ACT_SILU, ACT_GELU = range(4)
 FP8_E4M3, FP8_E5M2 = 0, 1
 PATH_NAMES = {PATH_AUTO: "none", PATH_GENERIC: "generic", PATH_F32_SIMT: "f32_simt",
-              PATH_BF16_TC: "bf16_tc", PATH_SKINNY: "skinny", PATH_INT4: "int4", PATH_W4: "w4"}
+              PATH_BF16_TC: "bf16_tc", PATH_SKINNY: "skinny", PATH_INT4: "int4", PATH_W4: "w4",
+              PATH_ATTN: "attention"}
 
 # every symbol the public header declares
 EXPORTS = ("gemm_f32", "gemm_bf16", "gemm_bf16_f32out", "gemm_f32_ex", "gemm_bf16_ex",
            "gemm_bf16_f32out_ex", "gemm_bf16_swiglu", "gemm_fp8", "gemm_fp8_f32out",
            "gemm_int4_dequant", "gemm_int4_dequant_f32", "gemm_w4a16", "gemm_w4a16_f32out",
-           "gemm_int4_repack", "gemm_w4_packed_bytes", "gemm_get_last_error",
+           "gemm_int4_repack", "gemm_w4_packed_bytes", "gemm_attention", "gemm_get_last_error",
            "gemm_device_status", "gemm_force_path", "gemm_last_path", "gemm_force_tile_n",
            "gemm_last_tile_n", "gemm_force_tc_pair", "gemm_last_tc_pair", "gemm_force_split_tiles",
            "gemm_last_k_split", "gemm_set_wait_timeout_ns", "gemm_selftest_wait_timeout",
@@ -96,6 +97,8 @@ def load(path: str | None = None):
             fn.restype = i
         lib.gemm_int4_repack.argtypes = [vp, i, i, i, vp, vp]
         lib.gemm_int4_repack.restype = i
+        lib.gemm_attention.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, f, i, vp]
+        lib.gemm_attention.restype = i
         lib.gemm_w4_packed_bytes.argtypes = [i, i]
         lib.gemm_w4_packed_bytes.restype = ctypes.c_size_t
         for name in ("gemm_fp8", "gemm_fp8_f32out"):
@@ -200,6 +203,10 @@ def gemm_w4_packed_bytes(K, N) -> int:
 
 def gemm_int4_repack(q, K, N, ldq, qk, stream=0):
     _check(load().gemm_int4_repack(q, K, N, ldq, qk, stream))
+
+
+def gemm_attention(B, Hq, Hkv, Sq, Sk, D, Q, K, V, O, scale=0.0, causal=0, stream=0):
+    _check(load().gemm_attention(B, Hq, Hkv, Sq, Sk, D, Q, K, V, O, scale, causal, stream))
 
 
 def device_status(stream=0) -> tuple[int, int]:
@@ -391,3 +398,21 @@ def w4a16(X, qk, scales, group: int, zero: int, C, alpha: float = 1.0, beta: flo
     else:
         raise TypeError(f"unsupported output dtype {C.dtype}")
     return C
+
+
+def attention(Q, K, V, O, scale: float = 0.0, causal: bool = False, stream=None):
+    """O = softmax(Q K^T * scale) V for contiguous bf16 CUDA tensors Q, O
+    [B][Hq][Sq][D] and K, V [B][Hkv][Sk][D] (scale 0: 1/sqrt(D)).  Argument
+    marshalling only."""
+    import torch
+    B, Hq, Sq, D = Q.shape
+    Hkv, Sk = K.shape[1], K.shape[2]
+    for t in (Q, K, V, O):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise TypeError("attention() takes contiguous bf16 CUDA tensors")
+    if tuple(V.shape) != tuple(K.shape) or tuple(O.shape) != tuple(Q.shape) or K.shape[0] != B or K.shape[3] != D:
+        raise ValueError("attention(): shape mismatch")
+    s = stream if stream is not None else torch.cuda.current_stream(Q.device).cuda_stream
+    gemm_attention(B, Hq, Hkv, Sq, Sk, D, Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(),
+                   float(scale), int(bool(causal)), s)
+    return O

@@ -13,6 +13,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -113,10 +114,11 @@ struct MapKey {
   uintptr_t ptr;
   uint64_t cols, rows, ld_bytes;
   uint32_t box_cols, box_rows, dtype, swizzle;
+  uint64_t depth = 1, ld2_bytes = 0;   // 3-D maps: the third extent and its stride
   bool operator==(const MapKey& o) const {
     return ptr == o.ptr && cols == o.cols && rows == o.rows && ld_bytes == o.ld_bytes &&
            box_cols == o.box_cols && box_rows == o.box_rows && dtype == o.dtype &&
-           swizzle == o.swizzle;
+           swizzle == o.swizzle && depth == o.depth && ld2_bytes == o.ld2_bytes;
   }
 };
 struct MapKeyHash {
@@ -126,6 +128,7 @@ struct MapKeyHash {
     h ^= (k.rows + 0x7F4Au) * 0x165667B19E3779F9ull + (h << 6) + (h >> 2);
     h ^= (k.ld_bytes ^ ((uint64_t)k.box_cols << 32) ^ ((uint64_t)k.box_rows << 48) ^
           ((uint64_t)k.dtype << 8) ^ k.swizzle) * 0x27D4EB2F165667C5ull;
+    h ^= (k.depth * 0x9E3779B97F4A7C15ull) ^ (k.ld2_bytes * 0xC2B2AE3D27D4EB4Full);
     return (size_t)h;
   }
 };
@@ -157,6 +160,36 @@ int make_map(const void* ptr, uint64_t cols, uint64_t rows, uint64_t ld_bytes, u
   if (r != CUDA_SUCCESS)
     return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for %llux%llu ld=%llu", (int)r,
                 (unsigned long long)rows, (unsigned long long)cols, (unsigned long long)ld_bytes);
+  auto ins = t_maps.emplace(key, map);
+  *out = &ins.first->second;
+  return GEMM_OK;
+}
+
+// A 3-D tiled map: cols x rows x depth with row stride ld_bytes and depth
+// stride ld2_bytes; boxes of box_cols x box_rows x 1.
+int make_map_3d(const void* ptr, uint64_t cols, uint64_t rows, uint64_t depth, uint64_t ld_bytes,
+                uint64_t ld2_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapDataType dtype,
+                CUtensorMapSwizzle swizzle, const CUtensorMap** out) {
+  MapKey key{reinterpret_cast<uintptr_t>(ptr), cols, rows, ld_bytes, box_cols, box_rows,
+             (uint32_t)dtype, (uint32_t)swizzle, depth, ld2_bytes};
+  auto it = t_maps.find(key);
+  if (it != t_maps.end()) {
+    *out = &it->second;
+    return GEMM_OK;
+  }
+  EncodeFn fn = encode_fn();
+  if (!fn) return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  if (t_maps.size() > 1024) t_maps.clear();
+  CUtensorMap map;
+  const cuuint64_t dims[3] = {cols, rows, depth};
+  const cuuint64_t strides[2] = {ld_bytes, ld2_bytes};
+  const cuuint32_t box[3] = {box_cols, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(&map, dtype, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled (3-D) failed (%d)", (int)r);
   auto ins = t_maps.emplace(key, map);
   *out = &ins.first->second;
   return GEMM_OK;
@@ -411,6 +444,53 @@ int w4a16(int M, int N, int K, float alpha, const void* X, int ldx, const uint8_
   return GEMM_OK;
 }
 
+int attention(int B, int Hq, int Hkv, int Sq, int Sk, int D, const void* Q, const void* K, const void* V,
+              void* O, float scale, int causal, cudaStream_t stream) {
+  t_msg[0] = '\0';
+  t_last_path = GEMM_PATH_AUTO;
+  t_last_k_split = 1;
+  if (B < 0 || Hq < 0 || Hkv < 0 || Sq < 0 || Sk < 0 || D < 1)
+    return fail(GEMM_ERR_INVALID_ARG, "bad sizes B=%d Hq=%d Hkv=%d Sq=%d Sk=%d D=%d", B, Hq, Hkv, Sq, Sk, D);
+  if (Hq > 0 && (Hkv < 1 || Hq % Hkv != 0))
+    return fail(GEMM_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
+  if (!(scale >= 0.f) || !std::isfinite(scale)) return fail(GEMM_ERR_INVALID_ARG, "bad scale");
+  if (B == 0 || Hq == 0 || Sq == 0) return GEMM_OK;
+  if (Q == nullptr || O == nullptr || (Sk > 0 && (K == nullptr || V == nullptr)))
+    return fail(GEMM_ERR_INVALID_ARG, "Q, K, V or O is NULL");
+  if ((reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) | reinterpret_cast<uintptr_t>(V) |
+       reinterpret_cast<uintptr_t>(O)) & 1u)
+    return fail(GEMM_ERR_MISALIGNED, "a tensor is not aligned to 2 bytes");
+  if (((size_t)Sk + 32) * 4 > 227 * 1024 && !(D == 64 || D == 128))
+    return fail(GEMM_ERR_UNSUPPORTED, "Sk %d too long for the generic attention kernel", Sk);
+  if (scale == 0.f) scale = 1.f / std::sqrt((float)D);
+  DeviceInfo* dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc != GEMM_OK) return rc;
+  const bool fast = (D == 64 || D == 128) && Sk > 0 && aligned16(Q) && aligned16(K) && aligned16(V) &&
+                    aligned16(O) && t_forced_path != GEMM_PATH_GENERIC;
+  if (!fast && ((size_t)Sk + 32) * 4 > 227 * 1024)
+    return fail(GEMM_ERR_UNSUPPORTED, "Sk %d too long for the generic attention kernel", Sk);
+  const CUtensorMap *mQ = nullptr, *mK = nullptr, *mV = nullptr;
+  if (fast) {
+    const uint64_t row = (uint64_t)D * 2;
+    if ((rc = make_map_3d(Q, D, Sq, (uint64_t)B * Hq, row, row * Sq, 64, 128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          CU_TENSOR_MAP_SWIZZLE_128B, &mQ)) != GEMM_OK)
+      return rc;
+    if ((rc = make_map_3d(K, D, Sk, (uint64_t)B * Hkv, row, row * Sk, 64, 64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          CU_TENSOR_MAP_SWIZZLE_128B, &mK)) != GEMM_OK)
+      return rc;
+    if ((rc = make_map_3d(V, D, Sk, (uint64_t)B * Hkv, row, row * Sk, 64, 64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          CU_TENSOR_MAP_SWIZZLE_128B, &mV)) != GEMM_OK)
+      return rc;
+  }
+  const int err = launch_attention(B, Hq, Hkv, Sq, Sk, D, Q, K, V, O, scale, causal ? 1 : 0, mQ, mK, mV, fast,
+                                   dev->status, g_timeout_ns.load(std::memory_order_relaxed), stream);
+  if (err != cudaSuccess)
+    return fail(GEMM_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString((cudaError_t)err));
+  t_last_path = fast ? GEMM_PATH_ATTN : GEMM_PATH_GENERIC;
+  return GEMM_OK;
+}
+
 __global__ void selftest_wait_kernel(int* status, uint64_t timeout_ns) {
   __shared__ uint64_t bar;
   if (threadIdx.x == 0) {
@@ -479,6 +559,11 @@ int gemm_int4_dequant(const uint8_t* q, int K, int N, int ldq, const gemm_bf16_t
 int gemm_int4_dequant_f32(const uint8_t* q, int K, int N, int ldq, const gemm_bf16_t* scales,
                           int lds, int group, int zero, float* W, int ldw, cudaStream_t stream) {
   return g3::int4_dequant(q, K, N, ldq, scales, lds, group, zero, W, ldw, false, stream);
+}
+
+int gemm_attention(int B, int Hq, int Hkv, int Sq, int Sk, int D, const gemm_bf16_t* Q, const gemm_bf16_t* K,
+                   const gemm_bf16_t* V, gemm_bf16_t* O, float scale, int causal, cudaStream_t stream) {
+  return g3::attention(B, Hq, Hkv, Sq, Sk, D, Q, K, V, O, scale, causal, stream);
 }
 
 size_t gemm_w4_packed_bytes(int K, int N) { return g3::w4_packed_bytes(K, N); }

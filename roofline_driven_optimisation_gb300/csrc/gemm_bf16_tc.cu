@@ -228,7 +228,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
       int m0, n0;
       tile_coords<BN>(tile, p, m0, n0);
-      if (!mbar_wait(tfull_bar(acc), acc_phase, a.timeout_ns, abort_flag)) {
+      // warp-uniform (the tcgen05.ld below is warp-wide)
+      if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), acc_phase, a.timeout_ns, abort_flag))) {
         if (!*abort_flag) report_status(a.status, 5, kSiteTcEpilogue);
         *abort_flag = 1;
         break;

@@ -301,7 +301,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int i = 0; i < n_items; ++i) {
       int m0, n0, bn;
       item(i, m0, n0, bn);
-      if (!mbar_wait(tfull_bar(acc), acc_phase, a.timeout_ns, abort_flag)) {
+      // warp-uniform (the tcgen05.ld below is warp-wide)
+      if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), acc_phase, a.timeout_ns, abort_flag))) {
         if (!*abort_flag) report_status(a.status, 5, kSiteTc2Epilogue);
         *abort_flag = 1;
         break;

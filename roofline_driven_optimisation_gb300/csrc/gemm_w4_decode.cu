@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     Ring rr;
     uint32_t s_cur = dg == 0 ? scale_raw(0) : 0u;
     auto consume_next = [&]() -> bool {
-      if (!mbar_wait(acc_full(rr.slot), rr.phase, a.timeout_ns, abort_flag)) {
+      if (!__all_sync(0xffffffffu, mbar_wait(acc_full(rr.slot), rr.phase, a.timeout_ns, abort_flag))) {
         if (!*abort_flag) report_status(a.status, 5, kSiteW4Epilogue);
         *abort_flag = 1;
         return false;
@@ -331,9 +331,12 @@ __global__ void __launch_bounds__(THREADS, 2)
       rs.advance(SSTAGES);
       ra.advance(ASTAGES);
     }
+    // wait results are made warp-uniform (__all_sync): a warp never splits
+    // between leaving the loop and the warp-wide tcgen05/__syncwarp below
     for (int i = dg; ok && i < my_stages; i += DQ_GROUPS) {
-      if (!mbar_wait(code_full(rs.slot), rs.phase, a.timeout_ns, abort_flag) ||
-          !mbar_wait(a_empty(ra.slot), ra.phase ^ 1u, a.timeout_ns, abort_flag)) {
+      const bool got = mbar_wait(code_full(rs.slot), rs.phase, a.timeout_ns, abort_flag) &&
+                       mbar_wait(a_empty(ra.slot), ra.phase ^ 1u, a.timeout_ns, abort_flag);
+      if (!__all_sync(0xffffffffu, got)) {
         if (!*abort_flag) report_status(a.status, 5, kSiteW4Epilogue);
         *abort_flag = 1;
         ok = false;

@@ -56,6 +56,10 @@ enum WaitSite : int {
   kSiteW4Mma = 41,
   kSiteW4Epilogue = 42,
   kSiteW4Drain = 43,
+  kSiteAttnProducer = 50,
+  kSiteAttnMma = 51,
+  kSiteAttnSoftmax = 52,
+  kSiteAttnDrain = 53,
 };
 
 // Each launcher returns a cudaError_t (as int) from the launch.
@@ -123,6 +127,15 @@ int launch_w4_decode(const GemmArgs& a, const void* scales, long long lds, int g
 // natural INT4 layout (packed along n) -> tiled layout (w4_packed_bytes)
 int launch_int4_repack(const uint8_t* q, long long ldq, uint8_t* qk, int K, int N, int num_sms,
                        cudaStream_t s);
+
+// Attention O = softmax(Q K^T * scale) V, [B][H][S][D] bf16 (K/V with Hkv
+// heads).  fast = the tcgen05 kernel (D 64 or 128, 16-byte-aligned tensors;
+// 3-D maps of Q with boxes 64 d x 128 rows and of K, V with 64 d x 64 keys),
+// else a one-block-per-row kernel.
+int launch_attention(int B, int Hq, int Hkv, int Sq, int Sk, int D, const void* Q, const void* K,
+                     const void* V, void* O, float scale, int causal, const CUtensorMap* mQ,
+                     const CUtensorMap* mK, const CUtensorMap* mV, bool fast, int* status,
+                     uint64_t timeout_ns, cudaStream_t s);
 
 int launch_selftest_wait(int* status, uint64_t timeout_ns, cudaStream_t s);
 
