@@ -327,6 +327,7 @@ def run_ours(args):
     fp8 = measure_fp8(g, torch, dev, pk["bf16_tflops"]) if rank == 0 else None
     int4_dq = measure_int4_dequant(g, torch, dev, hbm) if rank == 0 else None
     w4 = measure_w4_decode(g, torch, dev, hbm) if rank == 0 else None
+    attn = measure_attention(g, torch, dev, pk["bf16_tflops"]) if rank == 0 else None
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -345,6 +346,7 @@ def run_ours(args):
         "fp8_gemm": fp8,
         "int4_dequant": int4_dq,
         "w4a16_decode": w4,
+        "attention": attn,
         "e2e": e2e,
         "gpu_launches": len(parts) * args.steps,
         "clocks": clocks.summary(),
@@ -531,6 +533,40 @@ def measure_w4_decode(g, torch, dev, hbm, iters=20):
     return {"launches": len(calls), "ms": round(ms, 5), "bytes": int(by),
             "gbs": round(by / (ms * 1e-3) / 1e9, 1), "frac_hbm": round(by / (ms * 1e-3) / hbm, 4),
             "flops": int(sum(2 * m * N * K for m, N, K, *_ in calls))}
+
+
+def measure_attention(g, torch, dev, bf16_peak_tflops, reps=7):
+    """Attention forward: one LLaMA-7B layer's prefill (32 heads of 128, 2048
+    tokens, causal) and a 4096-token non-causal case.  FLOPs = 4 * D * (the
+    query-key pairs a query sees), i.e. both products; against the measured
+    bf16 peak.  Events around each call, median of `reps`.  Not part of the
+    step."""
+    from roofline_driven_optimisation_gb300 import inputs
+    stream = torch.cuda.current_stream(dev)
+    out = {"peak_tflops": round(bf16_peak_tflops, 1)}
+    for name, S, causal in (("llama7b_prefill_2048_causal", 2048, True), ("s4096_noncausal", 4096, False)):
+        c = inputs.make_attention(B=1, Hq=32, Hkv=32, Sq=S, Sk=S, D=128, seed=9)
+        Q, K, V = c.Q.to(dev), c.K.to(dev), c.V.to(dev)
+        O = torch.empty_like(Q)
+        g.attention(Q, K, V, O, causal=causal)
+        evs = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.attention(Q, K, V, O, causal=causal)
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+        pairs = S * (S + 1) // 2 if causal else S * S
+        flops = 4 * 32 * 128 * pairs
+        tf = flops / (ms * 1e-3) / 1e12
+        out[name] = {"ms": round(ms, 4), "tflops": round(tf, 1), "frac": round(tf / bf16_peak_tflops, 4)}
+        del Q, K, V, O
+    status, where = g.device_status(stream.cuda_stream)
+    if status != 0:
+        raise RuntimeError(f"device status {status} at {where} in the attention measurement")
+    return out
 
 
 def measure_fused_ffn(g, torch, dev, s, hbm, bf16_peak, reps=7):
