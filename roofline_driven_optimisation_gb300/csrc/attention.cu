@@ -8,16 +8,23 @@
 // Here a CTA owns 128 query rows of one head and walks the keys in tiles of
 // 64, keeping S, P and O on chip and the softmax online (running row maximum
 // m and sum l, O rescaled by exp(m_old - m_new) when the maximum moves):
-//   * warp 0 streams Q once and the K/V tiles by TMA (K two tiles ahead, V
-//     one), warp 1 issues the tcgen05 MMAs, warps 2-5 are the softmax, one
-//     thread per query row;
+//   * warp 0 streams Q once and the K/V tiles by TMA (two tiles ahead each),
+//     warp 1 issues the tcgen05 MMAs, warps 2-5 are the softmax, one thread
+//     per query row;
 //   * S_j = Q K_j^T goes into one of two TMEM buffers (M = 128, N = 64), so
 //     the MMA of tile j+1 runs while the softmax works on tile j;
 //   * the softmax reads its row of S_j from TMEM, updates m and l in fp32,
-//     writes P_j as bf16 into shared memory in the 128-byte-swizzled layout
-//     the next MMA reads, and rescales its row of O in TMEM;
-//   * O += P_j V_j accumulates in TMEM (M = 128, N = d); after the last tile
-//     each row is divided by l and written as bf16.
+//     writes P_j as bf16 back over the first half of the same TMEM buffer
+//     (the P V MMA reads its A operand from tensor memory, so P never
+//     passes through shared memory), and rescales its row of O in TMEM.  The reference
+//     maximum m of a row moves only when a tile's maximum exceeds it by more
+//     than TAU (log2 units): p = 2^(x - m) then stays below 2^TAU, O and l
+//     share the reference, so O / l is unchanged, and the TMEM rescale of O
+//     (a load, multiply and store of the whole row) becomes rare;
+//   * O += P_j V_j accumulates in TMEM (M = 128, N = d); a warp whose rows
+//     need no rescale releases P_j before the previous P V has finished, so
+//     the P V MMAs run back to back; after the last tile each row is divided
+//     by l and written as bf16.
 // Masked scores (causal, or keys past Sk) are -inf before the softmax.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -34,10 +41,12 @@ namespace {
 constexpr int BM = 128;        // query rows per CTA
 constexpr int BNK = 64;        // keys per tile
 constexpr int KSTAGES = 2;     // K tiles in flight
+constexpr int VSTAGES = 2;     // V tiles in flight
 constexpr int THREADS = 192;   // producer, MMA, four softmax warps
 constexpr int TMEM_COLS = 256; // two S buffers (2 x 64) + O (up to 128)
 constexpr int S_COLS = BNK;
 constexpr int O_COL0 = 2 * S_COLS;
+constexpr float TAU = 8.f;     // lazy rescale threshold (p <= 2^TAU = 256)
 
 template <int D>
 struct AttnCfg {
@@ -45,8 +54,7 @@ struct AttnCfg {
   static constexpr int BOXES = D / 64;                         // 64-column (128-byte) boxes of d
   static constexpr int Q_BYTES = BM * D * 2;                   // 16 / 32 KB
   static constexpr int KV_TILE_BYTES = BNK * D * 2;            // 8 / 16 KB
-  static constexpr int P_BYTES = BM * BNK * 2;                 // 16 KB
-  static constexpr int SMEM_DATA = Q_BYTES + (KSTAGES + 1) * KV_TILE_BYTES + P_BYTES;
+  static constexpr int SMEM_DATA = Q_BYTES + (KSTAGES + VSTAGES) * KV_TILE_BYTES;
   static constexpr int BAR_BYTES = 256;
   // padded so that at most two CTAs share an SM (their 2 x 256 tensor-memory
   // columns are then always free at allocation)
@@ -80,23 +88,27 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* base_ptr = smem_raw + (base - raw);
   const uint32_t q_tile = base;
   auto k_tile = [&](int s) { return base + Cfg::Q_BYTES + s * Cfg::KV_TILE_BYTES; };
-  const uint32_t v_tile = base + Cfg::Q_BYTES + KSTAGES * Cfg::KV_TILE_BYTES;
-  const uint32_t p_tile = v_tile + Cfg::KV_TILE_BYTES;
-  uint8_t* p_ptr = base_ptr + (p_tile - base);
+  auto v_tile = [&](int s) { return base + Cfg::Q_BYTES + (KSTAGES + s) * Cfg::KV_TILE_BYTES; };
   const uint32_t bar_base = base + Cfg::SMEM_DATA;
   uint8_t* bar_ptr = base_ptr + Cfg::SMEM_DATA;
   // barriers
   const uint32_t q_full = bar_base;
   auto k_full = [&](int s) { return bar_base + 8u * (1 + s); };
   auto k_empty = [&](int s) { return bar_base + 8u * (1 + KSTAGES + s); };
-  const uint32_t v_full = bar_base + 8u * (1 + 2 * KSTAGES);
-  const uint32_t v_empty = bar_base + 8u * (2 + 2 * KSTAGES);
-  auto s_full = [&](int b) { return bar_base + 8u * (3 + 2 * KSTAGES + b); };
-  auto s_empty = [&](int b) { return bar_base + 8u * (5 + 2 * KSTAGES + b); };
-  const uint32_t p_full = bar_base + 8u * (7 + 2 * KSTAGES);
-  const uint32_t o_done = bar_base + 8u * (8 + 2 * KSTAGES);
-  const uint32_t drain_bar = bar_base + 8u * (9 + 2 * KSTAGES);
-  constexpr int NBARS = 10 + 2 * KSTAGES;
+  constexpr int B0 = 1 + 2 * KSTAGES;
+  auto v_full = [&](int s) { return bar_base + 8u * (B0 + s); };
+  auto v_empty = [&](int s) { return bar_base + 8u * (B0 + VSTAGES + s); };
+  constexpr int B1 = B0 + 2 * VSTAGES;
+  auto s_full = [&](int b) { return bar_base + 8u * (B1 + b); };
+  auto s_empty = [&](int b) { return bar_base + 8u * (B1 + 2 + b); };
+  const uint32_t p_full = bar_base + 8u * (B1 + 4);
+  // P V of tile j completes on o_done(j % 2): a warp waits every phase of
+  // each, in order, and the next phase of the same barrier (tile j + 2)
+  // cannot start before that warp has released P of tile j + 1, so a waiter
+  // is never two phases behind
+  auto o_done = [&](int b) { return bar_base + 8u * (B1 + 5 + b); };
+  const uint32_t drain_bar = bar_base + 8u * (B1 + 7);
+  constexpr int NBARS = B1 + 8;
   static_assert(NBARS * 8 + 16 <= AttnCfg<64>::BAR_BYTES, "barrier area");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_ptr + 8 * NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_ptr + 8 * NBARS + 8);
@@ -115,14 +127,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(k_full(s), 1);
       mbar_init(k_empty(s), 1);
     }
-    mbar_init(v_full, 1);
-    mbar_init(v_empty, 1);
+    for (int s = 0; s < VSTAGES; ++s) {
+      mbar_init(v_full(s), 1);
+      mbar_init(v_empty(s), 1);
+    }
     for (int b = 0; b < 2; ++b) {
       mbar_init(s_full(b), 1);
       mbar_init(s_empty(b), 4);
+      mbar_init(o_done(b), 1);
     }
     mbar_init(p_full, 4);
-    mbar_init(o_done, 1);
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -142,7 +156,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producers
-    // lane 0: Q and the K tiles (two ahead); lane 1: the V tiles (one ahead)
+    // lane 0: Q and the K tiles, lane 1: the V tiles (two ahead each)
     if (lane == 0 && n_tiles > 0) {
       tma_prefetch_desc(&mapQ);
       tma_prefetch_desc(&mapK);
@@ -162,13 +176,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (lane == 1 && n_tiles > 0) {
       tma_prefetch_desc(&mapV);
       for (int j = 0; j < n_tiles; ++j) {
-        if (!mbar_wait(v_empty, ((uint32_t)j & 1u) ^ 1u, p.timeout_ns, abort_flag)) {
+        const int s = j % VSTAGES;
+        if (!mbar_wait(v_empty(s), (((uint32_t)(j / VSTAGES)) & 1u) ^ 1u, p.timeout_ns, abort_flag)) {
           fail_wait(kSiteAttnProducer);
           break;
         }
-        mbar_arrive_expect_tx(v_full, Cfg::KV_TILE_BYTES);
+        mbar_arrive_expect_tx(v_full(s), Cfg::KV_TILE_BYTES);
         for (int b = 0; b < Cfg::BOXES; ++b)
-          tma_load_3d(v_tile + b * (BNK * 128), &mapV, v_full, b * 64, j * BNK, kvh);
+          tma_load_3d(v_tile(s) + b * (BNK * 128), &mapV, v_full(s), b * 64, j * BNK, kvh);
       }
     }
     __syncwarp();
@@ -183,7 +198,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     if (elect_one_sync() && n_tiles > 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BNK, 0, 0);   // Q K-major, K K-major
-      constexpr uint32_t idesc_o = idesc_bf16_f32(BM, D, 0, 1);     // P K-major, V N-major
+      constexpr uint32_t idesc_o = idesc_bf16_f32(BM, D, 0, 1);     // P in TMEM, V N-major
       bool ok = mbar_wait(q_full, 0, p.timeout_ns, abort_flag);
       bool issued_any = false;
       // S_j = Q K_j^T
@@ -191,6 +206,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int s = j % KSTAGES, b = j & 1;
         if (!mbar_wait(k_full(s), ((uint32_t)(j / KSTAGES)) & 1u, p.timeout_ns, abort_flag)) return false;
         if (j >= 2 && !mbar_wait(s_empty(b), (((uint32_t)(j / 2)) & 1u) ^ 1u, p.timeout_ns, abort_flag))
+          return false;
+        // S_j overwrites P_{j-2}, which P V of tile j-2 reads from tensor
+        // memory; MMAs of different shapes are not ordered among themselves,
+        // so that P V must have completed
+        if (j >= 2 && !mbar_wait(o_done(b), (((uint32_t)(j / 2)) & 1u) ^ 1u, p.timeout_ns, abort_flag))
           return false;
         tc_fence_after();
 #pragma unroll
@@ -206,18 +226,20 @@ __global__ void __launch_bounds__(THREADS, 1)
       };
       // O += P_j V_j
       auto issue_pv = [&](int j) -> bool {
+        const int s = j % VSTAGES, b = j & 1;
         if (!mbar_wait(p_full, (uint32_t)j & 1u, p.timeout_ns, abort_flag)) return false;
-        if (!mbar_wait(v_full, (uint32_t)j & 1u, p.timeout_ns, abort_flag)) return false;
+        if (!mbar_wait(v_full(s), ((uint32_t)(j / VSTAGES)) & 1u, p.timeout_ns, abort_flag)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BNK / 16; ++kk) {
-          const uint64_t adesc = smem_desc_sw128(p_tile + kk * 32, 16, 1024);
-          const uint64_t bdesc = smem_desc_sw128(v_tile + kk * (16 * 128), BNK * 128, 1024);
-          tc_mma_f16(tmem_base + (uint32_t)O_COL0, adesc, bdesc, idesc_o, (j | kk) != 0 ? 1u : 0u);
+          // A = P_j: TMEM lanes = rows, columns b*64 + kk*8 .. +7 = keys 16kk .. 16kk+15
+          const uint32_t a_tmem = tmem_base + (uint32_t)(b * S_COLS + kk * 8);
+          const uint64_t bdesc = smem_desc_sw128(v_tile(s) + kk * (16 * 128), BNK * 128, 1024);
+          tc_mma_f16_tmem_a(tmem_base + (uint32_t)O_COL0, a_tmem, bdesc, idesc_o, (j | kk) != 0 ? 1u : 0u);
         }
         issued_any = true;
-        tc_commit(v_empty);
-        tc_commit(o_done);
+        tc_commit(v_empty(s));
+        tc_commit(o_done(b));
         return true;
       };
       if (ok) ok = issue_s(0);
@@ -260,20 +282,30 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_empty(b));
-      // masked, scaled scores (log2 domain) and the new running maximum
+      // scaled scores (log2 domain), masked only on tiles that need it
       float x[64];
       float mt = -INFINITY;
       const int k0 = j * BNK;
+      if (k0 + BNK - 1 <= min(vis_last, p.Sk - 1)) {
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const int kj = k0 + c;
-        const bool vis = kj < p.Sk && kj <= vis_last;
-        x[c] = vis ? __uint_as_float(c < 32 ? sa[c] : sb[c - 32]) * p.scale_log2 : -INFINITY;
-        mt = fmaxf(mt, x[c]);
+        for (int c = 0; c < 64; ++c) {
+          x[c] = __uint_as_float(c < 32 ? sa[c] : sb[c - 32]) * p.scale_log2;
+          mt = fmaxf(mt, x[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const int kj = k0 + c;
+          const bool vis = kj < p.Sk && kj <= vis_last;
+          x[c] = vis ? __uint_as_float(c < 32 ? sa[c] : sb[c - 32]) * p.scale_log2 : -INFINITY;
+          mt = fmaxf(mt, x[c]);
+        }
       }
-      const float m_new = fmaxf(m, mt);
+      // move the reference maximum only when this tile exceeds it by > TAU
+      const bool move = mt > m + TAU;       // also the first visible tile (m = -inf)
+      const float m_new = move ? mt : m;
       const float m_use = m_new == -INFINITY ? 0.f : m_new;   // no visible key yet
-      const float alpha = exp2f(m - m_use);                   // 0 on the first visible tile
+      const float alpha = move ? exp2f(m - m_use) : 1.f;     // 0 on the first visible tile
       float psum = 0.f;
       uint32_t pw[32];
 #pragma unroll
@@ -284,24 +316,25 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       l = l * alpha + psum;
       m = m_new;
-      // O and the P buffer are free once the previous P V has completed
-      if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(o_done, ((uint32_t)(j - 1)) & 1u, p.timeout_ns, abort_flag))) {
+      // P_j over the first 32 columns of its S buffer (two keys per column)
+      tmem_st_32x32b_x32(lane_base + (uint32_t)(b * S_COLS), pw);
+      tc_wait_st();
+      // O is touched only to rescale it; the warp decides together
+      const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
+      if (!rescale) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
+      }
+      // every P V phase is observed in order (see o_done)
+      if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(o_done((j - 1) & 1), ((uint32_t)((j - 1) / 2)) & 1u,
+                                                      p.timeout_ns, abort_flag))) {
         fail_wait(kSiteAttnSoftmax);
         ok = false;
         break;
       }
-      tc_fence_after();
-      // P row r: 128 bytes, 16-byte chunk c at position c ^ (r % 8)
-      uint8_t* prow = p_ptr + r * 128;
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) * 16)) =
-            make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
-      fence_proxy_async_smem();
-      // rescale O when the maximum of any row of this warp moved (not before
-      // the first P V).  tcgen05.ld/st are warp-wide (.sync.aligned): the
-      // decision is the warp's, and rows whose maximum stayed multiply by 1.
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      if (rescale) {
+        tc_fence_after();
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t o[32];
@@ -312,14 +345,15 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_st_32x32b_x32(lane_base + (uint32_t)(O_COL0 + c0), o);
         }
         tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
     }
     // ------------------------------------------------------------ epilogue
     if (ok && n_tiles > 0) {
-      if (!__all_sync(0xffffffffu, mbar_wait(o_done, ((uint32_t)(n_tiles - 1)) & 1u, p.timeout_ns, abort_flag))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(o_done((n_tiles - 1) & 1), ((uint32_t)((n_tiles - 1) / 2)) & 1u,
+                                             p.timeout_ns, abort_flag))) {
         fail_wait(kSiteAttnSoftmax);
         ok = false;
       }
