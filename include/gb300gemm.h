@@ -179,10 +179,12 @@ int gemm_fp8_f32out(int M, int N, int K, float alpha, const uint8_t* A, int fmt_
  * zero is one integer in 0..15, and group >= 1.  W is K x N (ldw >= N),
  * written as bf16 by gemm_int4_dequant (the exact fp32 value rounded once,
  * nearest even) or as fp32 by gemm_int4_dequant_f32 (exact).  All pointers
- * are DEVICE pointers owned by the caller.  The fast kernel needs N a
- * multiple of 32 and 16-byte-aligned rows of q, scales and W.  Other shapes
- * run a per-byte kernel with the same results.  Errors and asynchrony are
- * as for the GEMM entry points.
+ * are DEVICE pointers owned by the caller.  The fastest kernel (a thread
+ * per 4, 8 or 16 rows of 8 or 4 columns) needs N a multiple of 8, K and
+ * group both multiples of 4, 4-byte-aligned rows of q and 16-byte-aligned
+ * rows of scales and W; the next needs N a multiple of 32 and 16-byte-
+ * aligned rows of all three.  Other shapes run a per-byte kernel.  All give
+ * the same bits.  Errors and asynchrony are as for the GEMM entry points.
  */
 int gemm_int4_dequant(const uint8_t* q, int K, int N, int ldq, const gemm_bf16_t* scales, int lds,
                       int group, int zero, gemm_bf16_t* W, int ldw, cudaStream_t stream);

@@ -55,7 +55,9 @@ def _same_bits(a, b):
 
 
 @pytest.mark.parametrize("out", [BF16, F32])
-@pytest.mark.parametrize("group,zero", [(128, 8), (1, 0), (32, 15), (100, 8), (4096, 3)])
+# groups 128, 32 and 4096 run 16 rows per thread, 24 runs 8, 100 runs 4, and 1 the
+# 32-codes-per-thread kernel
+@pytest.mark.parametrize("group,zero", [(128, 8), (1, 0), (32, 15), (24, 5), (100, 8), (4096, 3)])
 def test_vector_kernel_bit_exact(cuda_lib, out, group, zero):
     c = inputs.make_int4(384, 512, group=group, zero=zero, seed=group + zero)
     W, ran = _run(c, out)
@@ -84,11 +86,13 @@ def test_odd_column_count(cuda_lib):
     assert _same_bits(W, _expected(c, BF16))
 
 
-def test_padded_vector_rows(cuda_lib):
-    c = inputs.make_int4(130, 256, group=64, zero=8, seed=3)
-    W, ran = _run(c, BF16, ldq_pad=16, ldw_pad=8)
+@pytest.mark.parametrize("K,out", [(130, BF16), (144, BF16), (144, F32)])
+def test_padded_vector_rows(cuda_lib, K, out):
+    # K = 130 takes the 32-codes-per-thread kernel, K = 144 the row-blocked one
+    c = inputs.make_int4(K, 256, group=48, zero=8, seed=3)
+    W, ran = _run(c, out, ldq_pad=16, ldw_pad=8)
     assert ran == g.PATH_INT4
-    assert _same_bits(W, _expected(c, BF16))
+    assert _same_bits(W, _expected(c, out))
 
 
 def test_long_by_long_sampled(cuda_lib):
