@@ -101,14 +101,19 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr int B1 = B0 + 2 * VSTAGES;
   auto s_full = [&](int b) { return bar_base + 8u * (B1 + b); };
   auto s_empty = [&](int b) { return bar_base + 8u * (B1 + 2 + b); };
-  const uint32_t p_full = bar_base + 8u * (B1 + 4);
+  // P_j is released on p_full(j % 2).  Two barriers, not one: a warp that
+  // needs no rescale releases P_j without waiting for P V of tile j - 1, so
+  // it can reach tile j + 1 while another warp is still on tile j, and its
+  // arrival must not count toward tile j's phase.  Tile j + 2 (the next
+  // phase of the same barrier) needs S_{j+2}, which waits for P V of tile j.
+  auto p_full = [&](int b) { return bar_base + 8u * (B1 + 4 + b); };
   // P V of tile j completes on o_done(j % 2): a warp waits every phase of
   // each, in order, and the next phase of the same barrier (tile j + 2)
   // cannot start before that warp has released P of tile j + 1, so a waiter
   // is never two phases behind
-  auto o_done = [&](int b) { return bar_base + 8u * (B1 + 5 + b); };
-  const uint32_t drain_bar = bar_base + 8u * (B1 + 7);
-  constexpr int NBARS = B1 + 8;
+  auto o_done = [&](int b) { return bar_base + 8u * (B1 + 6 + b); };
+  const uint32_t drain_bar = bar_base + 8u * (B1 + 8);
+  constexpr int NBARS = B1 + 9;
   static_assert(NBARS * 8 + 16 <= AttnCfg<64>::BAR_BYTES, "barrier area");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_ptr + 8 * NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_ptr + 8 * NBARS + 8);
@@ -135,8 +140,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(s_full(b), 1);
       mbar_init(s_empty(b), 4);
       mbar_init(o_done(b), 1);
+      mbar_init(p_full(b), 4);
     }
-    mbar_init(p_full, 4);
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -227,7 +232,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // O += P_j V_j
       auto issue_pv = [&](int j) -> bool {
         const int s = j % VSTAGES, b = j & 1;
-        if (!mbar_wait(p_full, (uint32_t)j & 1u, p.timeout_ns, abort_flag)) return false;
+        if (!mbar_wait(p_full(b), ((uint32_t)(j / 2)) & 1u, p.timeout_ns, abort_flag)) return false;
         if (!mbar_wait(v_full(s), ((uint32_t)(j / VSTAGES)) & 1u, p.timeout_ns, abort_flag)) return false;
         tc_fence_after();
 #pragma unroll
@@ -324,7 +329,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!rescale) {
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_full);
+        if (lane == 0) mbar_arrive(p_full(b));
       }
       // every P V phase is observed in order (see o_done)
       if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(o_done((j - 1) & 1), ((uint32_t)((j - 1) / 2)) & 1u,
@@ -347,7 +352,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_full);
+        if (lane == 0) mbar_arrive(p_full(b));
       }
     }
     // ------------------------------------------------------------ epilogue
