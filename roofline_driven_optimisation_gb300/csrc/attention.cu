@@ -77,6 +77,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// 2^x by the special-function unit (ex2.approx, flush to zero): relative
+// error about 2^-22, far below the bf16 rounding P takes next; 2^-inf = 0
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <int D>
 __global__ void __launch_bounds__(THREADS, 1)
     attention_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
@@ -289,36 +297,40 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) mbar_arrive(s_empty(b));
       // scaled scores (log2 domain), masked only on tiles that need it
       float x[64];
-      float mt = -INFINITY;
       const int k0 = j * BNK;
       if (k0 + BNK - 1 <= min(vis_last, p.Sk - 1)) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          x[c] = __uint_as_float(c < 32 ? sa[c] : sb[c - 32]) * p.scale_log2;
-          mt = fmaxf(mt, x[c]);
-        }
+        for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(c < 32 ? sa[c] : sb[c - 32]) * p.scale_log2;
       } else {
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
           const int kj = k0 + c;
           const bool vis = kj < p.Sk && kj <= vis_last;
           x[c] = vis ? __uint_as_float(c < 32 ? sa[c] : sb[c - 32]) * p.scale_log2 : -INFINITY;
-          mt = fmaxf(mt, x[c]);
         }
       }
+      // row maximum and (below) row sum over eight independent partials, so
+      // neither is a 64-long dependency chain
+      float red[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) red[i] = x[i];
+#pragma unroll
+      for (int c = 8; c < 64; ++c) red[c % 8] = fmaxf(red[c % 8], x[c]);
+      const float mt = fmaxf(fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])),
+                             fmaxf(fmaxf(red[4], red[5]), fmaxf(red[6], red[7])));
       // move the reference maximum only when this tile exceeds it by > TAU
       const bool move = mt > m + TAU;       // also the first visible tile (m = -inf)
       const float m_new = move ? mt : m;
       const float m_use = m_new == -INFINITY ? 0.f : m_new;   // no visible key yet
-      const float alpha = move ? exp2f(m - m_use) : 1.f;     // 0 on the first visible tile
-      float psum = 0.f;
+      const float alpha = move ? ex2_approx(m - m_use) : 1.f;  // 0 on the first visible tile
       uint32_t pw[32];
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
-        const float p0 = exp2f(x[c] - m_use), p1 = exp2f(x[c + 1] - m_use);
-        psum += p0 + p1;
+        const float p0 = ex2_approx(x[c] - m_use), p1 = ex2_approx(x[c + 1] - m_use);
+        red[(c / 2) % 8] = c < 16 ? p0 + p1 : red[(c / 2) % 8] + (p0 + p1);
         pw[c / 2] = pack_bf16x2(p0, p1);
       }
+      const float psum = ((red[0] + red[1]) + (red[2] + red[3])) + ((red[4] + red[5]) + (red[6] + red[7]));
       l = l * alpha + psum;
       m = m_new;
       // P_j over the first 32 columns of its S buffer (two keys per column)
