@@ -127,8 +127,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_ptr + 8 * NBARS + 8);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int q0 = blockIdx.x * BM;
-  const int bh = blockIdx.y;                        // b * Hq + h
+  // causal: the longest query tiles (last rows, most keys) of every head are
+  // dispatched first and the short ones fill in behind them
+  int qt = blockIdx.x, bh = blockIdx.y;             // query tile, b * Hq + h
+  if (p.causal) {
+    const int lin = blockIdx.y * gridDim.x + blockIdx.x;
+    qt = gridDim.x - 1 - lin / gridDim.y;
+    bh = lin % gridDim.y;
+  }
+  const int q0 = qt * BM;
   const int kvh = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / (p.Hq / p.Hkv);
   // keys this tile of queries can see: all, or (causal) up to its last row
   const int k_limit = p.causal ? min(p.Sk, q0 + BM + (p.Sk - p.Sq)) : p.Sk;
