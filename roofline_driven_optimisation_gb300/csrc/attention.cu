@@ -85,6 +85,35 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Packed pairs of fp32 (two IEEE operations per instruction, round to
+// nearest even, as the scalar forms).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// max of three in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 template <int D>
 __global__ void __launch_bounds__(THREADS, 1)
     attention_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
@@ -302,42 +331,55 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_empty(b));
-      // scaled scores (log2 domain), masked only on tiles that need it
-      float x[64];
+      // raw scores, masked (-inf) only on tiles that need it; the scale is
+      // applied inside the exponent's FMA below
+      float sv[64];
       const int k0 = j * BNK;
       if (k0 + BNK - 1 <= min(vis_last, p.Sk - 1)) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(c < 32 ? sa[c] : sb[c - 32]) * p.scale_log2;
+        for (int c = 0; c < 64; ++c) sv[c] = __uint_as_float(c < 32 ? sa[c] : sb[c - 32]);
       } else {
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
           const int kj = k0 + c;
           const bool vis = kj < p.Sk && kj <= vis_last;
-          x[c] = vis ? __uint_as_float(c < 32 ? sa[c] : sb[c - 32]) * p.scale_log2 : -INFINITY;
+          sv[c] = vis ? __uint_as_float(c < 32 ? sa[c] : sb[c - 32]) : -INFINITY;
         }
       }
-      // row maximum and (below) row sum over eight independent partials, so
-      // neither is a 64-long dependency chain
+      // row maximum of the raw scores over eight independent partials (the
+      // scale is positive, so the maximum of the scaled scores is this one
+      // scaled, exactly: rounding is monotonic)
       float red[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) red[i] = x[i];
-#pragma unroll
-      for (int c = 8; c < 64; ++c) red[c % 8] = fmaxf(red[c % 8], x[c]);
-      const float mt = fmaxf(fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])),
-                             fmaxf(fmaxf(red[4], red[5]), fmaxf(red[6], red[7])));
+      for (int i = 0; i < 8; ++i) {
+        red[i] = fmax3(sv[i], sv[8 + i], sv[16 + i]);
+        red[i] = fmax3(red[i], sv[24 + i], sv[32 + i]);
+        red[i] = fmax3(red[i], sv[40 + i], sv[48 + i]);
+        red[i] = fmaxf(red[i], sv[56 + i]);
+      }
+      const float mt = fmax3(fmax3(red[0], red[1], red[2]), fmax3(red[3], red[4], red[5]),
+                             fmaxf(red[6], red[7])) * p.scale_log2;
       // move the reference maximum only when this tile exceeds it by > TAU
       const bool move = mt > m + TAU;       // also the first visible tile (m = -inf)
       const float m_new = move ? mt : m;
       const float m_use = m_new == -INFINITY ? 0.f : m_new;   // no visible key yet
       const float alpha = move ? ex2_approx(m - m_use) : 1.f;  // 0 on the first visible tile
+      // p = 2^(s * scale - m): the argument of two keys in one packed FMA,
+      // the row sum over four packed (eight scalar) partials
+      const uint64_t scale2 = f2_pack(p.scale_log2, p.scale_log2);
+      const uint64_t negm2 = f2_pack(-m_use, -m_use);
+      uint64_t sum2[4];
       uint32_t pw[32];
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
-        const float p0 = ex2_approx(x[c] - m_use), p1 = ex2_approx(x[c + 1] - m_use);
-        red[(c / 2) % 8] = c < 16 ? p0 + p1 : red[(c / 2) % 8] + (p0 + p1);
+        const float2 arg = f2_unpack(ffma2(f2_pack(sv[c], sv[c + 1]), scale2, negm2));
+        const float p0 = ex2_approx(arg.x), p1 = ex2_approx(arg.y);
+        const uint64_t pp = f2_pack(p0, p1);
+        sum2[(c / 2) % 4] = c < 8 ? pp : fadd2(sum2[(c / 2) % 4], pp);
         pw[c / 2] = pack_bf16x2(p0, p1);
       }
-      const float psum = ((red[0] + red[1]) + (red[2] + red[3])) + ((red[4] + red[5]) + (red[6] + red[7]));
+      const float2 s01 = f2_unpack(fadd2(sum2[0], sum2[1])), s23 = f2_unpack(fadd2(sum2[2], sum2[3]));
+      const float psum = (s01.x + s01.y) + (s23.x + s23.y);
       l = l * alpha + psum;
       m = m_new;
       // P_j over the first 32 columns of its S buffer (two keys per column)

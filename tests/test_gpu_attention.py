@@ -61,6 +61,17 @@ def test_unequal_lengths(cuda_lib, Sq, Sk, causal):
     assert ran == g.PATH_ATTN
 
 
+@pytest.mark.parametrize("D", [128, 64])
+@pytest.mark.parametrize("Sq,Sk,causal", [(700, 700, True), (700, 700, False), (1000, 700, True),
+                                          (384, 1200, True), (640, 333, False)])
+def test_several_query_blocks_and_key_tiles(cuda_lib, D, Sq, Sk, causal):
+    # query blocks of two 128-row tiles, ragged last block (its second tile
+    # may lie past Sq), several 128-key tiles with a ragged last one
+    c = inputs.make_attention(B=1, Hq=2, Hkv=1, Sq=Sq, Sk=Sk, D=D, seed=Sq + 3 * Sk + D)
+    _, ran = _check(c, causal)
+    assert ran == g.PATH_ATTN
+
+
 def test_grouped_kv_heads_and_scale(cuda_lib):
     c = inputs.make_attention(B=2, Hq=8, Hkv=2, Sq=192, Sk=320, D=128, seed=3)
     _check(c, True)
