@@ -18,8 +18,9 @@
 //     (barrier waits, commits) is paid once per eight MMAs;
 //   * two groups of four dequantisation warps, taking alternate stages, turn
 //     each column's 64 codes into the exact bf16 integers q - z (two codes per
-//     instruction: the magic-number bf16 128 + code, minus 128 + z) and write
-//     them straight into tensor memory with tcgen05.st, so the weight operand
+//     step: one lop3 makes the magic-number bf16 pair 128 + code, one packed
+//     bf16 FMA subtracts 128 + z) and write them, eight columns per store,
+//     straight into tensor memory with tcgen05.st, so the weight operand
 //     never passes through shared memory (a bf16 tile written and read back
 //     there would need more shared-memory bandwidth per SM than the HBM rate
 //     leaves); two groups keep two stages' load-convert-store chains in flight;
@@ -90,11 +91,24 @@ struct W4Params {
   int split;                 // CTAs per cluster along K
 };
 
-__device__ __forceinline__ uint32_t sub_bf16x2(uint32_t a, uint32_t b) {
-  __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a);
-  __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162*>(&b);
-  __nv_bfloat162 r = __hsub2(x, y);
-  return *reinterpret_cast<uint32_t*>(&r);
+// (a & mask) | magic in one instruction (lop3)
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t mask, uint32_t magic) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(magic));
+  return d;
+}
+// a * 1 + c on bf16 pairs: one packed FMA (exact here: the operands are
+// integers below 256)
+__device__ __forceinline__ uint32_t fma1_bf16x2(uint32_t a, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(0x3F803F80u), "r"(c));
+  return d;
+}
+// 8 consecutive 32-bit columns of this thread's TMEM lane; eight registers
+// per store keep the dequantised words where the arithmetic left them
+__device__ __forceinline__ void tmem_st_x8(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]) : "memory");
 }
 
 template <bool OUT_BF16>
@@ -294,7 +308,8 @@ __global__ void __launch_bounds__(THREADS, 2)
     const int n_local = quarter * 32 + lane;   // this thread's TMEM lane and W column
     const long long n = (long long)n0 + n_local;
     const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
-    const uint32_t zz = 0x43004300u + (uint32_t)p.zero * 0x00010001u;   // bf16x2 (128 + z)
+    // bf16x2 -(128 + z): the sign bits set on the magic number plus the zero point
+    const uint32_t negzz = (0x43004300u + (uint32_t)p.zero * 0x00010001u) ^ 0x80008000u;
     const unsigned short* sraw = reinterpret_cast<const unsigned short*>(p.scales);
     auto scale_raw = [&](int gl) -> uint32_t {
       return (gl < my_groups && n < a.N) ? (uint32_t)sraw[(long long)(g_begin + gl) * p.lds + n] : 0u;
@@ -358,13 +373,16 @@ __global__ void __launch_bounds__(THREADS, 2)
         if (c < nc) {
           const uint32_t wds[8] = {cw[c][0].x, cw[c][0].y, cw[c][0].z, cw[c][0].w,
                                    cw[c][1].x, cw[c][1].y, cw[c][1].z, cw[c][1].w};
-          uint32_t t[32];
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
+          for (int j2 = 0; j2 < 8; j2 += 2) {
+            uint32_t t[8];
 #pragma unroll
-            for (int h = 0; h < 4; ++h)
-              t[j * 4 + h] = sub_bf16x2(((wds[j] >> (4 * h)) & 0x000F000Fu) | 0x43004300u, zz);
-          tmem_st_32x32b_x32(lane_base + (uint32_t)(ra.slot * A_COLS + c * (BK / 2)), t);
+            for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+              for (int h = 0; h < 4; ++h)
+                t[jj * 4 + h] = fma1_bf16x2(and_or(wds[j2 + jj] >> (4 * h), 0x000F000Fu, 0x43004300u), negzz);
+            tmem_st_x8(lane_base + (uint32_t)(ra.slot * A_COLS + c * (BK / 2) + j2 * 4), t);
+          }
         }
       }
       tc_wait_st();
