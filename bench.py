@@ -324,6 +324,7 @@ def run_ours(args):
     e2e = run_e2e(args, g, torch, dev, parts, s, world)
     fused_ffn = measure_fused_ffn(g, torch, dev, s, hbm, bf16_peak) if rank == 0 else None
     fma_probe = measure_fp32_fma(g, torch, dev, fp32_peak / 1e12) if rank == 0 else None
+    configs = measure_configs(g, torch, dev, pk["bf16_tflops"], hbm) if rank == 0 else None
     fp8 = measure_fp8(g, torch, dev, pk["bf16_tflops"]) if rank == 0 else None
     int4_dq = measure_int4_dequant(g, torch, dev, hbm) if rank == 0 else None
     w4 = measure_w4_decode(g, torch, dev, hbm) if rank == 0 else None
@@ -341,6 +342,7 @@ def run_ours(args):
                          "once per step"},
         "roofline": roofline,
         "parts": part_out,
+        "bf16_configs": configs,
         "fused_ffn_swiglu": fused_ffn,
         "fp32_fma_probe": fma_probe,
         "fp8_gemm": fp8,
@@ -420,6 +422,57 @@ def measure_fp32_fma(g, torch, dev, formula_tflops, iters=16000, reps=3):
             best = max(best, flops / (e0.elapsed_time(e1) * 1e-3) / 1e12)
         out[f"{name}_tflops"] = round(best, 2)
         out[f"{name}_frac_of_formula"] = round(best / formula_tflops, 4)
+    return out
+
+
+def measure_configs(g, torch, dev, bf16_peak_tflops, hbm, reps=7):
+    """The bf16 workloads the step leaves out, each timed alone: 4096^3 with
+    fp32 C, 8192^3 with bf16 and fp32 C (seed 2), and the LLaMA-7B prefill
+    GEMMs at M = 2048 tokens (seed 3, bf16 C).  Events around each call, L2
+    flushed by a read pass before every call, median of `reps`.  Fraction of
+    min(measured bf16 peak, AI x measured HBM bandwidth).  Not part of the
+    step."""
+    from roofline_driven_optimisation_gb300 import inputs
+    from roofline_driven_optimisation_gb300 import roofline as R
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+    cases = [("bf16_4096_f32out", "bf16_4096", torch.float32), ("bf16_8192", "bf16_8192", torch.bfloat16),
+             ("bf16_8192_f32out", "bf16_8192", torch.float32)]
+    cases += [(f"prefill_m2048_{w}", f"prefill_{w}", torch.bfloat16) for w in WEIGHTS]
+    out = {"peak_tflops": round(bf16_peak_tflops, 1)}
+    made = {}
+    for name, wl, odt in cases:
+        if wl not in made:
+            made.clear()
+            c = inputs.make(wl)
+            made[wl] = (c.A.to(dev), c.B.to(dev))
+        A, B = made[wl]
+        M, K = A.shape
+        N = B.shape[1]
+        C = torch.empty((M, N), dtype=odt, device=dev)
+        g.gemm(A, B, C, 1.0, 0.0)
+        path, pair, bn = g.last_path(), g.last_tc_pair(), g.last_tile_n()
+        evs = []
+        for _ in range(reps):
+            flush.sum()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.gemm(A, B, C, 1.0, 0.0)
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+        fl = R.gemm_flops(M, N, K)
+        by = R.gemm_bytes(M, N, K, 2, C.element_size(), False)
+        roof = min(bf16_peak_tflops * 1e12, fl / by * hbm)
+        out[name] = {"M": M, "N": N, "K": K, "ms": round(ms, 5), "tflops": round(fl / (ms * 1e-3) / 1e12, 1),
+                     "frac_roofline": round(fl / (ms * 1e-3) / roof, 4), "ai": round(fl / by, 1),
+                     "kernel": g.PATH_NAMES[path] + (f" pair x{pair} BN {bn}" if path == g.PATH_BF16_TC else "")}
+        del C
+    made.clear()
+    status, where = g.device_status(stream.cuda_stream)
+    if status != 0:
+        raise RuntimeError(f"device status {status} at {where} in the config measurement")
     return out
 
 
