@@ -135,6 +135,47 @@ def test_forced_generic_agrees(cuda_lib):
     assert torch.allclose(fast, slow, rtol=0, atol=1e-4 * float(slow.abs().max()))
 
 
+@pytest.mark.parametrize("M", [1, 16])
+def test_llama_down_shape(cuda_lib, M):
+    # K 11008: 86 groups of 128 over a split-K cluster, ranks with odd stage counts
+    w, X, C0 = _case(M, 512, 11008, seed=M + 7)
+    _, ran, split = _check(w, X, C0, BF16)
+    assert ran == g.PATH_W4 and split > 1
+
+
+def test_back_to_back_calls_match_synchronised_calls(cuda_lib):
+    # the LLaMA-7B weight shapes (fewer columns) at M = 1, 4, 16, launched back
+    # to back on one stream as a decode step does: every result must equal the
+    # same call made alone
+    st = torch.cuda.current_stream().cuda_stream
+    calls = []
+    for m in (1, 4, 16):
+        for K, N in ((4096, 1536), (4096, 512), (4096, 1376), (11008, 512), (4096, 4000)):
+            w, X, C0 = _case(m, N, K, seed=m * 31 + N + K)
+            qk = g.int4_repack(w.q.cuda(), K, N)
+            calls.append((m, N, K, X.cuda(), qk, w.scales.cuda(), C0.cuda()))
+
+    def run(sync):
+        outs = []
+        for m, N, K, X, qk, sc, C0 in calls:
+            C = C0.clone()
+            g.gemm_w4a16(m, N, K, 1.0, X.data_ptr(), K, qk.data_ptr(), sc.data_ptr(), N, 128, 8, 1.0,
+                         C.data_ptr(), N, st)
+            outs.append(C)
+            if sync:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        return [c.cpu() for c in outs]
+
+    ref = run(True)
+    for _ in range(3):
+        got = run(False)
+        status, where = g.device_status()
+        assert status == 0, (status, where)
+        for a, b in zip(got, ref):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
 def test_deterministic(cuda_lib):
     w, X, C0 = _case(16, 1024, 4096, seed=6)
     a1, _, split = _run(w, X, C0, F32)
