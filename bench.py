@@ -363,7 +363,11 @@ def run_ours(args):
 
 def run_e2e(args, g, torch, dev, parts, s, world):
     """Same step through the public API with host buffers: every step copies
-    its inputs host->device from pinned memory and reads its results back."""
+    its inputs host->device from pinned memory and reads its results back.
+    Copies in, GEMMs and copies out run on three streams ordered by events,
+    so part i+1's inputs travel while part i computes and part i-1's result
+    comes back (a copy into a part's buffers waits for that part's previous
+    read-back)."""
     host = []
     h2d = d2h = 0
     for p in parts:
@@ -376,32 +380,58 @@ def run_e2e(args, g, torch, dev, parts, s, world):
         if hC0 is not None:
             h2d += hC0.numel() * hC0.element_size()
         d2h += hC.numel() * hC.element_size()
-    stream = torch.cuda.current_stream(dev)
+    comp = torch.cuda.current_stream(dev)
+    cin, cout = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    done_out = [None] * len(parts)
 
     def step():
-        for p, (hA, hB, hC0, hC) in zip(parts, host):
-            p["A_d"].copy_(hA, non_blocking=True)
-            p["B_d"].copy_(hB, non_blocking=True)
-            if hC0 is not None:
-                p["C_d"].copy_(hC0, non_blocking=True)
-            launch(g, p, p["A_d"], p["B_d"], p["C_d"], s)
-            hC.copy_(p["C_d"], non_blocking=True)
+        for i, (p, (hA, hB, hC0, hC)) in enumerate(zip(parts, host)):
+            with torch.cuda.stream(cin):
+                if done_out[i] is not None:
+                    cin.wait_event(done_out[i])      # last step's read-back of this part
+                p["A_d"].copy_(hA, non_blocking=True)
+                p["B_d"].copy_(hB, non_blocking=True)
+                if hC0 is not None:
+                    p["C_d"].copy_(hC0, non_blocking=True)
+                ready = torch.cuda.Event()
+                ready.record(cin)
+            comp.wait_event(ready)
+            launch(g, p, p["A_d"], p["B_d"], p["C_d"], comp.cuda_stream)
+            computed = torch.cuda.Event()
+            computed.record(comp)
+            with torch.cuda.stream(cout):
+                cout.wait_event(computed)
+                hC.copy_(p["C_d"], non_blocking=True)
+                done_out[i] = torch.cuda.Event()
+                done_out[i].record(cout)
+
+    def join():
+        # the timed region ends when all three streams are done
+        for st in (cin, cout):
+            ev = torch.cuda.Event()
+            ev.record(st)
+            comp.wait_event(ev)
 
     steps = max(1, min(args.steps, 20))
     for _ in range(max(1, args.warmup)):
         step()
+    join()
     torch.cuda.synchronize(dev)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
+    t0.record(comp)
+    cin.wait_event(t0)
+    cout.wait_event(t0)
     for _ in range(steps):
         step()
-    t1.record(stream)
+    join()
+    t1.record(comp)
     torch.cuda.synchronize(dev)
     ms = t0.elapsed_time(t1) / steps
     flops = sum(2 * p["M"] * p["N"] * p["K"] for p in parts)
     return {"value": round(world * flops / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
             "ms_per_step": round(ms, 4), "steps": steps,
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "streams": "copies in, GEMMs, copies out on three streams, ordered by events"}
 
 
 def measure_fp32_fma(g, torch, dev, formula_tflops, iters=16000, reps=3):
