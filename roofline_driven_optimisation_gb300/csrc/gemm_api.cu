@@ -134,6 +134,13 @@ struct MapKeyHash {
 };
 thread_local std::unordered_map<MapKey, CUtensorMap, MapKeyHash> t_maps;
 
+// The cache is bounded by emptying it at the start of an entry point, never
+// inside make_map: a call holds pointers to its earlier maps (A's while B's is
+// made), and clearing would leave them dangling.
+void trim_maps() {
+  if (t_maps.size() > 1024) t_maps.clear();
+}
+
 // 2-D row-major matrix (rows x cols, leading dimension ld_bytes) as a TMA
 // tensor with box (box_cols x box_rows); elements outside read as zero.
 int make_map(const void* ptr, uint64_t cols, uint64_t rows, uint64_t ld_bytes, uint32_t box_cols,
@@ -148,7 +155,6 @@ int make_map(const void* ptr, uint64_t cols, uint64_t rows, uint64_t ld_bytes, u
   }
   EncodeFn fn = encode_fn();
   if (!fn) return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  if (t_maps.size() > 1024) t_maps.clear();
   CUtensorMap map;
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {ld_bytes};
@@ -179,7 +185,6 @@ int make_map_3d(const void* ptr, uint64_t cols, uint64_t rows, uint64_t depth, u
   }
   EncodeFn fn = encode_fn();
   if (!fn) return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  if (t_maps.size() > 1024) t_maps.clear();
   CUtensorMap map;
   const cuuint64_t dims[3] = {cols, rows, depth};
   const cuuint64_t strides[2] = {ld_bytes, ld2_bytes};
@@ -204,6 +209,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int lda, const void* B,
         int ldb, float beta, void* C, int ldc, const float* bias, int act, cudaStream_t stream,
         bool swiglu = false, const void* B2 = nullptr, int fmt_a = kE4M3, int fmt_b = kE4M3) {
+  trim_maps();
   t_msg[0] = '\0';
   t_last_path = GEMM_PATH_AUTO;
   t_last_k_split = 1;
@@ -403,6 +409,7 @@ int int4_repack(const uint8_t* q, int K, int N, int ldq, uint8_t* qk, cudaStream
 int w4a16(int M, int N, int K, float alpha, const void* X, int ldx, const uint8_t* qk,
           const void* scales, int lds, int group, int zero, float beta, void* C, int ldc, Elem out,
           cudaStream_t stream) {
+  trim_maps();
   t_msg[0] = '\0';
   t_last_path = GEMM_PATH_AUTO;
   t_last_k_split = 1;
@@ -446,6 +453,7 @@ int w4a16(int M, int N, int K, float alpha, const void* X, int ldx, const uint8_
 
 int attention(int B, int Hq, int Hkv, int Sq, int Sk, int D, const void* Q, const void* K, const void* V,
               void* O, float scale, int causal, cudaStream_t stream) {
+  trim_maps();
   t_msg[0] = '\0';
   t_last_path = GEMM_PATH_AUTO;
   t_last_k_split = 1;

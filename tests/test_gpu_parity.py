@@ -377,3 +377,29 @@ def test_invalid_arguments(cuda_lib):
     assert e.value.code == g.GEMM_ERR_MISALIGNED
     g.gemm_f32(0, 4, 4, 1.0, 0, 4, 0, 4, 0.0, 0, 4, s)         # no-op
     assert g.last_path() == g.PATH_AUTO
+
+
+def test_many_distinct_operands(cuda_lib):
+    # more distinct (pointer, shape) operands than the per-thread tensor-map
+    # cache holds: the cache empties between calls, never inside one, so a
+    # call's first map stays valid while its second is made
+    M = N = K = 64
+    gen = torch.Generator().manual_seed(41)
+    A_all = torch.randn((700 * 8 + M * K,), generator=gen).to(BF16)
+    B_all = torch.randn((700 * 8 + K * N,), generator=gen).to(BF16)
+    A_d, B_d = A_all.cuda(), B_all.cuda()
+    C = torch.zeros((M, N), dtype=F32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    for i in range(700):
+        off = 8 * i   # 16-byte steps: every call gets new A and B maps
+        g.gemm_bf16_f32out(M, N, K, 1.0, A_d.data_ptr() + 2 * off, K, B_d.data_ptr() + 2 * off, N, 0.0,
+                           C.data_ptr(), N, s)
+        if i % 233 == 0 or i == 699:
+            torch.cuda.synchronize()
+            Ai = A_all[off:off + M * K].view(M, K)
+            Bi = B_all[off:off + K * N].view(K, N)
+            ref = oracle.gemm(Ai, Bi, 1.0, 0.0, None)
+            err = oracle.normwise_error(C.cpu(), ref, oracle.abs_product_max(Ai, Bi))
+            assert err <= oracle.TOL_BF16_F32OUT, (i, err)
+    status, where = g.device_status()
+    assert status == 0, (status, where)
