@@ -519,15 +519,9 @@ __global__ void __launch_bounds__(128) attention_generic_kernel(const __nv_bfloa
 template <int D>
 int launch_fast(const AttnParams& p, const CUtensorMap* mQ, const CUtensorMap* mK, const CUtensorMap* mV,
                 cudaStream_t s) {
-  static int attr_done_mask = 0;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 31 && !(attr_done_mask & (1 << dev))) {
-    cudaError_t e = cudaFuncSetAttribute(attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         AttnCfg<D>::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_done_mask |= (1 << dev);
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  cudaError_t e = set_smem_once(smem_set, attention_kernel<D>, AttnCfg<D>::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
   dim3 grid((unsigned)((p.Sq + BM - 1) / BM), (unsigned)(p.B * p.Hq));
   attention_kernel<D><<<grid, THREADS, AttnCfg<D>::SMEM_BYTES, s>>>(*mQ, *mK, *mV, p);
   return cudaGetLastError();

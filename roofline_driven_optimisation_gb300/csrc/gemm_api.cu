@@ -52,7 +52,7 @@ __device__ int g_status_word[2];
 
 constexpr int kMaxDevices = 64;
 struct DeviceInfo {
-  bool ready = false;
+  std::atomic<bool> ready{false};   // published after the fields below are set
   bool supported = false;
   int num_sms = 0;
   int* status = nullptr;
@@ -66,9 +66,9 @@ int device_info(DeviceInfo** out) {
   if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return fail(GEMM_ERR_UNSUPPORTED, "device index %d", dev);
   DeviceInfo& d = g_devices[dev];
-  if (!d.ready) {
+  if (!d.ready.load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> lock(g_dev_mutex);
-    if (!d.ready) {
+    if (!d.ready.load(std::memory_order_relaxed)) {
       int major = 0, minor = 0, sms = 0;
       cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
@@ -81,7 +81,7 @@ int device_info(DeviceInfo** out) {
       if (e != cudaSuccess)
         return fail(GEMM_ERR_CUDA, "status word address: %s", cudaGetErrorString(e));
       d.status = static_cast<int*>(p);
-      d.ready = true;
+      d.ready.store(true, std::memory_order_release);
     }
   }
   if (!d.supported)

@@ -268,14 +268,10 @@ template <int BN, bool OUT_BF16>
 int launch_impl(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB, int num_sms,
                 cudaStream_t s) {
   using Cfg = TileCfg<BN>;
-  static int attr_done_mask = 0;  // per-device bits; a race only repeats the call
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 31 && !(attr_done_mask & (1 << dev))) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc_kernel<BN, OUT_BF16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+  static std::atomic<uint64_t> smem_set{0};
+  {
+    cudaError_t e = set_smem_once(smem_set, gemm_bf16_tc_kernel<BN, OUT_BF16>, Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_done_mask |= (1 << dev);
   }
   TcParams p;
   p.a = a;

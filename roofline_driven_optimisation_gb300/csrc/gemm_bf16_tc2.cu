@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 struct PairLaunchInfo {
-  bool ready = false;
+  std::atomic<bool> ready{false};   // published after max_clusters is set
   int max_clusters = 0;
 };
 
@@ -385,9 +385,9 @@ int launch_pair_impl(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorM
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (!info[dev].ready) {
+  if (!info[dev].ready.load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> lock(mu);
-    if (!info[dev].ready) {
+    if (!info[dev].ready.load(std::memory_order_relaxed)) {
       cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            Cfg::SMEM_BYTES);
       if (e != cudaSuccess) return e;
@@ -398,7 +398,7 @@ int launch_pair_impl(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorM
       e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
       if (e != cudaSuccess) return e;
       info[dev].max_clusters = n > 0 ? n : 1;
-      info[dev].ready = true;
+      info[dev].ready.store(true, std::memory_order_release);
     }
   }
   TcParams p;

@@ -262,15 +262,11 @@ __global__ void __launch_bounds__(THREADS, 2)
 
 int launch_f32_simt(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
                     cudaStream_t s) {
-  static bool attr_done = false;  // idempotent; a race only repeats the calls
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(sgemm_tma_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(sgemm_tma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               SMEM_BYTES);
+  static std::atomic<uint64_t> smem_set_plain{0}, smem_set_epi{0};
+  {
+    cudaError_t e = set_smem_once(smem_set_plain, sgemm_tma_kernel<false>, SMEM_BYTES);
+    if (e == cudaSuccess) e = set_smem_once(smem_set_epi, sgemm_tma_kernel<true>, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_done = true;
   }
   SimtParams p;
   p.a = a;

@@ -376,11 +376,11 @@ __global__ void __launch_bounds__(THREADS, 2)
 }
 
 int choose_split(int tiles_n, int k_tiles, int num_sms) {
-  static int forced = -1;
-  if (forced < 0) {
+  // read once (a function-local static is initialised exactly once)
+  static const int forced = [] {
     const char* e = std::getenv("GB300GEMM_SKINNY_SPLIT");
-    forced = e ? std::atoi(e) : 0;
-  }
+    return e ? std::atoi(e) : 0;
+  }();
   int s = 1;
   if (forced == 1 || forced == 2 || forced == 4 || forced == 8) {
     s = forced;
@@ -396,14 +396,10 @@ template <bool OUT_BF16, bool SW>
 int launch_impl(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
                 const CUtensorMap* mapB2, int num_sms, cudaStream_t s, int* k_split) {
   constexpr int OUT_COLS = SW ? BN / 2 : BN;
-  static int attr_done_mask = 0;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 31 && !(attr_done_mask & (1 << dev))) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_skinny_kernel<OUT_BF16, SW>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  static std::atomic<uint64_t> smem_set{0};
+  {
+    cudaError_t e = set_smem_once(smem_set, gemm_skinny_kernel<OUT_BF16, SW>, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_done_mask |= (1 << dev);
   }
   SkinnyParams p;
   p.a = a;

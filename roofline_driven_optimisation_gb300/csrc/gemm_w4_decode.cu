@@ -538,11 +538,11 @@ __global__ void __launch_bounds__(256) gemm_w4_generic_kernel(const W4Params p) 
 }
 
 int choose_split(int tiles_n, int groups, int num_sms) {
-  static int forced = -1;
-  if (forced < 0) {
+  // read once (a function-local static is initialised exactly once)
+  static const int forced = [] {
     const char* e = std::getenv("GB300GEMM_W4_SPLIT");
-    forced = e ? std::atoi(e) : 0;
-  }
+    return e ? std::atoi(e) : 0;
+  }();
   int s = 1;
   if (forced == 1 || forced == 2 || forced == 4 || forced == 8) {
     s = forced;
@@ -557,14 +557,10 @@ int choose_split(int tiles_n, int groups, int num_sms) {
 template <bool OUT_BF16>
 int launch_fast(const W4Params& p0, const CUtensorMap* mapX, int num_sms, cudaStream_t s,
                 int* k_split) {
-  static int attr_done_mask = 0;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 31 && !(attr_done_mask & (1 << dev))) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_w4_decode_kernel<OUT_BF16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  static std::atomic<uint64_t> smem_set{0};
+  {
+    cudaError_t e = set_smem_once(smem_set, gemm_w4_decode_kernel<OUT_BF16>, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_done_mask |= (1 << dev);
   }
   W4Params p = p0;
   const int tiles_n = (p.a.N + BN - 1) / BN;

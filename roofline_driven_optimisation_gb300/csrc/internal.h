@@ -1,11 +1,27 @@
 // Interface between the C-ABI/dispatcher (gemm_api.cu) and the kernel
 // translation units.  Not installed; not part of the public ABI.
 #pragma once
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace g3 {
+
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` once per device
+// (the attribute belongs to the device's context); `done` holds one bit per
+// device.  Two threads racing on the first call both set it, which is harmless.
+template <class Kernel>
+cudaError_t set_smem_once(std::atomic<uint64_t>& done, Kernel kernel, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev >= 0 && dev < 64 ? (1ull << dev) : 0ull;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 enum class Elem : int { F32 = 0, BF16 = 1, FP8 = 2 };
 
