@@ -773,9 +773,18 @@ def cpu_baseline(parts, target_s=15.0):
     t = time.perf_counter()
     fl = oracle_sample_step(parts, frac, threads)
     dt = time.perf_counter() - t
+    # the smallest workload (fp32 256^3, alpha 1, beta 0) in full, on one core and on all
+    from roofline_driven_optimisation_gb300 import inputs
+    c = inputs.make("fp32_256")
+    small = {}
+    for label, th in (("one_core", 1), ("all_cores", threads)):
+        t1 = time.perf_counter()
+        oracle.gemm(c.A, c.B, 1.0, 0.0, None, th)
+        small[label + "_gflops"] = round(2 * 256 ** 3 / (time.perf_counter() - t1) / 1e9, 3)
     return {"value": round(fl / dt / 1e12, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"fp64 oracle on the first {frac:.4%} of the rows of the two 4096^3 GEMMs and of "
-                      f"the columns of the 18 decode GEMMs ({fl / 1e9:.1f} GFLOP, {dt:.1f} s)"}
+                      f"the columns of the 18 decode GEMMs ({fl / 1e9:.1f} GFLOP, {dt:.1f} s)",
+            "fp32_256_full": small}
 
 
 def run_reference(args):
