@@ -339,6 +339,11 @@ __global__ void __launch_bounds__(THREADS, 2)
     for (int m = 0; m < MN; ++m) partial[m * BN + n_local] = __uint_as_float(r[m]);
     cluster_sync();  // partials of every rank are visible cluster-wide
     const uint32_t partial_addr = smem_u32(partial);
+    // the sums first (every read of another rank's shared memory), then this
+    // rank says it is done reading, then the stores: the stores overlap the
+    // wait for the other ranks, and no rank leaves while others may still
+    // read its partial
+    float4 sum[RED_ITEMS], up[SW ? RED_ITEMS : 1];
 #pragma unroll
     for (int j = 0; j < RED_ITEMS; ++j) {
       const int it = threadIdx.x + j * THREADS;
@@ -346,13 +351,23 @@ __global__ void __launch_bounds__(THREADS, 2)
         const int m = it / groups;
         const int nl = rank * cols + (it % groups) * 4;
         const uint32_t off = partial_addr + (uint32_t)(m * BN + nl) * 4u;
+        sum[j] = sum_ranks(off, p.split);
+        // SwiGLU: the up-projection of the same columns is 64 rows further down D^T
+        if (SW) up[SW ? j : 0] = sum_ranks(off + (uint32_t)(BN / 2) * 4u, p.split);
+      }
+    }
+    cluster_arrive();
+#pragma unroll
+    for (int j = 0; j < RED_ITEMS; ++j) {
+      const int it = threadIdx.x + j * THREADS;
+      if (it < items) {
+        const int m = it / groups;
+        const int nl = rank * cols + (it % groups) * 4;
         const long long n = (long long)n0 + nl;
-        const float4 sum = sum_ranks(off, p.split);
-        const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
+        const float sv[4] = {sum[j].x, sum[j].y, sum[j].z, sum[j].w};
         if (SW) {
-          // the up-projection of the same columns is 64 rows further down D^T
-          const float4 up = sum_ranks(off + (uint32_t)(BN / 2) * 4u, p.split);
-          const float uv[4] = {up.x, up.y, up.z, up.w};
+          const float4 u = up[SW ? j : 0];
+          const float uv[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             if (n + e < a.N) store_swiglu(a, m, n + e, sv[e], uv[e]);
@@ -365,7 +380,7 @@ __global__ void __launch_bounds__(THREADS, 2)
         }
       }
     }
-    cluster_sync();  // no rank leaves while others may still read its partial
+    cluster_wait();
   }
   tc_fence_before();
   __syncthreads();
