@@ -44,12 +44,14 @@ DECODE_MS = (1, 4, 16)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
                   "sm_max_mhz": 2070.0}
 
-# DRAM bytes per launch measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum)
-# for each kernel source file, valid only while the file hashes to `sha256`.
+# DRAM bytes per call measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum,
+# summed over the call's launches) for each kernel source file, valid only while
+# the file hashes to `sha256`.
 NCU_TRAFFIC = {
-    # profiles/sgemm_tma_kernel_fp32_4096.md: 340.9 MB read + 53.7 MB written
-    "gemm_f32_simt.cu": {"sha256": "362df7d57406d257548c0c949b2d30b60177e7ec9188789a0a6d856ad4323cd2",
-                         "bytes_per_launch": 340862208 + 53732352},
+    # profiles/sgemm_tma_kernel_fp32_4096.md: whole-wave launch 311.0 MB read + 45.7 MB
+    # written, split last wave 55.6 MB read + 0.2 MB written
+    "gemm_f32_simt.cu": {"sha256": "61e11a7dd91d454329eb529206b41c282d69a4672b75a54855808f4a24f08cb6",
+                         "bytes_per_call": 311000832 + 45722368 + 55634176 + 171008},
 }
 
 
@@ -71,7 +73,7 @@ def kernel_sha(fname):
 def traffic_for(fname):
     t = NCU_TRAFFIC.get(fname)
     if t and t["sha256"] == kernel_sha(fname):
-        return t["bytes_per_launch"]
+        return t["bytes_per_call"]
     return None
 
 
@@ -195,6 +197,9 @@ def run_ours(args):
     for p in parts:
         launch(g, p, p["A_d"], p["B_d"], p["C_d"], s)
         path = g.last_path()
+        # kernel launches per call: the FP32 SIMT call adds a second launch
+        # when it splits the tiles of its partial last wave
+        p["kernels"] = 2 if path == g.PATH_F32_SIMT and g.last_k_split() > 1 else 1
         if path == g.PATH_BF16_TC:
             p["kernel"] = "gemm_bf16_tc2.cu" if g.last_tc_pair() == 2 else "gemm_bf16_tc.cu"
         else:
@@ -264,7 +269,8 @@ def run_ours(args):
         flops_by_kernel[kern] = flops_by_kernel.get(kern, 0) + fl
         time_by_kernel[kern] = time_by_kernel.get(kern, 0.0) + ms
         launches_by_kernel[kern] = launches_by_kernel.get(kern, 0) + len(plist)
-        ent = {"ms": round(ms, 5), "launches": len(plist), "tflops": round(fl / (ms * 1e-3) / 1e12, 2),
+        ent = {"ms": round(ms, 5), "calls": len(plist), "launches": sum(p["kernels"] for p in plist),
+               "tflops": round(fl / (ms * 1e-3) / 1e12, 2),
                "gbs": round(by / (ms * 1e-3) / 1e9, 1), "ai": round(fl / by, 2)}
         bound = plist[0]["bound"]
         if bound == "hbm":
@@ -316,8 +322,10 @@ def run_ours(args):
                 "traffic": (tr if tr is None else int(tr)),
                 "kernel": dom, "peak_source": src if rb != "alu" else
                 f"{n_sm} SMs x 128 FP32 lanes x 2 FLOP x {sm_max:.0f} MHz",
-                "algorithmic_bytes_per_launch": int(bytes_by_kernel[dom] / launches),
-                "algorithmic_flops_per_launch": int(flops_by_kernel[dom] / launches)}
+                # one call of the dominant kernel's GEMM (its launches back to back)
+                "launches_per_call": dom_parts[0]["kernels"],
+                "algorithmic_bytes_per_call": int(bytes_by_kernel[dom] / launches),
+                "algorithmic_flops_per_call": int(flops_by_kernel[dom] / launches)}
 
     ms_step = elapsed_ms / args.steps
     value = replicas.whole_job_rate(flops_step, world, ms_step * 1e-3) / 1e12
@@ -350,7 +358,7 @@ def run_ours(args):
         "w4a16_decode": w4,
         "attention": attn,
         "e2e": e2e,
-        "gpu_launches": len(parts) * args.steps,
+        "gpu_launches": sum(p["kernels"] for p in parts) * args.steps,
         "clocks": clocks.summary(),
     }
     if rank == 0:

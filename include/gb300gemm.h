@@ -324,14 +324,17 @@ int gemm_last_tc_pair(void);
 
 /*
  * Allow (1, the default) or forbid (0), for later calls on this host thread,
- * that the CTA-pair kernel runs the tiles of a partial last wave as two
- * half-width tiles each, on otherwise idle pairs.  For A/B measurements and
- * tests.
+ * that the tiles of a partial last wave run split: the CTA-pair kernel runs
+ * each as two half-width tiles on otherwise idle pairs; the FP32 SIMT kernel
+ * runs them as a second launch in which a cluster of four CTAs shares each
+ * tile's K range (partial sums added in rank order, in distributed shared
+ * memory).  For A/B measurements and tests.
  */
 int gemm_force_split_tiles(int enable);
 
 /* For the last call on this host thread: the number of CTAs that shared the
- * K range of one C tile (the decode kernel's cluster split), 1 if none did. */
+ * K range of one C tile (the decode kernels' cluster split, or 4 when the FP32
+ * SIMT kernel split its partial last wave), 1 if none did. */
 int gemm_last_k_split(void);
 
 /*

@@ -281,7 +281,7 @@ int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int 
       if ((rc = make_map(B, N, K, (uint64_t)ldb * 4, kSimtBN, kSimtBK, CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                          CU_TENSOR_MAP_SWIZZLE_NONE, &mB)) != GEMM_OK)
         return rc;
-      err = launch_f32_simt(a, mA, mB, stream);
+      err = launch_f32_simt(a, mA, mB, dev->num_sms, stream, &t_last_k_split);
       break;
     case GEMM_PATH_BF16_TC:
       if (in == Elem::FP8) {

@@ -24,8 +24,20 @@
 // needs only 64 contiguous bytes per load.  TMA zero-fills outside the
 // matrix, so ragged M, N, K need no guards in the main loop (the role the
 // bounds checks play in the thread-tile kernel of ch.10, 10.6).
+//
+// Waves ("Kernel 性能从何而来", "SM 占用率与资源压力": CTA slots, registers and
+// shared memory bound the CTAs an SM holds): two CTAs fit on an SM, so C
+// tiles run in waves of 2 x SMs, and a partial last wave leaves SMs idle.
+// Its tiles can instead run as a second launch in which a cluster of
+// kTailSplit CTAs shares each tile's K range; the partial sums meet in
+// distributed shared memory (no global workspace) and are added in rank
+// order, so results stay deterministic.  4096^3 on 152 SMs: 1024 tiles are
+// three waves of 304 and 112 tiles, whose wave then holds 448 quarter-tiles.
 #include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <atomic>
+#include <mutex>
 
 #include "epilogue.cuh"
 #include "internal.h"
@@ -43,11 +55,19 @@ constexpr int COMPUTE_WARPS = 8;
 constexpr int THREADS = COMPUTE_WARPS * 32;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 static_assert(STAGES * 8 + 16 + 2 * STAGES * 4 <= 256, "barrier area");
+constexpr int kTailSplit = 4;
+// A split CTA's partial tile, [BM][PART_LD] fp32 over the idle ring: the row
+// pitch of 132 floats puts the eight rows one 128-bit store covers on
+// distinct banks.
+constexpr int PART_LD = BN + 4;
+static_assert(BM * PART_LD * 4 <= STAGES * STAGE_BYTES, "partial tile fits the ring");
+static_assert(BM % kTailSplit == 0 && (BM / kTailSplit) * (BN / 4) % THREADS == 0, "reduce split");
 
 struct SimtParams {
   GemmArgs a;
   int tiles_m, tiles_n;
-  int c_vec;  // C pointer 16-byte aligned and ldc % 4 == 0
+  int c_vec;      // C pointer 16-byte aligned and ldc % 4 == 0
+  int tile_base;  // raster index of the split launch's first C tile
 };
 
 __device__ __forceinline__ float2 lds64(uint32_t addr) {
@@ -80,9 +100,45 @@ __device__ __forceinline__ float2 unpack2(uint64_t v) {
   return r;
 }
 
+// Four consecutive C elements of row m from column n on: v holds alpha*A*B;
+// adds beta*C, then bias and activation (EPI), and stores what lies inside C.
+template <bool EPI>
+__device__ __forceinline__ void store_quad(const GemmArgs& a, int c_vec, long long m, long long n,
+                                           float v[4]) {
+  float* cp = static_cast<float*>(a.C) + m * a.ldc + n;
+  const bool beta_nz = a.beta != 0.f;
+  if (c_vec && n + 3 < a.N) {
+    if (beta_nz) {
+      const float4 c = *reinterpret_cast<const float4*>(cp);
+      v[0] = fmaf(a.beta, c.x, v[0]);
+      v[1] = fmaf(a.beta, c.y, v[1]);
+      v[2] = fmaf(a.beta, c.z, v[2]);
+      v[3] = fmaf(a.beta, c.w, v[3]);
+    }
+    if (EPI) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = finish(a, v[j], n + j);
+    }
+    *reinterpret_cast<float4*>(cp) = make_float4(v[0], v[1], v[2], v[3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (n + j < a.N) {
+        float r = v[j];
+        if (beta_nz) r = fmaf(a.beta, cp[j], r);
+        cp[j] = EPI ? finish(a, r, n + j) : r;
+      }
+    }
+  }
+}
+
 // EPI: bias and/or activation present (the plain instance has no trace of
 // them, so the common case keeps the main loop's register allocation).
-template <bool EPI>
+// SPLIT: CTAs of a cluster that share one C tile's K range (1: a whole tile
+// per CTA); cluster rank r takes the r-th of SPLIT contiguous K ranges.
+// TRIGGER: a split launch of the last wave follows on the stream (the plain
+// instance has no trace of it: its code runs at the original speed).
+template <bool EPI, int SPLIT, bool TRIGGER>
 __global__ void __launch_bounds__(THREADS, 2)
     sgemm_tma_kernel(const __grid_constant__ CUtensorMap mapA,
                      const __grid_constant__ CUtensorMap mapB, const SimtParams p) {
@@ -107,7 +163,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   // near-square block of C and the A and B panels they share stay in L2
   // (4096^3: 16 x 19 tiles, 32 MB of A and 38 MB of B; groups of 8 rows
   // kept all of B in flight and read 19 % more from DRAM).
-  const int tile = blockIdx.x;
+  const int tile = SPLIT > 1 ? p.tile_base + (int)(blockIdx.x / SPLIT) : (int)blockIdx.x;
   const int group = 16;
   const int tiles_in_group = group * p.tiles_n;
   const int g = tile / tiles_in_group;
@@ -116,7 +172,12 @@ __global__ void __launch_bounds__(THREADS, 2)
   const int tm_idx = first_m + (tile % tiles_in_group) % gsize;
   const int tn_idx = (tile % tiles_in_group) / gsize;
   const int m0 = tm_idx * BM, n0 = tn_idx * BN;
-  const int k_tiles = (a.K + BK - 1) / BK;
+  int k_tiles = (a.K + BK - 1) / BK, kt_first = 0, part = 0;
+  if constexpr (SPLIT > 1) {
+    part = (int)cluster_ctarank();
+    kt_first = k_tiles * part / SPLIT;
+    k_tiles = k_tiles * (part + 1) / SPLIT - kt_first;
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -126,6 +187,9 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
     *abort_flag = 0;
     fence_mbar_init();
+    // the split launch of the last wave may take SM slots as this grid's CTAs
+    // leave (it reads nothing this grid writes)
+    if constexpr (TRIGGER) griddep_launch_dependents();
   }
   __syncthreads();
 
@@ -138,8 +202,8 @@ __global__ void __launch_bounds__(THREADS, 2)
     tma_prefetch_desc(&mapB);
     for (int kt = 0; kt < k_tiles && kt < STAGES; ++kt) {
       mbar_arrive_expect_tx(full_bar(kt), STAGE_BYTES);
-      tma_load_2d(a_tile(kt), &mapA, full_bar(kt), kt * BK, m0);
-      tma_load_2d(b_tile(kt), &mapB, full_bar(kt), n0, kt * BK);
+      tma_load_2d(a_tile(kt), &mapA, full_bar(kt), (kt_first + kt) * BK, m0);
+      tma_load_2d(b_tile(kt), &mapB, full_bar(kt), n0, (kt_first + kt) * BK);
       issue_cnt[kt] = 1;
     }
   }
@@ -199,7 +263,7 @@ __global__ void __launch_bounds__(THREADS, 2)
         done_cnt[s] = 0;
         __threadfence_block();
         if (kt + STAGES < k_tiles && !*abort_flag) {
-          const int kn = kt + STAGES;
+          const int kn = kt_first + kt + STAGES;
           mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
           tma_load_2d(a_tile(s), &mapA, full_bar(s), kn * BK, m0);
           tma_load_2d(b_tile(s), &mapB, full_bar(s), n0, kn * BK);
@@ -218,71 +282,220 @@ __global__ void __launch_bounds__(THREADS, 2)
         report_status(a.status, 5, kSiteSimtDrain);
   }
 
-  if (ok) {
-    // ---------------------------------------------------------- epilogue
-    float* C = static_cast<float*>(a.C);
-    const bool beta_nz = a.beta != 0.f;
+  if constexpr (SPLIT == 1) {
+    if (ok) {
+      // ---------------------------------------------------------- epilogue
+      float* C = static_cast<float*>(a.C);
+      const bool beta_nz = a.beta != 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const long long m = (long long)m0 + wm * 64 + i * 8 + tm;
-      if (m >= a.M) continue;
+      for (int i = 0; i < 8; ++i) {
+        const long long m = (long long)m0 + wm * 64 + i * 8 + tm;
+        if (m >= a.M) continue;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const long long n = (long long)n0 + wn * 32 + h * 16 + tn * 4;
-        float* cp = C + m * a.ldc + n;
-        const float2 lo = unpack2(acc[i][2 * h]), hi = unpack2(acc[i][2 * h + 1]);
-        float v[4] = {a.alpha * lo.x, a.alpha * lo.y, a.alpha * hi.x, a.alpha * hi.y};
-        if (p.c_vec && n + 3 < a.N) {
-          if (beta_nz) {
-            const float4 c = *reinterpret_cast<const float4*>(cp);
-            v[0] = fmaf(a.beta, c.x, v[0]);
-            v[1] = fmaf(a.beta, c.y, v[1]);
-            v[2] = fmaf(a.beta, c.z, v[2]);
-            v[3] = fmaf(a.beta, c.w, v[3]);
-          }
-          if (EPI) {
+        for (int h = 0; h < 2; ++h) {
+          const long long n = (long long)n0 + wn * 32 + h * 16 + tn * 4;
+          float* cp = C + m * a.ldc + n;
+          const float2 lo = unpack2(acc[i][2 * h]), hi = unpack2(acc[i][2 * h + 1]);
+          float v[4] = {a.alpha * lo.x, a.alpha * lo.y, a.alpha * hi.x, a.alpha * hi.y};
+          if (p.c_vec && n + 3 < a.N) {
+            if (beta_nz) {
+              const float4 c = *reinterpret_cast<const float4*>(cp);
+              v[0] = fmaf(a.beta, c.x, v[0]);
+              v[1] = fmaf(a.beta, c.y, v[1]);
+              v[2] = fmaf(a.beta, c.z, v[2]);
+              v[3] = fmaf(a.beta, c.w, v[3]);
+            }
+            if (EPI) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = finish(a, v[j], n + j);
-          }
-          *reinterpret_cast<float4*>(cp) = make_float4(v[0], v[1], v[2], v[3]);
-        } else {
+              for (int j = 0; j < 4; ++j) v[j] = finish(a, v[j], n + j);
+            }
+            *reinterpret_cast<float4*>(cp) = make_float4(v[0], v[1], v[2], v[3]);
+          } else {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (n + j < a.N) {
-              float r = v[j];
-              if (beta_nz) r = fmaf(a.beta, cp[j], r);
-              cp[j] = EPI ? finish(a, r, n + j) : r;
+            for (int j = 0; j < 4; ++j) {
+              if (n + j < a.N) {
+                float r = v[j];
+                if (beta_nz) r = fmaf(a.beta, cp[j], r);
+                cp[j] = EPI ? finish(a, r, n + j) : r;
+              }
             }
           }
         }
       }
     }
+  } else {
+    // ------------------------------------------- split epilogue (cluster)
+    // Every copy this CTA issued has landed (all were consumed, or drained
+    // above), so the ring holds this CTA's partial tile.
+    if (!*abort_flag) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int row = wm * 64 + i * 8 + tm, col = wn * 32 + h * 16 + tn * 4;
+          const float2 lo = unpack2(acc[i][2 * h]), hi = unpack2(acc[i][2 * h + 1]);
+          *reinterpret_cast<float4*>(base_ptr + ((size_t)row * PART_LD + col) * 4) =
+              make_float4(lo.x, lo.y, hi.x, hi.y);
+        }
+      }
+    }
+    cluster_sync();  // every rank's partial (and abort flag) is written
+    bool all_ok = true;
+#pragma unroll
+    for (int r = 0; r < SPLIT; ++r)
+      all_ok &= ld_dsmem_u32(map_to_rank(bar_base + 8u * STAGES, (uint32_t)r)) == 0u;
+    if (all_ok) {
+      // rank `part` sums rows [part*BM/SPLIT, (part+1)*BM/SPLIT) over the
+      // ranks in order 0..SPLIT-1; a warp covers one row of 128 columns
+      constexpr int QUADS = (BM / SPLIT) * (BN / 4) / THREADS;
+      float4 t[QUADS][SPLIT];
+#pragma unroll
+      for (int q = 0; q < QUADS; ++q) {
+        const int idx = (int)threadIdx.x + q * THREADS;
+        const int row = part * (BM / SPLIT) + idx / (BN / 4), col = (idx % (BN / 4)) * 4;
+        const uint32_t off = base + (uint32_t)(row * PART_LD + col) * 4u;
+#pragma unroll
+        for (int r = 0; r < SPLIT; ++r) t[q][r] = ld_dsmem_f32x4(map_to_rank(off, (uint32_t)r));
+      }
+#pragma unroll
+      for (int q = 0; q < QUADS; ++q) {
+        const int idx = (int)threadIdx.x + q * THREADS;
+        const long long m = (long long)m0 + part * (BM / SPLIT) + idx / (BN / 4);
+        const long long n = (long long)n0 + (idx % (BN / 4)) * 4;
+        float4 sum = t[q][0];
+#pragma unroll
+        for (int r = 1; r < SPLIT; ++r) {
+          sum.x += t[q][r].x;
+          sum.y += t[q][r].y;
+          sum.z += t[q][r].z;
+          sum.w += t[q][r].w;
+        }
+        float v[4] = {a.alpha * sum.x, a.alpha * sum.y, a.alpha * sum.z, a.alpha * sum.w};
+        if (m < a.M) store_quad<EPI>(a, p.c_vec, m, n, v);
+      }
+    }
+    cluster_sync();  // no rank leaves while another still reads its partial
+    // A grid that finishes before the one it overlaps would let later work on
+    // the stream run early; completion waits for that grid.
+    griddep_wait();
   }
   __syncthreads();
 }
 
 }  // namespace
 
-int launch_f32_simt(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
-                    cudaStream_t s) {
-  static std::atomic<uint64_t> smem_set_plain{0}, smem_set_epi{0};
-  {
-    cudaError_t e = set_smem_once(smem_set_plain, sgemm_tma_kernel<false>, SMEM_BYTES);
-    if (e == cudaSuccess) e = set_smem_once(smem_set_epi, sgemm_tma_kernel<true>, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
+namespace {
+
+// Time of `units` CTAs, each `unit` of a whole tile, with `slots` resident at
+// once, in tiles run two to an SM; a round of at most one CTA per SM runs
+// about 1.9x as fast (GB300, 4096^3 slices: 304 tiles two to an SM take
+// 679 us, 16 tiles alone 361 us).
+double rounds_time(long long units, double unit, long long slots, int sms) {
+  const long long rest = units % slots;
+  return unit * (double)(units / slots) + (rest == 0 ? 0.0 : rest <= sms ? 0.53 * unit : unit);
+}
+
+struct SplitLaunchInfo {
+  std::atomic<bool> ready{false};  // published after max_clusters is set
+  int max_clusters = 0;
+};
+
+template <bool EPI>
+cudaError_t launch_plan(const CUtensorMap* mapA, const CUtensorMap* mapB, SimtParams p,
+                        long long tiles, int num_sms, cudaStream_t s, int* k_split) {
+  static std::atomic<uint64_t> smem_set_whole{0};
+  static SplitLaunchInfo info[64];
+  static std::mutex mu;
+  static std::atomic<uint64_t> smem_set_first{0};
+  auto whole_kernel = sgemm_tma_kernel<EPI, 1, false>;
+  auto first_kernel = sgemm_tma_kernel<EPI, 1, true>;
+  auto split_kernel = sgemm_tma_kernel<EPI, kTailSplit, false>;
+  cudaError_t e = set_smem_once(smem_set_whole, whole_kernel, SMEM_BYTES);
+  if (e == cudaSuccess) e = set_smem_once(smem_set_first, first_kernel, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+
+  const long long slots = 2LL * num_sms;
+  const long long rest = tiles % slots, whole = tiles - rest;
+  const int k_tiles = (p.a.K + BK - 1) / BK;
+  bool split = split_tiles_enabled() && rest > 0 && k_tiles >= kTailSplit * 2 * STAGES;
+
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kTailSplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int dev = 0;
+  if (split) {
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!info[dev].ready.load(std::memory_order_acquire)) {
+      std::lock_guard<std::mutex> lock(mu);
+      if (!info[dev].ready.load(std::memory_order_relaxed)) {
+        if ((e = cudaFuncSetAttribute(split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      SMEM_BYTES)) != cudaSuccess)
+          return e;
+        // clusters of four resident at once: a GPC whose free CTA slots are
+        // not a multiple of four leaves the rest idle
+        int n = 0;
+        cfg.gridDim = dim3((unsigned)(kTailSplit * num_sms), 1, 1);
+        if ((e = cudaOccupancyMaxActiveClusters(&n, split_kernel, &cfg)) != cudaSuccess) return e;
+        info[dev].max_clusters = n;
+        info[dev].ready.store(true, std::memory_order_release);
+      }
+    }
+    // split when the quarter-tiles finish the last wave sooner, by more than
+    // a tenth of a tile (the reduction and the shorter pipelines)
+    const long long split_slots = (long long)kTailSplit * info[dev].max_clusters;
+    split = split_slots > 0 &&
+            rounds_time(rest * kTailSplit, 1.0 / kTailSplit, split_slots, num_sms) + 0.1 <
+                rounds_time(rest, 1.0, slots, num_sms);
   }
+
+  const long long first = split ? whole : tiles;
+  if (first > 0) {
+    if (split)
+      first_kernel<<<(unsigned)first, THREADS, SMEM_BYTES, s>>>(*mapA, *mapB, p);
+    else
+      whole_kernel<<<(unsigned)first, THREADS, SMEM_BYTES, s>>>(*mapA, *mapB, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || !split) return e;
+  }
+  *k_split = kTailSplit;
+  p.tile_base = (int)whole;
+  cfg.gridDim = dim3((unsigned)(rest * kTailSplit), 1, 1);
+  // overlap the first launch's last CTAs only when there is one: otherwise
+  // the previous kernel on the stream may still be writing A, B or C
+  cfg.numAttrs = first > 0 ? 2 : 1;
+  e = cudaLaunchKernelEx(&cfg, split_kernel, *mapA, *mapB, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int launch_f32_simt(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
+                    int num_sms, cudaStream_t s, int* k_split) {
+  *k_split = 1;
   SimtParams p;
   p.a = a;
   p.tiles_m = (a.M + BM - 1) / BM;
   p.tiles_n = (a.N + BN - 1) / BN;
   p.c_vec = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && (a.ldc % 4) == 0) ? 1 : 0;
+  p.tile_base = 0;
   const long long tiles = (long long)p.tiles_m * p.tiles_n;
   if (tiles <= 0) return cudaSuccess;
+  if (tiles * kTailSplit > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   if (a.bias != nullptr || a.act != kActNone)
-    sgemm_tma_kernel<true><<<(unsigned)tiles, THREADS, SMEM_BYTES, s>>>(*mapA, *mapB, p);
-  else
-    sgemm_tma_kernel<false><<<(unsigned)tiles, THREADS, SMEM_BYTES, s>>>(*mapA, *mapB, p);
-  return cudaGetLastError();
+    return launch_plan<true>(mapA, mapB, p, tiles, num_sms, s, k_split);
+  return launch_plan<false>(mapA, mapB, p, tiles, num_sms, s, k_split);
 }
 
 }  // namespace g3

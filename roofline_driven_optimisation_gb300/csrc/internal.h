@@ -83,8 +83,10 @@ int launch_generic(const GemmArgs& a, cudaStream_t s);
 
 // FP32 SIMT kernel: TMA tiles of A (16 k x 128 m, 64-byte swizzle) and
 // B (128 n x 16 k).
+// The tiles of a partial last wave may run as a second launch, K split over
+// clusters of four CTAs (*k_split = 4; 1 otherwise).
 int launch_f32_simt(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
-                    cudaStream_t s);
+                    int num_sms, cudaStream_t s, int* k_split);
 constexpr int kSimtBM = 128, kSimtBN = 128, kSimtBK = 16;
 
 // BF16 tcgen05 kernel: TMA tiles of A (64 k x 128 m) and B (64 n x 64 k),

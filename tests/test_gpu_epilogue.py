@@ -52,6 +52,16 @@ def test_fp32_simt_and_generic(cuda_lib, act, with_bias):
 
 
 @pytest.mark.parametrize("act", ACTS)
+def test_fp32_split_last_wave(cuda_lib, act):
+    # nine tiles with K = 1024: each tile's K range is split over four CTAs,
+    # and the rank that sums a row block applies beta, bias and activation
+    c = inputs.make("fp32_4096", M=300, N=264, K=1024)
+    assert _run(c, F32, 1.5, 0.5, True, act) == g.PATH_F32_SIMT
+    assert g.last_k_split() == 4
+    _run(c, F32, 1.0, 0.0, False, act)
+
+
+@pytest.mark.parametrize("act", ACTS)
 @pytest.mark.parametrize("out", [BF16, F32])
 @pytest.mark.parametrize("sched", [(1, 256), (1, 128), (2, 256), (2, 128)])
 def test_bf16_tensor_core(cuda_lib, act, out, sched):

@@ -100,10 +100,58 @@ def test_fp32_4096_full_size_sampled(cuda_lib):
     g.gemm(A, B, C, 1.5, 0.5)
     torch.cuda.synchronize()
     assert g.last_path() == g.PATH_F32_SIMT
+    # 1024 tiles = 3 waves of 304 + 112; whether the 112 split depends on how
+    # many clusters of four fit at once
+    assert g.last_k_split() in (1, 4)
     gen = np.random.default_rng(11)
     rows = np.sort(gen.choice(4096, 24, replace=False))
     cols = np.sort(gen.choice(4096, 24, replace=False))
     sampled_check(A, B, C, c.A, c.B, c.C0, 1.5, 0.5, oracle.TOL_F32, rows, cols)
+
+
+@pytest.mark.parametrize("M,N,K,pad", [(1024, 1024, 1024, (0, 0, 0)), (2560, 2048, 1024, (0, 0, 0)),
+                                       (1000, 1004, 1001, (3, 0, 0)), (300, 200, 1000, (0, 0, 0))])
+def test_fp32_split_last_wave(cuda_lib, M, N, K, pad):
+    # 1024^2: 64 tiles, all in the split launch; 2560 x 2048: 320 tiles, the
+    # 16 past two whole waves of 2 x 152 split; 1000 x 1004 x 1001: ragged M,
+    # N and K (63 K-slices, ranks take 15/16/16/16); 300 x 200: six tiles.
+    # Each partial wave holds at most 64 tiles, which the dispatcher splits
+    # whenever at least 64 clusters of four fit at once.
+    c = inputs.make("fp32_4096", M=M, N=N, K=K)
+    err, path = check(c.A, c.B, c.C0, 1.5, 0.5, F32, pad=pad)
+    assert path == g.PATH_F32_SIMT and g.last_k_split() == 4
+    # partial sums are added in rank order: repeated calls give the same bits
+    a = run_abi(c.A, c.B, c.C0, 1.5, 0.5, F32, pad=pad)[0]
+    b = run_abi(c.A, c.B, c.C0, 1.5, 0.5, F32, pad=pad)[0]
+    assert torch.equal(a, b)
+    g.force_split_tiles(0)
+    try:
+        check(c.A, c.B, c.C0, 1.5, 0.5, F32, pad=pad)
+        assert g.last_k_split() == 1
+    finally:
+        g.force_split_tiles(1)
+
+
+def test_fp32_split_result_feeds_next_call(cuda_lib):
+    # the split launch overlaps the end of the whole-wave launch; a GEMM queued
+    # right after must still read every tile of C1 final (C1 starts as NaN)
+    c = inputs.make("fp32_4096", M=2560, N=2048, K=1024)
+    D_cpu = inputs.make("fp32_4096", M=1, N=512, K=2048).B
+    A, B, D = c.A.cuda(), c.B.cuda(), D_cpu.cuda()
+    C1 = torch.empty(2560, 2048, device="cuda")
+    C2 = torch.empty(2560, 512, device="cuda")
+    for _ in range(3):
+        C1.fill_(float("nan"))
+        g.gemm(A, B, C1, 1.0, 0.0)
+        assert g.last_k_split() == 4
+        g.gemm(C1, D, C2, 1.0, 0.0)
+    torch.cuda.synchronize()
+    assert g.device_status()[0] == 0
+    C1_cpu = C1.cpu()
+    assert torch.isfinite(C1_cpu).all() and torch.isfinite(C2.cpu()).all()
+    ref = oracle.gemm(C1_cpu, D_cpu, 1.0, 0.0, None)
+    denom = oracle.normwise_denominator(C1_cpu, D_cpu, 1.0, 0.0, None)
+    assert oracle.normwise_error(C2.cpu(), ref, denom) <= oracle.TOL_F32
 
 
 # ------------------------------------------------------------------ bf16 tensor-core path
