@@ -332,6 +332,7 @@ def run_ours(args):
     e2e = run_e2e(args, g, torch, dev, parts, s, world)
     fused_ffn = measure_fused_ffn(g, torch, dev, s, hbm, bf16_peak) if rank == 0 else None
     fma_probe = measure_fp32_fma(g, torch, dev, fp32_peak / 1e12) if rank == 0 else None
+    graph = measure_graph_step(g, torch, dev, parts, flops_step) if rank == 0 else None
     configs = measure_configs(g, torch, dev, pk["bf16_tflops"], hbm) if rank == 0 else None
     fp8 = measure_fp8(g, torch, dev, pk["bf16_tflops"]) if rank == 0 else None
     int4_dq = measure_int4_dequant(g, torch, dev, hbm) if rank == 0 else None
@@ -350,6 +351,7 @@ def run_ours(args):
                          "once per step"},
         "roofline": roofline,
         "parts": part_out,
+        "graph_step": graph,
         "bf16_configs": configs,
         "fused_ffn_swiglu": fused_ffn,
         "fp32_fma_probe": fma_probe,
@@ -367,6 +369,33 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def measure_graph_step(g, torch, dev, parts, flops_step, reps=20):
+    """The same step captured once as a CUDA graph (stream capture of the same
+    C-ABI calls) and replayed: no host launch work inside the replays."""
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr):
+        cs = torch.cuda.current_stream(dev).cuda_stream
+        for p in parts:
+            launch(g, p, p["A_d"], p["B_d"], p["C_d"], cs)
+    for _ in range(3):
+        gr.replay()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        gr.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    status, where = g.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} at {where} in the graph replays")
+    ms = e0.elapsed_time(e1) / reps
+    return {"ms_per_step": round(ms, 4), "tflops": round(flops_step / (ms * 1e-3) / 1e12, 2),
+            "replays": reps}
 
 
 def run_e2e(args, g, torch, dev, parts, s, world):

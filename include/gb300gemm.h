@@ -30,9 +30,14 @@
  *   - Results of one call are deterministic: the same inputs give the same
  *     bits on every run (fixed reduction order, including split-K).
  *   - Calls made concurrently from several host threads are safe.
+ *   - Calls can be captured into a CUDA graph (stream capture) once the same
+ *     kind of call has run on the device: the first call of a kernel family
+ *     on a device sets kernel attributes and queries occupancy.
  *
  * Errors: every entry point returns a gemm_status.  On a non-zero return
- * nothing was launched and gemm_get_last_error() describes the cause.  Errors
+ * nothing was launched (except when the second launch of a two-launch call,
+ * the FP32 path's split last wave, fails after the first was queued) and
+ * gemm_get_last_error() describes the cause.  Errors
  * found on the device (a bounded wait that ran out) are recorded in a status
  * word that gemm_device_status() reads.
  */
