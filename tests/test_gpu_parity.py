@@ -132,6 +132,16 @@ def test_fp32_split_last_wave(cuda_lib, M, N, K, pad):
         g.force_split_tiles(1)
 
 
+def test_fp32_split_unaligned_c_and_nan_c(cuda_lib):
+    # the split epilogue's scalar path (C one element past an aligned base,
+    # ldc not a multiple of 4), and beta = 0 over a NaN-filled C
+    c = inputs.make("fp32_4096", M=300, N=200, K=1000)
+    err, path = check(c.A, c.B, c.C0, 1.5, 0.5, F32, offset=(0, 0, 1), pad=(0, 0, 3))
+    assert path == g.PATH_F32_SIMT and g.last_k_split() == 4
+    C, _, _ = run_abi(c.A, c.B, None, 1.0, 0.0, F32, c_fill=float("nan"))
+    assert g.last_k_split() == 4 and torch.isfinite(C).all()
+
+
 def test_fp32_split_result_feeds_next_call(cuda_lib):
     # the split launch overlaps the end of the whole-wave launch; a GEMM queued
     # right after must still read every tile of C1 final (C1 starts as NaN)
