@@ -50,7 +50,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NCU_TRAFFIC = {
     # profiles/sgemm_tma_kernel_fp32_4096.md: whole-wave launch 311.0 MB read + 45.7 MB
     # written, split last wave 55.6 MB read + 0.2 MB written
-    "gemm_f32_simt.cu": {"sha256": "61e11a7dd91d454329eb529206b41c282d69a4672b75a54855808f4a24f08cb6",
+    "gemm_f32_simt.cu": {"sha256": "9dcea2d5e108bc809c15e5c2b2e230c388204e9518b8bd6e5a9fa7884e587ab6",
                          "bytes_per_call": 311000832 + 45722368 + 55634176 + 171008},
 }
 

@@ -32,6 +32,7 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "plan.h"
 #include "ptx.cuh"
 #include "tc_epilogue.cuh"
 
@@ -303,60 +304,11 @@ int launch_bn(int bn, const GemmArgs& a, const CUtensorMap* mapA, const CUtensor
 
 }  // namespace
 
-// Tile width for a persistent grid: every wave of tiles costs about one
-// tile-time, so minimise waves(BN) * BN * cost_per_column(BN).  The relative
-// per-column costs are measured on GB300 at 8192^3, where the last-wave loss is
-// small: 1.000 (256), 1.012 (192), 1.070 (128); 224-wide MMAs cost 1.115 and
-// are never chosen automatically.  Ties go to the wider tile.
-int choose_tc_bn(int M, int N, int num_sms) {
-  static const int cands[] = {256, 192, 128};
-  static const int cost_milli[] = {1000, 1012, 1070};
-  const long long tiles_m = (M + BM - 1) / BM;
-  int best = 256;
-  long long best_cost = -1;
-  for (int i = 0; i < 3; ++i) {
-    const int bn = cands[i];
-    const long long tiles = tiles_m * ((N + bn - 1) / bn);
-    const long long waves = (tiles + num_sms - 1) / num_sms;
-    const long long cost = waves * bn * cost_milli[i];
-    if (best_cost < 0 || cost < best_cost) {
-      best_cost = cost;
-      best = bn;
-    }
-  }
-  return best;
-}
+// The wave models live in plan.h (host arithmetic shared with a CPU test).
+int choose_tc_bn(int M, int N, int num_sms) { return plan::tc_bn(M, N, num_sms); }
 
-// Single CTA or CTA pair, and the tile width: the same wave model over both
-// families.  A pair tile (256 x bn) runs on two SMs, so per SM it is a
-// 128 x bn tile; measured at 8192^3 its per-column cost is 0.882 (bn = 256)
-// and 1.018 (bn = 128) of the single-CTA 256-wide tile.  A partial last wave
-// of 256-wide pair tiles that fits in half the pairs runs as 128-wide halves
-// (when splitting is allowed), so it costs one 128-wide wave.  On a tie the
-// 128-wide pair kernel, evaluated first, is kept.
 void choose_tc_config(int M, int N, int num_sms, int* pair, int* bn) {
-  *pair = 1;
-  *bn = choose_tc_bn(M, N, num_sms);
-  const long long single_tiles = (long long)((M + BM - 1) / BM) * ((N + *bn - 1) / *bn);
-  const long long single_waves = (single_tiles + num_sms - 1) / num_sms;
-  const int single_cost_milli = *bn == 256 ? 1000 : *bn == 192 ? 1012 : 1070;
-  long long best = single_waves * *bn * single_cost_milli;
-  static const int pair_bn[] = {128, 256};
-  static const int pair_cost_milli[] = {1018, 882};
-  const int clusters = num_sms / 2 > 0 ? num_sms / 2 : 1;
-  for (int i = 0; i < 2; ++i) {
-    const long long tiles = (long long)((M + 2 * BM - 1) / (2 * BM)) * ((N + pair_bn[i] - 1) / pair_bn[i]);
-    const long long rem = tiles % clusters;
-    const long long wave = (long long)pair_bn[i] * pair_cost_milli[i];
-    const bool halved = pair_bn[i] == 256 && split_tiles_enabled() && rem > 0 && 2 * rem <= clusters;
-    const long long cost =
-        (tiles / clusters) * wave + (rem == 0 ? 0 : halved ? 128LL * pair_cost_milli[0] : wave);
-    if (cost < best) {
-      best = cost;
-      *pair = 2;
-      *bn = pair_bn[i];
-    }
-  }
+  plan::tc_config(M, N, num_sms, split_tiles_enabled(), pair, bn);
 }
 
 int launch_bf16_tc(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,

@@ -41,6 +41,7 @@
 
 #include "epilogue.cuh"
 #include "internal.h"
+#include "plan.h"
 #include "ptx.cuh"
 
 namespace g3 {
@@ -386,15 +387,6 @@ __global__ void __launch_bounds__(THREADS, 2)
 
 namespace {
 
-// Time of `units` CTAs, each `unit` of a whole tile, with `slots` resident at
-// once, in tiles run two to an SM; a round of at most one CTA per SM runs
-// about 1.9x as fast (GB300, 4096^3 slices: 304 tiles two to an SM take
-// 679 us, 16 tiles alone 361 us).
-double rounds_time(long long units, double unit, long long slots, int sms) {
-  const long long rest = units % slots;
-  return unit * (double)(units / slots) + (rest == 0 ? 0.0 : rest <= sms ? 0.53 * unit : unit);
-}
-
 struct SplitLaunchInfo {
   std::atomic<bool> ready{false};  // published after max_clusters is set
   int max_clusters = 0;
@@ -417,6 +409,7 @@ cudaError_t launch_plan(const CUtensorMap* mapA, const CUtensorMap* mapB, SimtPa
   const long long slots = 2LL * num_sms;
   const long long rest = tiles % slots, whole = tiles - rest;
   const int k_tiles = (p.a.K + BK - 1) / BK;
+  // a cheap first test before the occupancy query; plan::simt_split decides
   bool split = split_tiles_enabled() && rest > 0 && k_tiles >= kTailSplit * 2 * STAGES;
 
   cudaLaunchConfig_t cfg = {};
@@ -451,12 +444,9 @@ cudaError_t launch_plan(const CUtensorMap* mapA, const CUtensorMap* mapB, SimtPa
         info[dev].ready.store(true, std::memory_order_release);
       }
     }
-    // split when the quarter-tiles finish the last wave sooner, by more than
-    // a tenth of a tile (the reduction and the shorter pipelines)
-    const long long split_slots = (long long)kTailSplit * info[dev].max_clusters;
-    split = split_slots > 0 &&
-            rounds_time(rest * kTailSplit, 1.0 / kTailSplit, split_slots, num_sms) + 0.1 <
-                rounds_time(rest, 1.0, slots, num_sms);
+    // ten K-slices a rank at least (two rounds of the ring)
+    split = plan::simt_split(tiles, k_tiles, num_sms, info[dev].max_clusters, kTailSplit,
+                             2 * STAGES, true);
   }
 
   const long long first = split ? whole : tiles;

@@ -43,6 +43,7 @@
 
 #include "epilogue.cuh"
 #include "internal.h"
+#include "plan.h"
 #include "ptx.cuh"
 
 namespace g3 {
@@ -396,15 +397,7 @@ int choose_split(int tiles_n, int k_tiles, int num_sms) {
     const char* e = std::getenv("GB300GEMM_SKINNY_SPLIT");
     return e ? std::atoi(e) : 0;
   }();
-  int s = 1;
-  if (forced == 1 || forced == 2 || forced == 4 || forced == 8) {
-    s = forced;
-  } else {
-    const int target = 2 * num_sms;  // two CTAs fit on an SM
-    while (s * 2 <= MAX_SPLIT && tiles_n * s * 2 <= target) s *= 2;
-  }
-  while (s > 1 && s > k_tiles) s /= 2;
-  return s;
+  return plan::cluster_split(tiles_n, k_tiles, num_sms, forced, MAX_SPLIT);
 }
 
 template <bool OUT_BF16, bool SW>

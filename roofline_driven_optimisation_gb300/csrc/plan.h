@@ -1,0 +1,113 @@
+// Launch planning: the wave models that pick a kernel configuration from the
+// problem shape and the GPU's SM count.  Plain host arithmetic with no CUDA
+// types, so that the library and a CPU test compile the same code.
+//
+// Every model counts waves ("Kernel 性能从何而来", "SM 占用率与资源压力": the CTA
+// slots, registers and shared memory of an SM bound how many CTAs run at
+// once, so tiles run in waves and a partial last wave leaves SMs idle).
+// Per-column and per-tile costs are measured on GB300.
+#pragma once
+
+namespace g3 {
+namespace plan {
+
+// Tile width of the single-CTA tensor-core kernel: every wave of 128 x bn
+// tiles costs about one tile-time, so minimise waves(bn) * bn * cost(bn).
+// Relative per-column costs at 8192^3, where the last-wave loss is small:
+// 1.000 (256), 1.012 (192), 1.070 (128); 224-wide MMAs cost 1.115 and are
+// never chosen automatically.  Ties go to the wider tile.
+inline int tc_bn(int M, int N, int num_sms) {
+  static const int cands[] = {256, 192, 128};
+  static const int cost_milli[] = {1000, 1012, 1070};
+  const long long tiles_m = (M + 127) / 128;
+  int best = 256;
+  long long best_cost = -1;
+  for (int i = 0; i < 3; ++i) {
+    const int bn = cands[i];
+    const long long tiles = tiles_m * ((N + bn - 1) / bn);
+    const long long waves = (tiles + num_sms - 1) / num_sms;
+    const long long cost = waves * bn * cost_milli[i];
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+// Single CTA (pair = 1) or CTA pair (pair = 2), and the tile width: the same
+// wave model over both families.  A pair tile (256 x bn) runs on two SMs, so
+// per SM it is a 128 x bn tile; its per-column cost at 8192^3 is 0.882
+// (bn = 256) and 1.018 (bn = 128) of the single-CTA 256-wide tile.  A
+// partial last wave of 256-wide pair tiles that fits in half the pairs runs
+// as 128-wide halves when `split_allowed`, so it costs one 128-wide wave.  On
+// a tie the 128-wide pair kernel, evaluated first, is kept.
+inline void tc_config(int M, int N, int num_sms, bool split_allowed, int* pair, int* bn) {
+  *pair = 1;
+  *bn = tc_bn(M, N, num_sms);
+  const long long single_tiles = (long long)((M + 127) / 128) * ((N + *bn - 1) / *bn);
+  const long long single_waves = (single_tiles + num_sms - 1) / num_sms;
+  const int single_cost_milli = *bn == 256 ? 1000 : *bn == 192 ? 1012 : 1070;
+  long long best = single_waves * *bn * single_cost_milli;
+  static const int pair_bn[] = {128, 256};
+  static const int pair_cost_milli[] = {1018, 882};
+  const int clusters = num_sms / 2 > 0 ? num_sms / 2 : 1;
+  for (int i = 0; i < 2; ++i) {
+    const long long tiles = (long long)((M + 255) / 256) * ((N + pair_bn[i] - 1) / pair_bn[i]);
+    const long long rem = tiles % clusters;
+    const long long wave = (long long)pair_bn[i] * pair_cost_milli[i];
+    const bool halved = pair_bn[i] == 256 && split_allowed && rem > 0 && 2 * rem <= clusters;
+    const long long cost =
+        (tiles / clusters) * wave + (rem == 0 ? 0 : halved ? 128LL * pair_cost_milli[0] : wave);
+    if (cost < best) {
+      best = cost;
+      *pair = 2;
+      *bn = pair_bn[i];
+    }
+  }
+}
+
+// Time of `units` CTAs, each `unit` of a whole tile, with `slots` resident at
+// once, in tiles run two to an SM; a round of at most one CTA per SM runs
+// about 1.9x as fast (FP32 SIMT kernel on GB300, 4096^3 slices: 304 tiles two
+// to an SM take 679 us, 16 tiles alone 361 us).
+inline double rounds_time(long long units, double unit, long long slots, int sms) {
+  const long long rest = units % slots;
+  return unit * (double)(units / slots) + (rest == 0 ? 0.0 : rest <= sms ? 0.53 * unit : unit);
+}
+
+// FP32 SIMT kernel (two CTAs per SM): whether the tiles past the last whole
+// wave run as a second launch with K split over clusters of `split` CTAs.
+// `max_clusters` is how many such clusters are resident at once; each rank
+// needs at least `min_k_tiles` K-slices.  The quarter-tiles must finish the
+// partial wave sooner by more than a tenth of a tile (the reduction and the
+// shorter pipelines).
+inline bool simt_split(long long tiles, int k_tiles, int num_sms, int max_clusters, int split,
+                       int min_k_tiles, bool split_allowed) {
+  const long long slots = 2LL * num_sms;
+  const long long rest = tiles % slots;
+  if (!split_allowed || rest == 0 || k_tiles < split * min_k_tiles || max_clusters <= 0)
+    return false;
+  const long long split_slots = (long long)split * max_clusters;
+  return rounds_time(rest * split, 1.0 / split, split_slots, num_sms) + 0.1 <
+         rounds_time(rest, 1.0, slots, num_sms);
+}
+
+// Decode kernels: CTAs of a cluster that share one column slab's K range.  The
+// largest power of two up to `max_split` whose grid still fits two CTAs per
+// SM, and no more than the K units there are; `forced` (1, 2, 4 or 8)
+// overrides the first choice.
+inline int cluster_split(int tiles_n, int k_units, int num_sms, int forced, int max_split) {
+  int s = 1;
+  if (forced == 1 || forced == 2 || forced == 4 || forced == 8) {
+    s = forced;
+  } else {
+    const int target = 2 * num_sms;
+    while (s * 2 <= max_split && tiles_n * s * 2 <= target) s *= 2;
+  }
+  while (s > 1 && s > k_units) s /= 2;
+  return s;
+}
+
+}  // namespace plan
+}  // namespace g3
