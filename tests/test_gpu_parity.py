@@ -303,6 +303,26 @@ def test_bf16_tc_tile_width_choice(cuda_lib):
         g.force_tile_n(100)
 
 
+def test_bf16_dispatcher_counts_the_halved_last_wave(cuda_lib):
+    # 512 x 11008: 86 pair tiles of 256 x 256 = one wave of 76 pairs and 10
+    # tiles halved on 20 pairs, which beats single-CTA 192-wide tiles on
+    # GB300 (47.1 against 52.0 us at K = 4096); with the split forbidden the
+    # dispatcher keeps the single-CTA tiles
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    c = inputs.make("bf16_4096", M=512, N=11008, K=256)
+    for out in (BF16, F32):
+        check(c.A, c.B, None, 1.0, 0.0, out)
+        if sms == 152:
+            assert (g.last_tc_pair(), g.last_tile_n()) == (4, 256)
+    g.force_split_tiles(0)
+    try:
+        check(c.A, c.B, None, 1.0, 0.0, BF16)
+        if sms == 152:
+            assert (g.last_tc_pair(), g.last_tile_n()) == (1, 192)
+    finally:
+        g.force_split_tiles(1)
+
+
 def test_bf16_tc_padded_and_unaligned_c(cuda_lib):
     c = inputs.make("bf16_4096", M=260, N=272, K=136)
     check(c.A, c.B, None, 1.0, 0.0, BF16, pad=(8, 16, 3))
