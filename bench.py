@@ -48,10 +48,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # summed over the call's launches) for each kernel source file, valid only while
 # the file hashes to `sha256`.
 NCU_TRAFFIC = {
-    # profiles/sgemm_tma_kernel_fp32_4096.md: whole-wave launch 311.0 MB read + 45.7 MB
-    # written, split last wave 55.6 MB read + 0.2 MB written
-    "gemm_f32_simt.cu": {"sha256": "9dcea2d5e108bc809c15e5c2b2e230c388204e9518b8bd6e5a9fa7884e587ab6",
-                         "bytes_per_call": 311000832 + 45722368 + 55634176 + 171008},
+    # profiles/sgemm_tma_kernel_fp32_4096.md: whole-wave launch 311.5 MB read + 45.9 MB
+    # written, split last wave 55.7 MB read + 0.2 MB written
+    "gemm_f32_simt.cu": {"sha256": "2cb5f483b5d99dc16801f421672e218cc7eb534462a4eb58c6a00f3ca65cd284",
+                         "bytes_per_call": 311519488 + 45881600 + 55728896 + 221952},
 }
 
 

@@ -413,13 +413,15 @@ cudaError_t launch_plan(const CUtensorMap* mapA, const CUtensorMap* mapB, SimtPa
   bool split = split_tiles_enabled() && rest > 0 && k_tiles >= kTailSplit * 2 * STAGES;
 
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kTailSplit;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterSchedulingPolicyPreference;
+  attr[1].val.clusterSchedulingPolicyPreference = cudaClusterSchedulingPolicyLoadBalancing;
+  attr[2].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[2].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(THREADS, 1, 1);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = s;
@@ -461,9 +463,11 @@ cudaError_t launch_plan(const CUtensorMap* mapA, const CUtensorMap* mapB, SimtPa
   *k_split = kTailSplit;
   p.tile_base = (int)whole;
   cfg.gridDim = dim3((unsigned)(rest * kTailSplit), 1, 1);
-  // overlap the first launch's last CTAs only when there is one: otherwise
-  // the previous kernel on the stream may still be writing A, B or C
-  cfg.numAttrs = first > 0 ? 2 : 1;
+  // The hardware may place a cluster's CTAs where slots are free (4096^3 on
+  // GB300: 2.352 -> 2.272 ms against the default placement).  Overlap the
+  // first launch's last CTAs only when there is one: otherwise the previous
+  // kernel on the stream may still be writing A, B or C.
+  cfg.numAttrs = first > 0 ? 3 : 2;
   e = cudaLaunchKernelEx(&cfg, split_kernel, *mapA, *mapB, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
