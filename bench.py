@@ -15,6 +15,7 @@ for the two square GEMMs, HBM GB/s for the decode GEMMs (their arithmetic
 intensity is about M FLOP/byte).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --case bf16_8192 --reps 3      (one workload, for profiling)
 
 Under torchrun every rank runs the same step on its own GPU (replicas, weak
 scaling); time is the max over ranks.  ``--impl reference`` times the CPU
@@ -283,23 +284,46 @@ def run_ours(args):
         part_out[gname] = ent
 
     # per-shape decode times, isolated (events around every launch, after the
-    # timed region; the weights of the 18 GEMMs are distinct, so L2 is cold)
+    # timed region; the weights of the 18 GEMMs are distinct, so L2 is cold).
+    # A hold kernel keeps the stream busy while the host enqueues each batch,
+    # so no launch waits for the host and every interval is device time.  The
+    # same batch times two floors: a read-only pass over each weight's bytes
+    # and an empty launch.
+    import bench_probe
+    bench_probe.build()
     dec = groups[2][1]
+    sink = torch.zeros(4, dtype=torch.int32, device=dev)
     iso = {p["name"]: [] for p in dec}
+    floor = {p["name"]: [] for p in dec}
+    empty = []
+
+    def timed(fn, into):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        into.append((e0, e1))
+
     for _ in range(5):
+        bench_probe.probe_hold(20_000_000, s)
         for p in dec:
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            launch(g, p, p["A_d"], p["B_d"], p["C_d"], s)
-            e1.record(stream)
-            iso[p["name"]].append((e0, e1))
-    torch.cuda.synchronize(dev)
+            timed(lambda: launch(g, p, p["A_d"], p["B_d"], p["C_d"], s), iso[p["name"]])
+        for p in dec:
+            timed(lambda: bench_probe.probe_read_stream(p["B_d"].data_ptr(), p["B_d"].numel() * 2,
+                                                        sink.data_ptr(), s), floor[p["name"]])
+        for _ in range(4):
+            timed(lambda: bench_probe.probe_empty(s), empty)
+        torch.cuda.synchronize(dev)
     shapes = {}
     for p in dec:
         ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in iso[p["name"]])
+        fl_ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in floor[p["name"]])
         by = R.gemm_bytes(p["M"], p["N"], p["K"], 2, 2, True)
         shapes[p["name"]] = {"ms": round(ms, 5), "gbs": round(by / (ms * 1e-3) / 1e9, 1),
-                             "frac_hbm": round(by / (ms * 1e-3) / hbm, 4)}
+                             "frac_hbm": round(by / (ms * 1e-3) / hbm, 4),
+                             "read_only_floor_ms": round(fl_ms, 5),
+                             "vs_floor": round(fl_ms / ms, 4)}
+    shapes["empty_launch_ms"] = round(statistics.median(e0.elapsed_time(e1) for e0, e1 in empty), 5)
     part_out["decode"]["isolated"] = shapes
 
     dom = max(time_by_kernel, key=time_by_kernel.get)
@@ -474,16 +498,18 @@ def run_e2e(args, g, torch, dev, parts, s, world):
 def measure_fp32_fma(g, torch, dev, formula_tflops, iters=16000, reps=3):
     """Measured FP32 FMA rate with scalar and packed (f32x2) FMAs, against
     the SMs x 128 lanes x 2 x clock peak the FP32 roofline uses."""
+    import bench_probe
+    bench_probe.build()
     stream = torch.cuda.current_stream(dev)
     sink = torch.zeros(1, dtype=torch.float32, device=dev)
     out = {"formula_tflops": round(formula_tflops, 2)}
     for name, packed in (("scalar", False), ("packed_f32x2", True)):
-        g.probe_fp32_fma(packed, iters, sink.data_ptr(), stream.cuda_stream)   # warm-up
+        bench_probe.probe_fp32_fma(packed, iters, sink.data_ptr(), stream.cuda_stream)   # warm-up
         best = 0.0
         for _ in range(reps):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            flops = g.probe_fp32_fma(packed, iters, sink.data_ptr(), stream.cuda_stream)
+            flops = bench_probe.probe_fp32_fma(packed, iters, sink.data_ptr(), stream.cuda_stream)
             e1.record(stream)
             torch.cuda.synchronize(dev)
             best = max(best, flops / (e0.elapsed_time(e1) * 1e-3) / 1e12)
@@ -859,6 +885,153 @@ def run_reference(args):
     }), flush=True)
 
 
+# ---------------------------------------------------------------- profiling cases
+# ``python bench.py --case <workload>`` (or --swiglu/--fp8/--attention/--int4/--w4)
+# runs one workload through the C ABI a few times and prints the kernel family
+# and the CUDA-event time of each call: the commands the ncu summaries under
+# profiles/ are taken with.  Workload names are those of
+# ``roofline_driven_optimisation_gb300.inputs``.
+
+CASE_ARGS = ("case", "swiglu", "fp8", "attention", "int4", "w4")
+
+
+def run_case(a):
+    import torch
+    import roofline_driven_optimisation_gb300 as g
+    from roofline_driven_optimisation_gb300 import inputs
+
+    g.load()
+    if a.swiglu is not None:
+        return case_swiglu(g, torch, inputs, a)
+    if a.fp8 is not None:
+        return case_fp8(g, torch, inputs, a)
+    if a.attention is not None:
+        return case_attention(g, torch, inputs, a)
+    if a.int4 is not None:
+        return case_int4(g, torch, inputs, a)
+    if a.w4 is not None:
+        return case_w4(g, torch, inputs, a)
+    c = inputs.make(a.case, M=a.M, N=a.N, K=a.K)
+    sp = c.spec
+    if sp.in_dtype == "f32":
+        out = torch.float32
+    else:
+        out = torch.float32 if a.out == "f32" else torch.bfloat16
+    A, B = c.A.cuda(), c.B.cuda()
+    C = c.C0.to(out).cuda() if c.C0 is not None else torch.zeros((sp.M, sp.N), dtype=out, device="cuda")
+    for i in range(a.reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.gemm(A, B, C, sp.alpha, sp.beta)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        print(f"{a.case} M={sp.M} N={sp.N} K={sp.K} path={g.PATH_NAMES[g.last_path()]} "
+              f"call {i}: {ms:.4f} ms, {2 * sp.M * sp.N * sp.K / ms / 1e9:.1f} TFLOP/s")
+    status, where = g.device_status()
+    if status != 0:
+        raise SystemExit(f"device status {status} at site {where}")
+
+
+def case_swiglu(g, torch, inputs, a):
+    kw = {k: v for k, v in (("N", a.N), ("K", a.K)) if v is not None}
+    c = inputs.make_swiglu(a.swiglu, **kw)
+    A, Bg, Bu = c.A.cuda(), c.Bgate.cuda(), c.Bup.cuda()
+    M, K = A.shape
+    N = Bg.shape[1]
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    for i in range(a.reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.swiglu(A, Bg, Bu, C)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        by = 2 * M * K + 4 * K * N + 2 * M * N
+        print(f"swiglu M={M} N={N} K={K} path={g.PATH_NAMES[g.last_path()]} call {i}: {ms:.4f} ms, "
+              f"{4 * M * N * K / ms / 1e9:.1f} TFLOP/s, {by / ms / 1e6:.1f} GB/s")
+    status, where = g.device_status()
+    if status != 0:
+        raise SystemExit(f"device status {status} at site {where}")
+
+
+def case_fp8(g, torch, inputs, a):
+    n = a.fp8
+    c = inputs.make_fp8(n, n, n, inputs.FP8_E4M3, inputs.FP8_E4M3, seed=7)
+    A, B = c.A.cuda(), c.B.cuda()
+    C = torch.empty((n, n), dtype=torch.bfloat16, device="cuda")
+    for i in range(a.reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.gemm_fp8_tensors(A, 0, B, 0, C, c.alpha)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        print(f"fp8 e4m3 n={n} path={g.PATH_NAMES[g.last_path()]} call {i}: {ms:.4f} ms, "
+              f"{2 * n ** 3 / ms / 1e9:.1f} TFLOP/s")
+    status, where = g.device_status()
+    if status != 0:
+        raise SystemExit(f"device status {status} at site {where}")
+
+
+def _case_status(g):
+    status, where = g.device_status()
+    if status != 0:
+        raise SystemExit(f"device status {status} at site {where}")
+
+
+def _case_case_timed(torch, fn):
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def case_attention(g, torch, inputs, a):
+    S = a.attention
+    causal = not a.noncausal
+    c = inputs.make_attention(B=1, Hq=32, Hkv=32, Sq=S, Sk=S, D=128, seed=9)
+    Q, K, V = c.Q.cuda(), c.K.cuda(), c.V.cuda()
+    O = torch.empty_like(Q)
+    pairs = S * (S + 1) // 2 if causal else S * S
+    for i in range(a.reps):
+        ms = _case_timed(torch, lambda: g.attention(Q, K, V, O, causal=causal))
+        print(f"attention S={S} causal={causal} path={g.PATH_NAMES[g.last_path()]} call {i}: {ms:.4f} ms, "
+              f"{4 * 32 * 128 * pairs / ms / 1e9:.1f} TFLOP/s")
+    _case_status(g)
+
+
+def case_int4(g, torch, inputs, a):
+    n = a.int4
+    c = inputs.make_int4(n, n, group=128, zero=8, seed=8)
+    q, sc = c.q.cuda(), c.scales.cuda()
+    out = torch.float32 if a.out == "f32" else torch.bfloat16
+    W = torch.empty((n, n), dtype=out, device="cuda")
+    by = q.numel() + sc.numel() * 2 + W.numel() * W.element_size()
+    for i in range(a.reps):
+        ms = _case_timed(torch, lambda: g.int4_dequant(q, sc, n, 128, 8, W))
+        print(f"int4 dequant n={n} out={a.out} path={g.PATH_NAMES[g.last_path()]} call {i}: {ms:.4f} ms, "
+              f"{by / ms / 1e6:.1f} GB/s")
+    _case_status(g)
+
+
+def case_w4(g, torch, inputs, a):
+    M, K, N = a.w4, a.K or 4096, a.N or 32000
+    c = inputs.make_int4(K, N, group=128, zero=8, seed=1)
+    qk = g.int4_repack(c.q.cuda(), K, N)
+    X = torch.randn((M, K), generator=torch.Generator().manual_seed(4)).to(torch.bfloat16).cuda()
+    C = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+    sc = c.scales.cuda()
+    by = K * N // 2 + sc.numel() * 2 + 2 * M * K + 2 * M * N
+    for i in range(a.reps):
+        ms = _case_timed(torch, lambda: g.w4a16(X, qk, sc, 128, 8, C))
+        print(f"w4a16 M={M} N={N} K={K} path={g.PATH_NAMES[g.last_path()]} call {i}: {ms:.4f} ms, "
+              f"{by / ms / 1e6:.1f} GB/s")
+    _case_status(g)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -866,7 +1039,28 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    # profiling cases (one workload, a few calls; no JSON line)
+    ap.add_argument("--case", help="a workload of roofline_driven_optimisation_gb300.inputs")
+    ap.add_argument("--swiglu", type=int, metavar="M",
+                    help="fused silu(X Wg) * (X Wu) with M rows and the LLaMA-7B gate/up shapes")
+    ap.add_argument("--fp8", type=int, metavar="n", help="E4M3 GEMM of size n^3, bf16 C")
+    ap.add_argument("--attention", type=int, metavar="S", help="causal attention, 32 heads of 128")
+    ap.add_argument("--noncausal", action="store_true", help="attention without the causal mask")
+    ap.add_argument("--int4", type=int, metavar="n", help="INT4 dequantisation of an n x n weight (group 128)")
+    ap.add_argument("--w4", type=int, metavar="M",
+                    help="INT4-weight decode GEMM with M rows (K 4096, N 32000 unless given; group 128)")
+    ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--out", default="auto", choices=["auto", "bf16", "f32"])
+    ap.add_argument("--M", type=int)
+    ap.add_argument("--N", type=int)
+    ap.add_argument("--K", type=int)
     args = ap.parse_args()
+    n_case = sum(getattr(args, k) is not None for k in CASE_ARGS)
+    if n_case > 1:
+        ap.error("give at most one of --case, --swiglu, --fp8, --attention, --int4 and --w4")
+    if n_case == 1:
+        run_case(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -14,7 +14,7 @@
 
 #include <cstdint>
 
-#include "gb300gemm_probe.h"
+#include "gb300probe.h"
 
 namespace {
 
@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(THREADS) fma_rate_kernel(int iters, float* sin
 
 }  // namespace
 
-extern "C" int gemm_probe_fp32_fma(int packed, int iters, float* sink, double* flops,
+extern "C" int probe_fp32_fma(int packed, int iters, float* sink, double* flops,
                                    cudaStream_t stream) {
   if (iters <= 0 || sink == nullptr || flops == nullptr) return 1;
   int dev = 0, sms = 0;
@@ -88,4 +88,71 @@ extern "C" int gemm_probe_fp32_fma(int packed, int iters, float* sink, double* f
   if (cudaGetLastError() != cudaSuccess) return 4;
   *flops = (double)blocks * THREADS * (double)iters * CH * 2.0 /*lanes*/ * 2.0 /*FLOP per FMA*/;
   return 0;
+}
+
+// ---------------------------------------------------------------- HBM floors
+// What any kernel that must read `bytes` from HBM costs when launched alone
+// between two events: a read-only stream of 16-byte loads over the buffer
+// (two CTAs of 512 threads per SM, grid-stride), and an empty kernel (the
+// launch alone).  They bound the decode GEMMs' isolated times from below.
+
+namespace {
+
+__global__ void __launch_bounds__(512) read_stream_kernel(const uint4* __restrict__ p, size_t n16,
+                                                          unsigned* sink) {
+  unsigned x = 0;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  // four independent loads in flight per thread per round
+  for (; i + 3 * stride < n16; i += 4 * stride) {
+    const uint4 a = __ldcs(p + i), b = __ldcs(p + i + stride), c = __ldcs(p + i + 2 * stride),
+                d = __ldcs(p + i + 3 * stride);
+    x ^= a.x ^ a.y ^ a.z ^ a.w ^ b.x ^ b.y ^ b.z ^ b.w ^ c.x ^ c.y ^ c.z ^ c.w ^ d.x ^ d.y ^ d.z ^ d.w;
+  }
+  for (; i < n16; i += stride) {
+    const uint4 a = __ldcs(p + i);
+    x ^= a.x ^ a.y ^ a.z ^ a.w;
+  }
+  if (x == 0x9E3779B9u) sink[0] = x;  // data-dependent, so the loads stay
+}
+
+__global__ void empty_kernel() {}
+
+}  // namespace
+
+extern "C" int probe_read_stream(const void* buf, size_t bytes, unsigned* sink, cudaStream_t stream) {
+  if (buf == nullptr || sink == nullptr || (reinterpret_cast<uintptr_t>(buf) & 15u) || bytes % 16)
+    return 1;
+  if (bytes == 0) return 0;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 4;
+  read_stream_kernel<<<(unsigned)(2 * sms), 512, 0, stream>>>(static_cast<const uint4*>(buf), bytes / 16,
+                                                              sink);
+  return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}
+
+extern "C" int probe_empty(cudaStream_t stream) {
+  empty_kernel<<<1, 32, 0, stream>>>();
+  return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}
+
+// One CTA that spins on the global timer for `ns` nanoseconds, then returns:
+// it keeps the stream busy while the host enqueues a batch of timed launches,
+// so that no launch in the batch waits for the host.
+namespace {
+__global__ void hold_kernel(unsigned long long ns) {
+  unsigned long long t0, t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  do {
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  } while (t - t0 < ns);
+}
+}  // namespace
+
+extern "C" int probe_hold(unsigned long long ns, cudaStream_t stream) {
+  if (ns > 1000000000ull) return 1;  // at most one second
+  hold_kernel<<<1, 32, 0, stream>>>(ns);
+  return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }

@@ -265,11 +265,17 @@ int gemm_attention(int B, int Hq, int Hkv, int Sq, int Sk, int D, const gemm_bf1
 const char* gemm_get_last_error(void);
 
 /*
- * Synchronises `stream`, then reads and clears the device status word of the
- * current device.  Returns GEMM_OK, GEMM_ERR_DEVICE_TIMEOUT (a kernel gave up
- * a bounded wait and returned early; its C is unspecified), or GEMM_ERR_CUDA
- * if synchronisation itself failed.  If `where` is not NULL it receives the
- * kernel-specific location code of the first failure (0 if none).
+ * Takes the device status word of the current device: a one-thread kernel on
+ * `stream` exchanges it with zero atomically, then the stream is
+ * synchronised and the value returned.  The word is per device and shared by
+ * every stream and host thread: a failure recorded by a kernel on another
+ * stream is either in the value taken or left for the next call, never lost.
+ * Returns GEMM_OK, GEMM_ERR_DEVICE_TIMEOUT (a kernel gave up a bounded wait
+ * and returned early; its C is unspecified), or GEMM_ERR_CUDA if the launch
+ * or synchronisation itself failed.  If `where` is not NULL it receives the
+ * kernel-specific location code of the first failure (0 if none).  The
+ * `where` argument is this library's addition to the surveyed
+ * gemm_device_status(stream); NULL is accepted.
  */
 int gemm_device_status(cudaStream_t stream, int* where);
 
@@ -346,9 +352,29 @@ int gemm_last_k_split(void);
  * Upper bound, in nanoseconds, on any single wait inside a kernel launched
  * later by this process (default 1e9).  After it a kernel records
  * GEMM_ERR_DEVICE_TIMEOUT in the status word and returns.  0 restores the
- * default.
+ * default; other values outside [1e6, 1e10] (1 ms to 10 s) return
+ * GEMM_ERR_INVALID_ARG and leave the bound unchanged.  The waits that let
+ * copies and MMAs already in flight land after such an abort have their own
+ * fixed bound (200 ms) and do not use this one.
  */
 int gemm_set_wait_timeout_ns(uint64_t timeout_ns);
+
+/*
+ * Test hook for the abort paths of the CTA-pair tensor-core kernel, the
+ * decode split-K kernel and the FP32 SIMT kernel (including its split last
+ * wave).  With enable = 1, later calls on this host thread make one role of
+ * the first CTA or cluster wait on a barrier that nothing arrives at: the MMA
+ * issuer of the first pair, the MMA issuer of rank 0 of the first decode
+ * cluster, warp 0 of the first FP32 CTA.  That bounded wait runs out after
+ * a quarter of the gemm_set_wait_timeout_ns() limit (before any wait that
+ * follows from it, so its location code is the one recorded), the kernel records
+ * GEMM_ERR_DEVICE_TIMEOUT with that role's location code and leaves through
+ * its abort path (the other CTAs of the cluster included); C is unspecified.
+ * enable = 0 (the default) turns it off; other values return
+ * GEMM_ERR_INVALID_ARG.  Never faults: no copy is skipped and nothing is
+ * read or written out of bounds.
+ */
+int gemm_test_stall(int enable);
 
 /*
  * Self-test of the bounded-wait mechanism: launches one CTA that waits on a

@@ -46,7 +46,7 @@ EXPORTS = ("gemm_f32", "gemm_bf16", "gemm_bf16_f32out", "gemm_f32_ex", "gemm_bf1
            "gemm_device_status", "gemm_force_path", "gemm_last_path", "gemm_force_tile_n",
            "gemm_last_tile_n", "gemm_force_tc_pair", "gemm_last_tc_pair", "gemm_force_split_tiles",
            "gemm_last_k_split", "gemm_set_wait_timeout_ns", "gemm_selftest_wait_timeout",
-           "gemm_probe_fp32_fma")
+           "gemm_test_stall")
 
 _lib = None
 _lock = threading.Lock()
@@ -129,8 +129,8 @@ def load(path: str | None = None):
         lib.gemm_set_wait_timeout_ns.restype = i
         lib.gemm_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
         lib.gemm_selftest_wait_timeout.restype = i
-        lib.gemm_probe_fp32_fma.argtypes = [i, i, vp, ctypes.POINTER(ctypes.c_double), vp]
-        lib.gemm_probe_fp32_fma.restype = i
+        lib.gemm_test_stall.argtypes = [i]
+        lib.gemm_test_stall.restype = i
         _lib = lib
         return lib
 
@@ -256,15 +256,10 @@ def selftest_wait_timeout(ns: int, stream=0):
     _check(load().gemm_selftest_wait_timeout(ns, stream))
 
 
-def probe_fp32_fma(packed: bool, iters: int, sink_ptr: int, stream=0) -> float:
-    """Launch the FP32 FMA throughput probe; returns the launch's FLOPs."""
-    flops = ctypes.c_double(0.0)
-    rc = load().gemm_probe_fp32_fma(int(bool(packed)), int(iters), sink_ptr, ctypes.byref(flops),
-                                    stream)
-    if rc != 0:
-        raise GemmError(rc, "FMA probe launch failed")
-    return flops.value
-
+def test_stall(enable: int):
+    """Test hook: later calls on this thread make one role of the first CTA
+    wait on a barrier nothing arrives at, so the kernel's abort path runs."""
+    _check(load().gemm_test_stall(int(enable)))
 
 def _ld(t) -> int:
     """Leading dimension of a row-major 2-D tensor (unit stride along columns)."""

@@ -301,7 +301,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         fail_wait(kSiteAttnMma);
         if (issued_any) {
           tc_commit(drain_bar);
-          if (!mbar_wait(drain_bar, 0, p.timeout_ns, nullptr)) report_status(p.status, 5, kSiteAttnDrain);
+          if (!mbar_wait(drain_bar, 0, kDrainWaitNs, nullptr)) report_status(p.status, 5, kSiteAttnDrain);
         }
       }
     }

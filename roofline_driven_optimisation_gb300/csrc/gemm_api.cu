@@ -37,7 +37,11 @@ thread_local int t_forced_pair = 0;
 thread_local int t_last_pair = 0;
 thread_local int t_split_tiles = 1;
 thread_local int t_last_k_split = 1;
-std::atomic<uint64_t> g_timeout_ns{1000000000ull};
+thread_local int t_stall = 0;
+constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;  // 1 s
+constexpr uint64_t kMinTimeoutNs = 1000000ull;         // 1 ms
+constexpr uint64_t kMaxTimeoutNs = 10000000000ull;     // 10 s
+std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
 
 int fail(int code, const char* fmt, ...) {
   va_list ap;
@@ -48,7 +52,14 @@ int fail(int code, const char* fmt, ...) {
 }
 
 // ---------------------------------------------------------------- devices
-__device__ int g_status_word[2];
+__device__ int g_status_word;
+// Values taken by gemm_device_status: one slot per call in flight (a host
+// counter picks the slot), so concurrent readers on other streams never
+// overwrite each other's result.
+constexpr int kTakeSlots = 64;
+__device__ int g_status_taken[kTakeSlots];
+
+__global__ void status_take_kernel(int* status, int* out) { *out = atomicExch(status, 0); }
 
 constexpr int kMaxDevices = 64;
 struct DeviceInfo {
@@ -56,6 +67,7 @@ struct DeviceInfo {
   bool supported = false;
   int num_sms = 0;
   int* status = nullptr;
+  int* taken = nullptr;   // g_status_taken on this device
 };
 DeviceInfo g_devices[kMaxDevices];
 std::mutex g_dev_mutex;
@@ -81,6 +93,10 @@ int device_info(DeviceInfo** out) {
       if (e != cudaSuccess)
         return fail(GEMM_ERR_CUDA, "status word address: %s", cudaGetErrorString(e));
       d.status = static_cast<int*>(p);
+      e = cudaGetSymbolAddress(&p, g_status_taken);
+      if (e != cudaSuccess)
+        return fail(GEMM_ERR_CUDA, "status slot address: %s", cudaGetErrorString(e));
+      d.taken = static_cast<int*>(p);
       d.ready.store(true, std::memory_order_release);
     }
   }
@@ -248,6 +264,7 @@ int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int 
   a.swiglu = swiglu ? 1 : 0;
   a.fmt_a = fmt_a;
   a.fmt_b = fmt_b;
+  a.stall = t_stall;
 
   const bool tma_ok = K > 0 && aligned16(A) && aligned16(B) && (!swiglu || aligned16(B2)) &&
                       ((size_t)lda * in_sz) % 16 == 0 && ((size_t)ldb * in_sz) % 16 == 0;
@@ -622,18 +639,20 @@ int gemm_device_status(cudaStream_t stream, int* where) {
   g3::DeviceInfo* dev = nullptr;
   int rc = g3::device_info(&dev);
   if (rc != GEMM_OK) return rc;
-  cudaError_t e = cudaStreamSynchronize(stream);
-  if (e != cudaSuccess) return g3::fail(GEMM_ERR_CUDA, "stream sync: %s", cudaGetErrorString(e));
-  int word[2] = {0, 0};
-  e = cudaMemcpy(word, dev->status, sizeof(word), cudaMemcpyDeviceToHost);
+  // One atomic exchange on the device takes the word and leaves it zero: a
+  // failure recorded by a kernel on any stream is either in this value or
+  // stays for the next call, never lost between a read and a clear.
+  static std::atomic<unsigned> next_slot{0};
+  int* slot = dev->taken + (next_slot.fetch_add(1, std::memory_order_relaxed) % g3::kTakeSlots);
+  g3::status_take_kernel<<<1, 1, 0, stream>>>(dev->status, slot);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return g3::fail(GEMM_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
-  if (word[0] != 0) {
-    const int zero[2] = {0, 0};
-    e = cudaMemcpy(dev->status, zero, sizeof(zero), cudaMemcpyHostToDevice);
-    if (e != cudaSuccess) return g3::fail(GEMM_ERR_CUDA, "status clear: %s", cudaGetErrorString(e));
-  }
-  if (where) *where = word[1];
-  return word[0];
+  int word = 0;
+  e = cudaMemcpyAsync(&word, slot, sizeof(word), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return g3::fail(GEMM_ERR_CUDA, "stream sync: %s", cudaGetErrorString(e));
+  if (where) *where = (int)((unsigned)word >> 8);
+  return word & 0xff;
 }
 
 int gemm_force_path(int path) {
@@ -671,7 +690,17 @@ int gemm_force_split_tiles(int enable) {
 int gemm_last_k_split(void) { return g3::t_last_k_split; }
 
 int gemm_set_wait_timeout_ns(uint64_t timeout_ns) {
-  g3::g_timeout_ns.store(timeout_ns == 0 ? 1000000000ull : timeout_ns);
+  if (timeout_ns == 0) timeout_ns = g3::kDefaultTimeoutNs;
+  if (timeout_ns < g3::kMinTimeoutNs || timeout_ns > g3::kMaxTimeoutNs)
+    return g3::fail(GEMM_ERR_INVALID_ARG, "timeout_ns %llu outside [1e6, 1e10] (0 = default 1e9)",
+                    (unsigned long long)timeout_ns);
+  g3::g_timeout_ns.store(timeout_ns);
+  return GEMM_OK;
+}
+
+int gemm_test_stall(int enable) {
+  if (enable != 0 && enable != 1) return g3::fail(GEMM_ERR_INVALID_ARG, "enable must be 0 or 1");
+  g3::t_stall = enable;
   return GEMM_OK;
 }
 

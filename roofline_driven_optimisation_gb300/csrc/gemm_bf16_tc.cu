@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (*abort_flag) {
         for (int s = 0; s < STAGES; ++s)
           if (((issued >> s) & 1u) &&
-              !mbar_wait(full_bar(s), (issued_par >> s) & 1u, a.timeout_ns, nullptr))
+              !mbar_wait(full_bar(s), (issued_par >> s) & 1u, kDrainWaitNs, nullptr))
             report_status(a.status, 5, kSiteTcDrain);
       }
     }
@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (*abort_flag && issued_any) {
         // all MMAs issued so far must finish before TMEM and shared memory go away
         tc_commit(drain_bar);
-        if (!mbar_wait(drain_bar, 0, a.timeout_ns, nullptr)) report_status(a.status, 5, kSiteTcDrain);
+        if (!mbar_wait(drain_bar, 0, kDrainWaitNs, nullptr)) report_status(a.status, 5, kSiteTcDrain);
       }
     }
   } else {

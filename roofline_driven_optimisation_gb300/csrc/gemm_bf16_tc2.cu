@@ -136,6 +136,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_ptr + 8 * (2 * STAGES + 5));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_ptr + 8 * (2 * STAGES + 5) + 8);
+  const uint32_t stall_bar = bar_base + 8u * (2 * STAGES + 7);  // test hook: nothing arrives
+  static_assert(8 * (2 * STAGES + 8) <= BAR_BYTES, "barrier area");
   auto a_tile = [&](int s) { return base + s * STAGE_BYTES; };
   auto b_tile = [&](int s) { return base + s * STAGE_BYTES + A_STAGE_BYTES; };
 
@@ -169,6 +171,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(tempty_bar(b), 2 * NUM_EPI_WARPS * 32);
     }
     mbar_init(drain_bar, 1);
+    mbar_init(stall_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -224,7 +227,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (leader) {
           for (int s = 0; s < STAGES; ++s)
             if (((issued >> s) & 1u) &&
-                !mbar_wait(full_bar(s), (issued_par >> s) & 1u, a.timeout_ns, nullptr))
+                !mbar_wait(full_bar(s), (issued_par >> s) & 1u, kDrainWaitNs, nullptr))
               report_status(a.status, 5, kSiteTc2Drain);
         }
         // the peer's copies complete on a barrier this CTA cannot wait on:
@@ -247,6 +250,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true, issued_any = false;
+        if (a.stall && pair_id == 0 && !mbar_wait(stall_bar, 0, a.timeout_ns / 4, abort_flag)) {
+          // test hook: this wait runs out; the pair takes its abort path
+          if (!*abort_flag) report_status(a.status, 5, kSiteTc2Mma);
+          *abort_flag = 1;
+          ok = false;
+        }
         for (int i = 0; ok && i < n_items; ++i) {
           const uint32_t idesc = i < n_dp ? idesc_full : idesc_half;
           if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, a.timeout_ns, abort_flag)) {
@@ -290,7 +299,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         if (*abort_flag && issued_any) {
           tc_commit_pair_mc(drain_bar, 0x1);
-          if (!mbar_wait(drain_bar, 0, a.timeout_ns, nullptr)) report_status(a.status, 5, kSiteTc2Drain);
+          if (!mbar_wait(drain_bar, 0, kDrainWaitNs, nullptr)) report_status(a.status, 5, kSiteTc2Drain);
         }
       }
     }

@@ -55,7 +55,7 @@ constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int COMPUTE_WARPS = 8;
 constexpr int THREADS = COMPUTE_WARPS * 32;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
-static_assert(STAGES * 8 + 16 + 2 * STAGES * 4 <= 256, "barrier area");
+static_assert(STAGES * 8 + 16 + 2 * STAGES * 4 <= 128, "barrier area (the stall barrier sits at 128)");
 constexpr int kTailSplit = 4;
 // A split CTA's partial tile, [BM][PART_LD] fp32 over the idle ring: the row
 // pitch of 132 floats puts the eight rows one 128-bit store covers on
@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   // per slot: warps done with it this round, and copies issued into it so far
   uint32_t* done_cnt = reinterpret_cast<uint32_t*>(bars + STAGES) + 4;
   uint32_t* issue_cnt = done_cnt + STAGES;
+  const uint32_t stall_bar = bar_base + 128u;  // test hook: nothing arrives
   auto full_bar = [&](int s) { return bar_base + 8u * s; };
   auto a_tile = [&](int s) { return base + s * STAGE_BYTES; };
   auto b_tile = [&](int s) { return base + s * STAGE_BYTES + A_STAGE_BYTES; };
@@ -186,6 +187,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       done_cnt[s] = 0;
       issue_cnt[s] = 0;
     }
+    mbar_init(stall_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
     // the split launch of the last wave may take SM slots as this grid's CTAs
@@ -222,7 +224,18 @@ __global__ void __launch_bounds__(THREADS, 2)
     for (int q = 0; q < 4; ++q) acc[i][q] = 0ull;
 
   bool ok = true;
-  for (int kt = 0; kt < k_tiles; ++kt) {
+  int my_k_tiles = k_tiles;
+  if (a.stall && warp == 0 && blockIdx.x == 0 && k_tiles > 0) {
+    // test hook: warp 0 of the first CTA waits on a barrier nothing arrives
+    // at, so its bounded wait runs out and the abort path runs
+    if (!mbar_wait(stall_bar, 0, a.timeout_ns / 4, abort_flag)) {
+      if (!*abort_flag) report_status(a.status, 5, kSiteSimtConsumer);
+      *abort_flag = 1;
+      ok = false;
+      my_k_tiles = 0;
+    }
+  }
+  for (int kt = 0; kt < my_k_tiles; ++kt) {
     const int s = kt % STAGES;
     const uint32_t parity = (uint32_t)(kt / STAGES) & 1u;
     if (!mbar_wait(full_bar(s), parity, a.timeout_ns, abort_flag)) {
@@ -279,7 +292,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     // the latest copy into slot s completes its phase issue_cnt[s] - 1
     for (int s = 0; s < STAGES; ++s)
       if (issue_cnt[s] > 0 &&
-          !mbar_wait(full_bar(s), (issue_cnt[s] - 1u) & 1u, a.timeout_ns, nullptr))
+          !mbar_wait(full_bar(s), (issue_cnt[s] - 1u) & 1u, kDrainWaitNs, nullptr))
         report_status(a.status, 5, kSiteSimtDrain);
   }
 

@@ -147,6 +147,8 @@ __global__ void __launch_bounds__(THREADS, 2)
   const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 1);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_ptr + 8 * (2 * STAGES + 2));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_ptr + 8 * (2 * STAGES + 2) + 8);
+  const uint32_t stall_bar = bar_base + 8u * (2 * STAGES + 4);  // test hook: nothing arrives
+  static_assert(8 * (2 * STAGES + 5) <= 256, "barrier area");
   auto b_tile = [&](int s) { return base + s * STAGE_BYTES; };
   auto a_tile = [&](int s) { return base + s * STAGE_BYTES + B_STAGE_BYTES; };
   float* partial = reinterpret_cast<float*>(base_ptr);  // [MN][BN], valid after the main loop
@@ -169,6 +171,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
     mbar_init(tfull_bar, 1);
     mbar_init(drain_bar, 1);
+    mbar_init(stall_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -259,7 +262,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       if (*abort_flag) {
         for (int s = 0; s < STAGES; ++s)
           if (((issued >> s) & 1u) &&
-              !mbar_wait(full_bar(s), (issued_par >> s) & 1u, a.timeout_ns, nullptr))
+              !mbar_wait(full_bar(s), (issued_par >> s) & 1u, kDrainWaitNs, nullptr))
             report_status(a.status, 5, kSiteSkinnyDrain);
       }
     }
@@ -270,7 +273,14 @@ __global__ void __launch_bounds__(THREADS, 2)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int kt = 0; kt < my_kt; ++kt) {
+      if (a.stall && rank == 0 && blockIdx.y == 0 &&
+          !mbar_wait(stall_bar, 0, a.timeout_ns / 4, abort_flag)) {
+        // test hook: this wait runs out; the cluster takes its abort path
+        if (!*abort_flag) report_status(a.status, 5, kSiteSkinnyMma);
+        *abort_flag = 1;
+        ok = false;
+      }
+      for (int kt = 0; ok && kt < my_kt; ++kt) {
         if (!mbar_wait(full_bar(stage), phase, a.timeout_ns, abort_flag)) {
           if (!*abort_flag) report_status(a.status, 5, kSiteSkinnyMma);
           *abort_flag = 1;
@@ -294,7 +304,7 @@ __global__ void __launch_bounds__(THREADS, 2)
         tc_commit(tfull_bar);
       } else {
         tc_commit(drain_bar);
-        if (!mbar_wait(drain_bar, 0, a.timeout_ns, nullptr)) report_status(a.status, 5, kSiteSkinnyDrain);
+        if (!mbar_wait(drain_bar, 0, kDrainWaitNs, nullptr)) report_status(a.status, 5, kSiteSkinnyDrain);
       }
     }
   }

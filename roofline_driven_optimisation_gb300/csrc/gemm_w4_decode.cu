@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       if (*abort_flag) {
         for (int s = 0; s < SSTAGES; ++s)
           if (((issued >> s) & 1u) &&
-              !mbar_wait(code_full(s), (issued_par >> s) & 1u, a.timeout_ns, nullptr))
+              !mbar_wait(code_full(s), (issued_par >> s) & 1u, kDrainWaitNs, nullptr))
             report_status(a.status, 5, kSiteW4Drain);
       }
     }
@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       }
       if (*abort_flag && issued_any) {
         tc_commit(drain_bar);
-        if (!mbar_wait(drain_bar, 0, a.timeout_ns, nullptr)) report_status(a.status, 5, kSiteW4Drain);
+        if (!mbar_wait(drain_bar, 0, kDrainWaitNs, nullptr)) report_status(a.status, 5, kSiteW4Drain);
       }
     }
   } else {

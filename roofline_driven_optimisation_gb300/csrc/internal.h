@@ -42,16 +42,20 @@ struct GemmArgs {
   void* C;
   long long ldc;
   Elem in, out;
-  int* status;          // device status word (2 ints)
+  int* status;          // device status word (one int, see report_status)
   uint64_t timeout_ns;  // bound on any single wait inside a kernel
   const float* bias;    // N fp32 values added to every row of C, or null
   int act;              // Act applied last
   const void* B2;       // SwiGLU: the up-projection (K x N, leading dimension ldb), else null
   int swiglu;           // 1: C = silu(A*B) * (A*B2) (alpha 1, beta 0, no bias)
   int fmt_a, fmt_b;     // in == FP8: the formats of A and B (Fp8Fmt)
+  int stall;            // test hook: one role of the first CTA (or cluster) waits on a
+                        // barrier nothing arrives at, so its bounded wait runs out and
+                        // the kernel's abort path runs (tc2, skinny, FP32 SIMT kernels)
 };
 
-// Location codes recorded with a device timeout (status[1]).
+// Location codes recorded with a device timeout (bits 8 and up of the
+// status word; the low 8 bits hold the gemm_status code).
 enum WaitSite : int {
   kSiteSelftest = 1,
   kSiteTcProducer = 10,

@@ -392,12 +392,19 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 }
 
 // ---------------------------------------------------------------- status
-// Device-side status word: the first error code wins; the host reads and
-// clears it.  Codes match gemm_status in the public header.
+// Device-side status word: the first error wins; the host takes it with one
+// atomic exchange, so a failure recorded at any moment is either in the value
+// taken or left for the next read.  Low 8 bits: a gemm_status code of the
+// public header; the bits above: the location code (WaitSite).
 __device__ __forceinline__ void report_status(int* status, int code, int where) {
-  if (status != nullptr) {
-    if (atomicCAS(status, 0, code) == 0) status[1] = where;
-  }
+  if (status != nullptr) atomicCAS(status, 0, (code & 0xff) | (where << 8));
 }
+
+// Bound on the waits that let copies and MMAs already in flight land after
+// an abort, before a CTA releases its shared and tensor memory.  Fixed and
+// independent of the caller's wait limit: in-flight work finishes in
+// microseconds, and a short caller limit must never free memory that an
+// asynchronous copy may still write.
+constexpr uint64_t kDrainWaitNs = 200000000ull;  // 200 ms
 
 }  // namespace g3

@@ -34,7 +34,7 @@ def lib_path():
 def test_header_declares_the_abi():
     names = _declared_functions()
     for want in ("gemm_f32", "gemm_bf16", "gemm_bf16_f32out", "gemm_get_last_error",
-                 "gemm_device_status", "gemm_bf16_swiglu", "gemm_probe_fp32_fma"):
+                 "gemm_device_status", "gemm_bf16_swiglu", "gemm_test_stall"):
         assert want in names
 
 
@@ -60,7 +60,7 @@ def test_header_is_valid_c(tmp_path):
     if shutil.which("gcc") is None:
         pytest.skip("gcc unavailable")
     src = tmp_path / "use.c"
-    src.write_text('#include "gb300gemm.h"\n#include "gb300gemm_probe.h"\n'
+    src.write_text('#include "gb300gemm.h"\n'
                    'int main(void){ return gemm_get_last_error() == 0; }\n')
     r = subprocess.run(["gcc", "-std=c99", "-Wall", "-fsyntax-only",
                         "-I", os.path.join(ROOT, "include"), "-I", "/usr/local/cuda/include", str(src)],

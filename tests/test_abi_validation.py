@@ -85,3 +85,24 @@ NO_OPS = [
 @pytest.mark.parametrize("fn,args", NO_OPS)
 def test_empty_calls_are_no_ops(g, fn, args):
     getattr(g, fn)(*args)   # no GPU here: any device access would raise
+
+
+def test_wait_limit_is_clamped(g):
+    # 1 ms .. 10 s, 0 restores the default; outside the range is refused and
+    # leaves the limit as it was
+    for bad in (1, 999_999, 10_000_000_001, (1 << 64) - 1):
+        with pytest.raises(g.GemmError) as e:
+            g.set_wait_timeout_ns(bad)
+        assert e.value.code == g.GEMM_ERR_INVALID_ARG
+        assert "outside" in str(e.value)
+    for ok in (1_000_000, 2_500_000, 10_000_000_000, 0):
+        g.set_wait_timeout_ns(ok)
+
+
+def test_stall_hook_validation(g):
+    for bad in (-1, 2):
+        with pytest.raises(g.GemmError) as e:
+            g.test_stall(bad)
+        assert e.value.code == g.GEMM_ERR_INVALID_ARG
+    g.test_stall(1)
+    g.test_stall(0)

@@ -106,7 +106,7 @@ def test_fp32_4096_full_size_sampled(cuda_lib):
     gen = np.random.default_rng(11)
     rows = np.sort(gen.choice(4096, 24, replace=False))
     cols = np.sort(gen.choice(4096, 24, replace=False))
-    sampled_check(A, B, C, c.A, c.B, c.C0, 1.5, 0.5, oracle.TOL_F32, rows, cols)
+    sampled_check(A, B, C, c.A, c.B, c.C0, 1.5, 0.5, oracle.TOL_F32, rows, cols, strict=True)
 
 
 @pytest.mark.parametrize("M,N,K,pad", [(1024, 1024, 1024, (0, 0, 0)), (2560, 2048, 1024, (0, 0, 0)),
@@ -288,7 +288,7 @@ def test_bf16_tc_pair_8192_sampled(cuda_lib, out):
     rows = np.sort(gen.choice(8192, 12, replace=False))
     cols = np.sort(gen.choice(8192, 12, replace=False))
     tol = oracle.TOL_BF16_OUT if out == BF16 else oracle.TOL_BF16_F32OUT
-    sampled_check(A, B, C, c.A, c.B, None, 1.0, 0.0, tol, rows, cols)
+    sampled_check(A, B, C, c.A, c.B, None, 1.0, 0.0, tol, rows, cols, strict=True)
 
 
 def test_bf16_tc_tile_width_choice(cuda_lib):
@@ -360,7 +360,7 @@ def test_bf16_square_full_size_sampled(cuda_lib, n, out):
     rows = np.sort(gen.choice(n, 16, replace=False))
     cols = np.sort(gen.choice(n, 16, replace=False))
     tol = oracle.TOL_BF16_OUT if out == BF16 else oracle.TOL_BF16_F32OUT
-    sampled_check(A, B, C, c.A, c.B, None, 1.0, 0.0, tol, rows, cols)
+    sampled_check(A, B, C, c.A, c.B, None, 1.0, 0.0, tol, rows, cols, strict=True)
 
 
 @pytest.mark.parametrize("w", ["qkv", "o", "gate", "down", "lm"])
@@ -373,7 +373,8 @@ def test_prefill_full_size_sampled(cuda_lib, w):
     gen = np.random.default_rng(3)
     rows = np.sort(gen.choice(c.spec.M, 8, replace=False))
     cols = np.sort(gen.choice(c.spec.N, 8, replace=False))
-    sampled_check(A, B, C, c.A, c.B, None, 1.0, 0.0, oracle.TOL_BF16_OUT, rows, cols)
+    sampled_check(A, B, C, c.A, c.B, None, 1.0, 0.0, oracle.TOL_BF16_OUT, rows, cols,
+                  strict=True)
 
 
 # ------------------------------------------------------------------ skinny split-K path
