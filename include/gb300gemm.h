@@ -251,8 +251,9 @@ int gemm_int4_repack(const uint8_t* q, int K, int N, int ldq, uint8_t* qk, cudaS
  * is in fp32 (running maximum and sum), P is rounded to bf16 for the second
  * product, and O is rounded once to bf16.  The fast path (tcgen05) needs
  * D = 64 or 128 and 16-byte-aligned tensors.  Other calls run a
- * one-block-per-row kernel, for Sk up to about 58,000.  Errors and
- * asynchrony are as for the GEMM entry points.
+ * one-block-per-row kernel, for Sk up to about 58,000.  B * Hq above 65535
+ * returns GEMM_ERR_UNSUPPORTED (one grid row per batch and head).  Errors
+ * and asynchrony are as for the GEMM entry points.
  */
 int gemm_attention(int B, int Hq, int Hkv, int Sq, int Sk, int D, const gemm_bf16_t* Q, const gemm_bf16_t* K,
                    const gemm_bf16_t* V, gemm_bf16_t* O, float scale, int causal, cudaStream_t stream);
@@ -307,15 +308,19 @@ int gemm_force_path(int path);
 int gemm_last_path(void);
 
 /*
- * Pin the C tile width of the tensor-core kernel for later calls on this host
- * thread: 128, 192, 224 or 256 columns (tiles are 128 rows high); 0 restores
- * the automatic choice, which minimises the work of the last partial wave of
- * tiles over the SMs.  Other values return GEMM_ERR_INVALID_ARG.  For A/B
+ * Pin the C tile width for later calls on this host thread: 128, 192, 224
+ * or 256 columns (tiles are 128 rows high); 0 restores the automatic choice,
+ * which minimises the work of the last partial wave of tiles over the SMs.
+ * The tensor-core kernel takes every width; the FP32 SIMT kernel takes 128
+ * (8 x 8 register tiles, two CTAs per SM) or 256 (8 x 16 register tiles, one
+ * CTA per SM), and an FP32 call with another forced width returns
+ * GEMM_ERR_UNSUPPORTED.  Other values return GEMM_ERR_INVALID_ARG.  For A/B
  * measurements and tests.
  */
 int gemm_force_tile_n(int bn);
 
-/* Tile width the last tensor-core call on this host thread used (0 if none). */
+/* Tile width the last tensor-core or FP32 SIMT call on this host thread used
+ * (0 if none). */
 int gemm_last_tile_n(void);
 
 /*
@@ -337,15 +342,15 @@ int gemm_last_tc_pair(void);
  * Allow (1, the default) or forbid (0), for later calls on this host thread,
  * that the tiles of a partial last wave run split: the CTA-pair kernel runs
  * each as two half-width tiles on otherwise idle pairs; the FP32 SIMT kernel
- * runs them as a second launch in which a cluster of four CTAs shares each
+ * runs them as a second launch in which a cluster of CTAs shares each
  * tile's K range (partial sums added in rank order, in distributed shared
- * memory).  For A/B measurements and tests.
+ * memory; clusters of two or four).  For A/B measurements and tests.
  */
 int gemm_force_split_tiles(int enable);
 
 /* For the last call on this host thread: the number of CTAs that shared the
- * K range of one C tile (the decode kernels' cluster split, or 4 when the FP32
- * SIMT kernel split its partial last wave), 1 if none did. */
+ * K range of one C tile (the decode kernels' cluster split, or 2 or 4 when the
+ * FP32 SIMT kernel split its partial last wave), 1 if none did. */
 int gemm_last_k_split(void);
 
 /*

@@ -45,8 +45,8 @@ EXPORTS = ("gemm_f32", "gemm_bf16", "gemm_bf16_f32out", "gemm_f32_ex", "gemm_bf1
            "gemm_int4_repack", "gemm_w4_packed_bytes", "gemm_attention", "gemm_get_last_error",
            "gemm_device_status", "gemm_force_path", "gemm_last_path", "gemm_force_tile_n",
            "gemm_last_tile_n", "gemm_force_tc_pair", "gemm_last_tc_pair", "gemm_force_split_tiles",
-           "gemm_last_k_split", "gemm_set_wait_timeout_ns", "gemm_selftest_wait_timeout",
-           "gemm_test_stall")
+           "gemm_last_k_split", "gemm_set_wait_timeout_ns",
+           "gemm_selftest_wait_timeout", "gemm_test_stall")
 
 _lib = None
 _lock = threading.Lock()

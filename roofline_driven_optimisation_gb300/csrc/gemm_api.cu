@@ -291,15 +291,23 @@ int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int 
     case GEMM_PATH_GENERIC:
       err = launch_generic(a, stream);
       break;
-    case GEMM_PATH_F32_SIMT:
+    case GEMM_PATH_F32_SIMT: {
+      // forced tile widths: 128 -> 8 x 8 register tiles, 256 -> 8 x 16
+      if (t_forced_bn != 0 && t_forced_bn != kSimtBN8 && t_forced_bn != kSimtBN16)
+        return fail(GEMM_ERR_UNSUPPORTED, "FP32 tiles are 128 or 256 wide, not %d", t_forced_bn);
+      SimtPlan plan;
+      const int forced_tn = t_forced_bn == kSimtBN16 ? 16 : t_forced_bn == kSimtBN8 ? 8 : 0;
+      if ((err = plan_f32_simt(M, N, K, dev->num_sms, forced_tn, &plan)) != cudaSuccess) break;
       if ((rc = make_map(A, K, M, (uint64_t)lda * 4, kSimtBK, kSimtBM, CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                          CU_TENSOR_MAP_SWIZZLE_64B, &mA)) != GEMM_OK)
         return rc;
-      if ((rc = make_map(B, N, K, (uint64_t)ldb * 4, kSimtBN, kSimtBK, CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                         CU_TENSOR_MAP_SWIZZLE_NONE, &mB)) != GEMM_OK)
+      if ((rc = make_map(B, N, K, (uint64_t)ldb * 4, (uint32_t)(16 * plan.tn), kSimtBK,
+                         CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_NONE, &mB)) != GEMM_OK)
         return rc;
-      err = launch_f32_simt(a, mA, mB, dev->num_sms, stream, &t_last_k_split);
+      err = launch_f32_simt(a, mA, mB, plan, dev->num_sms, stream, &t_last_k_split);
+      if (err == cudaSuccess) t_last_bn = 16 * plan.tn;
       break;
+    }
     case GEMM_PATH_BF16_TC:
       if (in == Elem::FP8) {
         if ((rc = make_map(A, K, M, (uint64_t)lda, kF8BK, kTcBM, CU_TENSOR_MAP_DATA_TYPE_UINT8,
@@ -480,6 +488,9 @@ int attention(int B, int Hq, int Hkv, int Sq, int Sk, int D, const void* Q, cons
     return fail(GEMM_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
   if (!(scale >= 0.f) || !std::isfinite(scale)) return fail(GEMM_ERR_INVALID_ARG, "bad scale");
   if (B == 0 || Hq == 0 || Sq == 0) return GEMM_OK;
+  // one grid row per (batch, head): the grid's y extent is at most 65535
+  if ((long long)B * Hq > 65535)
+    return fail(GEMM_ERR_UNSUPPORTED, "B*Hq = %lld exceeds 65535 (batch x heads)", (long long)B * Hq);
   if (Q == nullptr || O == nullptr || (Sk > 0 && (K == nullptr || V == nullptr)))
     return fail(GEMM_ERR_INVALID_ARG, "Q, K, V or O is NULL");
   if ((reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) | reinterpret_cast<uintptr_t>(V) |

@@ -3,36 +3,52 @@
 // FP32 has no dense tensor-core route, so this path is the three-level tiling
 // of "CUDA 算子工程 ch.10 朴素 GEMM 与 Roofline 分析", section 10.4, done with
 // FFMA instead of MMA:
-//   * block tile 128 x 128 (section 10.4.1: each K column of A and B tile,
-//     256 floats, feeds 16384 FMAs, 64x reuse), K-slices of 16;
-//   * warp tile 64 x 32 (10.4.1: about 21x reuse from shared memory);
-//   * register tile 8 x 8 per thread (10.4.1: every loaded element used 8x;
-//     section 10.6 is the 4 x 4 version of the same idea), accumulated with
-//     the packed fma.rn.f32x2 (two IEEE fp32 FMAs per instruction), so the
-//     FMA pipe, not instruction issue, is the limit.
-// The K-slices stream through a 5-stage shared-memory ring filled by TMA
-// ("Kernel 性能从何而来", section "优化阶梯": TMA-backed loads are the first big
-// step).  A slot is handed to the eight warps by an mbarrier that the copy
+//   * block tile 128 x BN, K-slices of 16 (section 10.4.1: each K column of
+//     the A and B tiles feeds 128 x BN FMAs);
+//   * warp tile 64 x 4*TN (10.4.1: the warp tile's reuse of shared memory);
+//   * register tile 8 x TN per thread (10.4.1: every loaded element is used
+//     TN or 8 times; section 10.6 is the 4 x 4 version of the same idea),
+//     accumulated with the packed fma.rn.f32x2 (two IEEE fp32 FMAs per
+//     instruction).
+// Two register tiles share the code:
+//   TN = 16: 128 x 256 C tiles, one CTA of eight warps per SM, ~200
+//            registers a thread, an 8-stage ring -- the large-shape kernel;
+//   TN = 8:  128 x 128 C tiles, two CTAs per SM at 128 registers, 5 stages --
+//            for shapes whose tile count the wide tiles cover badly.
+// The wide tile is faster because of the register file, not shared memory:
+// each packed FMA reads its accumulator pair, one operand pair and one
+// operand broadcast from a single register, and the issue order keeps the B
+// pair the same over consecutive FMAs (for each B pair, all 8 rows), so only
+// the accumulator and the broadcast A value change from one FMA to the next.
+// A bare copy of the inner loop (shared-memory fragments and FMAs, no TMA)
+// retires 0.78 of the FP32 peak with the old order (for each row, all B
+// pairs) and the 8 x 8 tile, 0.80 with this order, and 0.86 with this order
+// and the 8 x 16 tile, on one GB300; handing the FMA a full A pair instead of
+// a broadcast was slower (0.71).
+//
+// The K-slices stream through a shared-memory ring filled by TMA ("Kernel
+// 性能从何而来", section "优化阶梯": TMA-backed loads are the first big step).
+// A slot is handed to the eight warps by an mbarrier that the copy
 // completes, and handed back by a counter: the last warp to finish with a
 // slot issues its refill, so no warp ever waits for the others to release
 // one (same page, "通过重叠执行减少硬件空闲": keep every unit busy).
 //
 // Shared-memory bank conflicts ("CUDA 算子工程 ch.4 内存层级与代价表", sections
 // 4.3.1-4.3.4): the A tile is stored [m][k] (64 bytes per row) with the TMA
-// 64-byte swizzle, so the eight rows a warp reads with one 128-bit load land
-// on eight disjoint groups of four banks; B is read along n, where a warp
-// needs only 64 contiguous bytes per load.  TMA zero-fills outside the
-// matrix, so ragged M, N, K need no guards in the main loop (the role the
-// bounds checks play in the thread-tile kernel of ch.10, 10.6).
+// 64-byte swizzle, so the eight rows a warp reads with one 64-bit load land
+// on eight disjoint groups of banks; B is read along n, where a warp needs
+// only 64 contiguous bytes per load.  TMA zero-fills outside the matrix, so
+// ragged M, N, K need no guards in the main loop (the role the bounds checks
+// play in the thread-tile kernel of ch.10, 10.6).
 //
 // Waves ("Kernel 性能从何而来", "SM 占用率与资源压力": CTA slots, registers and
-// shared memory bound the CTAs an SM holds): two CTAs fit on an SM, so C
-// tiles run in waves of 2 x SMs, and a partial last wave leaves SMs idle.
-// Its tiles can instead run as a second launch in which a cluster of
-// kTailSplit CTAs shares each tile's K range; the partial sums meet in
-// distributed shared memory (no global workspace) and are added in rank
-// order, so results stay deterministic.  4096^3 on 152 SMs: 1024 tiles are
-// three waves of 304 and 112 tiles, whose wave then holds 448 quarter-tiles.
+// shared memory bound the CTAs an SM holds): C tiles run in waves of
+// CTAs-per-SM x SMs, and a partial last wave leaves SMs idle.  Its tiles can
+// instead run as a second launch in which a cluster of SPLIT CTAs shares each
+// tile's K range; the partial sums meet in distributed shared memory (no
+// global workspace) and are added in rank order, so results stay
+// deterministic.  4096^3 on 152 SMs with 128 x 256 tiles: 512 tiles are
+// three waves of 152 and 56 tiles, which run as 112 half-K tiles.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -47,22 +63,31 @@
 namespace g3 {
 namespace {
 
-constexpr int BM = kSimtBM, BN = kSimtBN, BK = kSimtBK;
-constexpr int STAGES = 5;
-constexpr int A_STAGE_BYTES = BM * BK * 4;  // 8 KB
-constexpr int B_STAGE_BYTES = BK * BN * 4;  // 8 KB
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int BM = kSimtBM, BK = kSimtBK;
 constexpr int COMPUTE_WARPS = 8;
 constexpr int THREADS = COMPUTE_WARPS * 32;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
-static_assert(STAGES * 8 + 16 + 2 * STAGES * 4 <= 128, "barrier area (the stall barrier sits at 128)");
-constexpr int kTailSplit = 4;
-// A split CTA's partial tile, [BM][PART_LD] fp32 over the idle ring: the row
-// pitch of 132 floats puts the eight rows one 128-bit store covers on
-// distinct banks.
-constexpr int PART_LD = BN + 4;
-static_assert(BM * PART_LD * 4 <= STAGES * STAGE_BYTES, "partial tile fits the ring");
-static_assert(BM % kTailSplit == 0 && (BM / kTailSplit) * (BN / 4) % THREADS == 0, "reduce split");
+
+template <int TN_>
+struct SimtCfg {
+  static constexpr int TN = TN_;                 // C columns per thread
+  static_assert(TN == 8 || TN == 16, "register tiles are 8 x 8 or 8 x 16");
+  static constexpr int WN = 4 * TN;              // warp tile width (4 lanes along n)
+  static constexpr int BN = 4 * WN;              // four warps along n
+  static constexpr int CTAS_PER_SM = TN == 8 ? 2 : 1;
+  static constexpr int STAGES = TN == 8 ? 5 : 8;
+  static constexpr int A_STAGE_BYTES = BM * BK * 4;
+  static constexpr int B_STAGE_BYTES = BK * BN * 4;
+  static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+  static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+  static constexpr int SMEM_BYTES = RING_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  // A split CTA's partial tile, [BM][PART_LD] fp32 over the idle ring: a row
+  // pitch of BN + 4 floats puts the eight rows one 128-bit store covers on
+  // distinct banks.
+  static constexpr int PART_LD = BN + 4;
+  static_assert(BM * PART_LD * 4 <= RING_BYTES, "partial tile fits the ring");
+  static_assert(STAGES * 8 + 16 + 2 * STAGES * 4 <= 192, "barrier area (the stall barrier sits at 192)");
+};
+static_assert(SimtCfg<8>::BN == kSimtBN8 && SimtCfg<16>::BN == kSimtBN16, "tile widths");
 
 struct SimtParams {
   GemmArgs a;
@@ -90,9 +115,13 @@ __device__ __forceinline__ uint64_t dup2(float x) {
 }
 
 // d.lo += a.lo * b.lo; d.hi += a.hi * b.hi -- two IEEE fp32 FMAs in one
-// instruction, which halves the FMA issue slots of the outer product.
+// instruction, which halves the FMA issue slots of the outer product.  The
+// product is issued as b * a: the B pair, the same over consecutive FMAs,
+// takes the first multiplicand slot (on GB300: 8192^2 x 4096 0.725 -> 0.730
+// of the FP32 peak on 8 x 8 tiles, unchanged on 8 x 16; an FMA rounds once,
+// so the result is the same bits).
 __device__ __forceinline__ void ffma2(uint64_t& d, uint64_t a, uint64_t b) {
-  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+  asm("fma.rn.f32x2 %0, %2, %1, %0;" : "+l"(d) : "l"(a), "l"(b));
 }
 
 __device__ __forceinline__ float2 unpack2(uint64_t v) {
@@ -133,16 +162,21 @@ __device__ __forceinline__ void store_quad(const GemmArgs& a, int c_vec, long lo
   }
 }
 
+// TN: register-tile width (SimtCfg).
 // EPI: bias and/or activation present (the plain instance has no trace of
 // them, so the common case keeps the main loop's register allocation).
 // SPLIT: CTAs of a cluster that share one C tile's K range (1: a whole tile
 // per CTA); cluster rank r takes the r-th of SPLIT contiguous K ranges.
 // TRIGGER: a split launch of the last wave follows on the stream (the plain
 // instance has no trace of it: its code runs at the original speed).
-template <bool EPI, int SPLIT, bool TRIGGER>
-__global__ void __launch_bounds__(THREADS, 2)
+template <int TN, bool EPI, int SPLIT, bool TRIGGER>
+__global__ void __launch_bounds__(THREADS, SimtCfg<TN>::CTAS_PER_SM)
     sgemm_tma_kernel(const __grid_constant__ CUtensorMap mapA,
                      const __grid_constant__ CUtensorMap mapB, const SimtParams p) {
+  using Cfg = SimtCfg<TN>;
+  constexpr int BN = Cfg::BN, WN = Cfg::WN, STAGES = Cfg::STAGES;
+  constexpr int STAGE_BYTES = Cfg::STAGE_BYTES, A_STAGE_BYTES = Cfg::A_STAGE_BYTES;
+  constexpr int PART_LD = Cfg::PART_LD;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - smem_u32(smem_raw));
@@ -152,7 +186,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   // per slot: warps done with it this round, and copies issued into it so far
   uint32_t* done_cnt = reinterpret_cast<uint32_t*>(bars + STAGES) + 4;
   uint32_t* issue_cnt = done_cnt + STAGES;
-  const uint32_t stall_bar = bar_base + 128u;  // test hook: nothing arrives
+  const uint32_t stall_bar = bar_base + 192u;  // test hook: nothing arrives
   auto full_bar = [&](int s) { return bar_base + 8u * s; };
   auto a_tile = [&](int s) { return base + s * STAGE_BYTES; };
   auto b_tile = [&](int s) { return base + s * STAGE_BYTES + A_STAGE_BYTES; };
@@ -161,10 +195,10 @@ __global__ void __launch_bounds__(THREADS, 2)
   const GemmArgs& a = p.a;
 
   // Grouped raster over C tiles: groups of 16 row-panels, column-panel by
-  // column-panel, so the CTAs in flight at one time (two per SM) cover a
-  // near-square block of C and the A and B panels they share stay in L2
-  // (4096^3: 16 x 19 tiles, 32 MB of A and 38 MB of B; groups of 8 rows
-  // kept all of B in flight and read 19 % more from DRAM).
+  // column-panel, so the CTAs in flight at one time cover a near-square
+  // block of C and the A and B panels they share stay in L2 (4096^3 with
+  // 128 x 128 tiles: 16 x 19 tiles, 32 MB of A and 38 MB of B; groups of 8
+  // rows kept all of B in flight and read 19 % more from DRAM).
   const int tile = SPLIT > 1 ? p.tile_base + (int)(blockIdx.x / SPLIT) : (int)blockIdx.x;
   const int group = 16;
   const int tiles_in_group = group * p.tiles_n;
@@ -211,17 +245,20 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
   }
 
+  // Warp (wm, wn) owns rows 64*wm .. +64 and columns WN*wn .. +WN of the C
+  // tile; lane (tm, tn) owns rows 64*wm + 8*i + tm (i < 8) and the columns
+  // WN*wn + 16*h + 4*tn .. +4 (h < TN/4).
   const int wm = warp / 4, wn = warp % 4;
   const int tm = lane % 8, tn = lane / 8;
   const int sw = (tm >> 1) & 3;                // 64-byte swizzle phase of my rows
   const uint32_t a_row_off = (uint32_t)(wm * 64 + tm) * 64u;
-  const uint32_t b_col_off = (uint32_t)(wn * 32 + tn * 4) * 4u;
-  // acc[i][q] holds C columns (2q, 2q+1) of my 8 columns, row i
-  uint64_t acc[8][4];
+  const uint32_t b_col_off = (uint32_t)(wn * WN + tn * 4) * 4u;
+  // acc[i][q] holds C columns (2q, 2q+1) of my TN columns, row i
+  uint64_t acc[8][TN / 2];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int q = 0; q < 4; ++q) acc[i][q] = 0ull;
+    for (int q = 0; q < TN / 2; ++q) acc[i][q] = 0ull;
 
   bool ok = true;
   int my_k_tiles = k_tiles;
@@ -250,6 +287,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     for (int kp = 0; kp < BK / 2; ++kp) {
       // rows i*8+tm, k = 2kp, 2kp+1: one 8-byte load per row inside the
       // swizzled 16-byte chunk that holds k = 4*(kp/2) .. 4*(kp/2)+3
+      // (loading the next pair's values a step ahead was 2 % slower)
       const uint32_t off = (uint32_t)((((kp >> 1) ^ sw) * 16) + (kp & 1) * 8);
       float2 av[8];
 #pragma unroll
@@ -257,14 +295,27 @@ __global__ void __launch_bounds__(THREADS, 2)
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
         const uint32_t brow = bt + (uint32_t)(kp * 2 + kk) * (BN * 4);
-        uint64_t b[4];
-        lds_pairs(brow, b[0], b[1]);
-        lds_pairs(brow + 64, b[2], b[3]);
+        uint64_t b[TN / 2];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint64_t a2 = dup2(kk == 0 ? av[i].x : av[i].y);
+        for (int h = 0; h < TN / 4; ++h) lds_pairs(brow + h * 64, b[2 * h], b[2 * h + 1]);
+        if constexpr (TN == 8 && EPI) {
+          // rows outer: the 8 x 8 instance with an epilogue would spill at
+          // 128 registers with all eight broadcasts live at once
 #pragma unroll
-          for (int q = 0; q < 4; ++q) ffma2(acc[i][q], a2, b[q]);
+          for (int i = 0; i < 8; ++i) {
+            const uint64_t a2 = dup2(kk == 0 ? av[i].x : av[i].y);
+#pragma unroll
+            for (int q = 0; q < TN / 2; ++q) ffma2(acc[i][q], a2, b[q]);
+          }
+        } else {
+          uint64_t a2[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) a2[i] = dup2(kk == 0 ? av[i].x : av[i].y);
+          // B pair outer, rows inner: consecutive FMAs share the B operand
+#pragma unroll
+          for (int q = 0; q < TN / 2; ++q)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ffma2(acc[i][q], a2[i], b[q]);
         }
       }
     }
@@ -299,41 +350,16 @@ __global__ void __launch_bounds__(THREADS, 2)
   if constexpr (SPLIT == 1) {
     if (ok) {
       // ---------------------------------------------------------- epilogue
-      float* C = static_cast<float*>(a.C);
-      const bool beta_nz = a.beta != 0.f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const long long m = (long long)m0 + wm * 64 + i * 8 + tm;
         if (m >= a.M) continue;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const long long n = (long long)n0 + wn * 32 + h * 16 + tn * 4;
-          float* cp = C + m * a.ldc + n;
+        for (int h = 0; h < TN / 4; ++h) {
+          const long long n = (long long)n0 + wn * WN + h * 16 + tn * 4;
           const float2 lo = unpack2(acc[i][2 * h]), hi = unpack2(acc[i][2 * h + 1]);
           float v[4] = {a.alpha * lo.x, a.alpha * lo.y, a.alpha * hi.x, a.alpha * hi.y};
-          if (p.c_vec && n + 3 < a.N) {
-            if (beta_nz) {
-              const float4 c = *reinterpret_cast<const float4*>(cp);
-              v[0] = fmaf(a.beta, c.x, v[0]);
-              v[1] = fmaf(a.beta, c.y, v[1]);
-              v[2] = fmaf(a.beta, c.z, v[2]);
-              v[3] = fmaf(a.beta, c.w, v[3]);
-            }
-            if (EPI) {
-#pragma unroll
-              for (int j = 0; j < 4; ++j) v[j] = finish(a, v[j], n + j);
-            }
-            *reinterpret_cast<float4*>(cp) = make_float4(v[0], v[1], v[2], v[3]);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              if (n + j < a.N) {
-                float r = v[j];
-                if (beta_nz) r = fmaf(a.beta, cp[j], r);
-                cp[j] = EPI ? finish(a, r, n + j) : r;
-              }
-            }
-          }
+          store_quad<EPI>(a, p.c_vec, m, n, v);
         }
       }
     }
@@ -345,8 +371,8 @@ __global__ void __launch_bounds__(THREADS, 2)
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int row = wm * 64 + i * 8 + tm, col = wn * 32 + h * 16 + tn * 4;
+        for (int h = 0; h < TN / 4; ++h) {
+          const int row = wm * 64 + i * 8 + tm, col = wn * WN + h * 16 + tn * 4;
           const float2 lo = unpack2(acc[i][2 * h]), hi = unpack2(acc[i][2 * h + 1]);
           *reinterpret_cast<float4*>(base_ptr + ((size_t)row * PART_LD + col) * 4) =
               make_float4(lo.x, lo.y, hi.x, hi.y);
@@ -360,32 +386,38 @@ __global__ void __launch_bounds__(THREADS, 2)
       all_ok &= ld_dsmem_u32(map_to_rank(bar_base + 8u * STAGES, (uint32_t)r)) == 0u;
     if (all_ok) {
       // rank `part` sums rows [part*BM/SPLIT, (part+1)*BM/SPLIT) over the
-      // ranks in order 0..SPLIT-1; a warp covers one row of 128 columns
+      // ranks in order 0..SPLIT-1, in chunks of QC quads per thread (all
+      // of a chunk's loads in flight before the first add)
       constexpr int QUADS = (BM / SPLIT) * (BN / 4) / THREADS;
-      float4 t[QUADS][SPLIT];
+      constexpr int QC = QUADS < 4 ? QUADS : 4;
+      static_assert(QUADS % QC == 0 && (BM / SPLIT) * (BN / 4) % THREADS == 0, "reduce split");
+#pragma unroll 1
+      for (int q0 = 0; q0 < QUADS; q0 += QC) {
+        float4 t[QC][SPLIT];
 #pragma unroll
-      for (int q = 0; q < QUADS; ++q) {
-        const int idx = (int)threadIdx.x + q * THREADS;
-        const int row = part * (BM / SPLIT) + idx / (BN / 4), col = (idx % (BN / 4)) * 4;
-        const uint32_t off = base + (uint32_t)(row * PART_LD + col) * 4u;
+        for (int q = 0; q < QC; ++q) {
+          const int idx = (int)threadIdx.x + (q0 + q) * THREADS;
+          const int row = part * (BM / SPLIT) + idx / (BN / 4), col = (idx % (BN / 4)) * 4;
+          const uint32_t off = base + (uint32_t)(row * PART_LD + col) * 4u;
 #pragma unroll
-        for (int r = 0; r < SPLIT; ++r) t[q][r] = ld_dsmem_f32x4(map_to_rank(off, (uint32_t)r));
-      }
-#pragma unroll
-      for (int q = 0; q < QUADS; ++q) {
-        const int idx = (int)threadIdx.x + q * THREADS;
-        const long long m = (long long)m0 + part * (BM / SPLIT) + idx / (BN / 4);
-        const long long n = (long long)n0 + (idx % (BN / 4)) * 4;
-        float4 sum = t[q][0];
-#pragma unroll
-        for (int r = 1; r < SPLIT; ++r) {
-          sum.x += t[q][r].x;
-          sum.y += t[q][r].y;
-          sum.z += t[q][r].z;
-          sum.w += t[q][r].w;
+          for (int r = 0; r < SPLIT; ++r) t[q][r] = ld_dsmem_f32x4(map_to_rank(off, (uint32_t)r));
         }
-        float v[4] = {a.alpha * sum.x, a.alpha * sum.y, a.alpha * sum.z, a.alpha * sum.w};
-        if (m < a.M) store_quad<EPI>(a, p.c_vec, m, n, v);
+#pragma unroll
+        for (int q = 0; q < QC; ++q) {
+          const int idx = (int)threadIdx.x + (q0 + q) * THREADS;
+          const long long m = (long long)m0 + part * (BM / SPLIT) + idx / (BN / 4);
+          const long long n = (long long)n0 + (idx % (BN / 4)) * 4;
+          float4 sum = t[q][0];
+#pragma unroll
+          for (int r = 1; r < SPLIT; ++r) {
+            sum.x += t[q][r].x;
+            sum.y += t[q][r].y;
+            sum.z += t[q][r].z;
+            sum.w += t[q][r].w;
+          }
+          float v[4] = {a.alpha * sum.x, a.alpha * sum.y, a.alpha * sum.z, a.alpha * sum.w};
+          if (m < a.M) store_quad<EPI>(a, p.c_vec, m, n, v);
+        }
       }
     }
     cluster_sync();  // no rank leaves while another still reads its partial
@@ -396,39 +428,76 @@ __global__ void __launch_bounds__(THREADS, 2)
   __syncthreads();
 }
 
-}  // namespace
-
-namespace {
-
-struct SplitLaunchInfo {
-  std::atomic<bool> ready{false};  // published after max_clusters is set
-  int max_clusters = 0;
+// Resident clusters of 2 and of 4 CTAs of one configuration's split kernel,
+// per device (a GPC whose free CTA slots are not a multiple of the cluster
+// size leaves the rest idle); queried once, the EPI instances having the
+// same resources.
+struct SimtDeviceInfo {
+  std::atomic<bool> ready{false};   // published after the fields below are set
+  int max_clusters2 = 0, max_clusters4 = 0;
 };
 
-template <bool EPI>
-cudaError_t launch_plan(const CUtensorMap* mapA, const CUtensorMap* mapB, SimtParams p,
-                        long long tiles, int num_sms, cudaStream_t s, int* k_split) {
-  static std::atomic<uint64_t> smem_set_whole{0};
-  static SplitLaunchInfo info[64];
-  static std::mutex mu;
-  static std::atomic<uint64_t> smem_set_first{0};
-  auto whole_kernel = sgemm_tma_kernel<EPI, 1, false>;
-  auto first_kernel = sgemm_tma_kernel<EPI, 1, true>;
-  auto split_kernel = sgemm_tma_kernel<EPI, kTailSplit, false>;
-  cudaError_t e = set_smem_once(smem_set_whole, whole_kernel, SMEM_BYTES);
-  if (e == cudaSuccess) e = set_smem_once(smem_set_first, first_kernel, SMEM_BYTES);
+template <int TN, int SPLIT>
+cudaError_t query_clusters(int num_sms, int* n) {
+  using Cfg = SimtCfg<TN>;
+  auto k = sgemm_tma_kernel<TN, false, SPLIT, false>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = SPLIT;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3((unsigned)(SPLIT * Cfg::CTAS_PER_SM * num_sms), 1, 1);
+  return cudaOccupancyMaxActiveClusters(n, k, &cfg);
+}
 
-  const long long slots = 2LL * num_sms;
-  const long long rest = tiles % slots, whole = tiles - rest;
-  const int k_tiles = (p.a.K + BK - 1) / BK;
-  // a cheap first test before the occupancy query; plan::simt_split decides
-  bool split = split_tiles_enabled() && rest > 0 && k_tiles >= kTailSplit * 2 * STAGES;
+template <int TN>
+cudaError_t device_clusters(int num_sms, int* c2, int* c4) {
+  static SimtDeviceInfo info[64];
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!info[dev].ready.load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!info[dev].ready.load(std::memory_order_relaxed)) {
+      int n2 = 0, n4 = 0;
+      if constexpr (TN == 16) {  // only the wide tile has a split-2 instance
+        if ((e = query_clusters<TN, 2>(num_sms, &n2)) != cudaSuccess) return e;
+      }
+      if ((e = query_clusters<TN, 4>(num_sms, &n4)) != cudaSuccess) return e;
+      info[dev].max_clusters2 = n2;
+      info[dev].max_clusters4 = n4;
+      info[dev].ready.store(true, std::memory_order_release);
+    }
+  }
+  *c2 = info[dev].max_clusters2;
+  *c4 = info[dev].max_clusters4;
+  return cudaSuccess;
+}
 
+// The split launch: `units` C tiles (the tiles past the last whole wave),
+// each K-split over a cluster of SPLIT CTAs.  overlap: a first launch
+// precedes it on the stream and triggers it early.
+template <int TN, bool EPI, int SPLIT>
+cudaError_t launch_split(const CUtensorMap* mapA, const CUtensorMap* mapB, const SimtParams& p,
+                         long long units, bool overlap, cudaStream_t s) {
+  using Cfg = SimtCfg<TN>;
+  static std::atomic<uint64_t> smem_set{0};
+  auto k = sgemm_tma_kernel<TN, EPI, SPLIT, false>;
+  cudaError_t e = set_smem_once(smem_set, k, Cfg::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[3];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kTailSplit;
+  attr[0].val.clusterDim.x = (unsigned)SPLIT;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeClusterSchedulingPolicyPreference;
@@ -436,73 +505,114 @@ cudaError_t launch_plan(const CUtensorMap* mapA, const CUtensorMap* mapB, SimtPa
   attr[2].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[2].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int dev = 0;
-  if (split) {
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!info[dev].ready.load(std::memory_order_acquire)) {
-      std::lock_guard<std::mutex> lock(mu);
-      if (!info[dev].ready.load(std::memory_order_relaxed)) {
-        if ((e = cudaFuncSetAttribute(split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      SMEM_BYTES)) != cudaSuccess)
-          return e;
-        // clusters of four resident at once: a GPC whose free CTA slots are
-        // not a multiple of four leaves the rest idle
-        int n = 0;
-        cfg.gridDim = dim3((unsigned)(kTailSplit * num_sms), 1, 1);
-        if ((e = cudaOccupancyMaxActiveClusters(&n, split_kernel, &cfg)) != cudaSuccess) return e;
-        info[dev].max_clusters = n;
-        info[dev].ready.store(true, std::memory_order_release);
-      }
-    }
-    // ten K-slices a rank at least (two rounds of the ring)
-    split = plan::simt_split(tiles, k_tiles, num_sms, info[dev].max_clusters, kTailSplit,
-                             2 * STAGES, true);
-  }
-
-  const long long first = split ? whole : tiles;
-  if (first > 0) {
-    if (split)
-      first_kernel<<<(unsigned)first, THREADS, SMEM_BYTES, s>>>(*mapA, *mapB, p);
-    else
-      whole_kernel<<<(unsigned)first, THREADS, SMEM_BYTES, s>>>(*mapA, *mapB, p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess || !split) return e;
-  }
-  *k_split = kTailSplit;
-  p.tile_base = (int)whole;
-  cfg.gridDim = dim3((unsigned)(rest * kTailSplit), 1, 1);
+  cfg.gridDim = dim3((unsigned)(units * SPLIT), 1, 1);
   // The hardware may place a cluster's CTAs where slots are free (4096^3 on
-  // GB300: 2.352 -> 2.272 ms against the default placement).  Overlap the
-  // first launch's last CTAs only when there is one: otherwise the previous
-  // kernel on the stream may still be writing A, B or C.
-  cfg.numAttrs = first > 0 ? 3 : 2;
-  e = cudaLaunchKernelEx(&cfg, split_kernel, *mapA, *mapB, p);
+  // GB300 with 128 x 128 tiles: 2.352 -> 2.272 ms against the default
+  // placement).  Overlap the first launch's last CTAs only when there is
+  // one: otherwise the previous kernel on the stream may still be writing A,
+  // B or C.
+  cfg.numAttrs = overlap ? 3 : 2;
+  e = cudaLaunchKernelEx(&cfg, k, *mapA, *mapB, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
+template <int TN, bool EPI>
+cudaError_t launch_plan(const CUtensorMap* mapA, const CUtensorMap* mapB, SimtParams p,
+                        long long tiles, const SimtPlan& plan, int num_sms, cudaStream_t s) {
+  using Cfg = SimtCfg<TN>;
+  static std::atomic<uint64_t> smem_whole{0}, smem_first{0};
+  auto whole_kernel = sgemm_tma_kernel<TN, EPI, 1, false>;
+  auto first_kernel = sgemm_tma_kernel<TN, EPI, 1, true>;
+  cudaError_t e = set_smem_once(smem_whole, whole_kernel, Cfg::SMEM_BYTES);
+  if (e == cudaSuccess) e = set_smem_once(smem_first, first_kernel, Cfg::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  if (plan.split == 1) {
+    whole_kernel<<<(unsigned)tiles, THREADS, Cfg::SMEM_BYTES, s>>>(*mapA, *mapB, p);
+    return cudaGetLastError();
+  }
+  const long long slots = (long long)Cfg::CTAS_PER_SM * num_sms;
+  const long long rest = tiles % slots, whole = tiles - rest;
+  if (rest == 0) return cudaErrorInvalidValue;  // the plan splits only a partial wave
+  if (whole > 0) {
+    first_kernel<<<(unsigned)whole, THREADS, Cfg::SMEM_BYTES, s>>>(*mapA, *mapB, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  p.tile_base = (int)whole;
+  if constexpr (TN == 16) {  // only the wide tile has a split-2 instance
+    if (plan.split == 2) return launch_split<TN, EPI, 2>(mapA, mapB, p, rest, whole > 0, s);
+  }
+  if (plan.split == 4) return launch_split<TN, EPI, 4>(mapA, mapB, p, rest, whole > 0, s);
+  return cudaErrorInvalidValue;
+}
+
+// The wave model's estimate for one configuration (plan::simt_option), after
+// the occupancy queries it needs.
+template <int TN>
+cudaError_t option_for(long long tiles, int k_tiles, int num_sms, bool split_allowed,
+                       plan::SimtOption* o) {
+  using Cfg = SimtCfg<TN>;
+  int c2 = 0, c4 = 0;
+  const long long slots = (long long)Cfg::CTAS_PER_SM * num_sms;
+  const int min_k_tiles = 2 * Cfg::STAGES;  // two rounds of the ring per rank
+  // a cheap first test before the occupancy query
+  if (split_allowed && tiles % slots != 0 && k_tiles >= 2 * min_k_tiles) {
+    const cudaError_t e = device_clusters<TN>(num_sms, &c2, &c4);
+    if (e != cudaSuccess) return e;
+  }
+  *o = plan::simt_option(TN, tiles, k_tiles, num_sms, c2, c4, min_k_tiles, split_allowed);
+  return cudaSuccess;
+}
+
 }  // namespace
 
+int plan_f32_simt(int M, int N, int K, int num_sms, int forced_tn, SimtPlan* out) {
+  const long long tiles_m = (M + BM - 1) / BM;
+  const long long tiles8 = tiles_m * ((N + kSimtBN8 - 1) / kSimtBN8);
+  const long long tiles16 = tiles_m * ((N + kSimtBN16 - 1) / kSimtBN16);
+  const int k_tiles = (K + BK - 1) / BK;
+  const bool allowed = split_tiles_enabled();
+  plan::SimtOption o8{}, o16{};
+  cudaError_t e;
+  if (forced_tn != 16 && (e = option_for<8>(tiles8, k_tiles, num_sms, allowed, &o8)) != cudaSuccess) return e;
+  if (forced_tn != 8 && (e = option_for<16>(tiles16, k_tiles, num_sms, allowed, &o16)) != cudaSuccess)
+    return e;
+  // the wide tiles must win by the model's margin of error (2560 x 2048 x
+  // 1024 on GB300: estimated 4 % faster wide, measured 7 % slower)
+  const bool wide = forced_tn == 16 || (forced_tn != 8 && o16.time < plan::kSimtWideMargin * o8.time);
+  out->tn = wide ? 16 : 8;
+  out->split = wide ? o16.split : o8.split;
+  return cudaSuccess;
+}
+
 int launch_f32_simt(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
-                    int num_sms, cudaStream_t s, int* k_split) {
+                    const SimtPlan& plan, int num_sms, cudaStream_t s, int* k_split) {
   *k_split = 1;
   SimtParams p;
   p.a = a;
+  const int bn = plan.tn == 16 ? kSimtBN16 : kSimtBN8;
   p.tiles_m = (a.M + BM - 1) / BM;
-  p.tiles_n = (a.N + BN - 1) / BN;
+  p.tiles_n = (a.N + bn - 1) / bn;
   p.c_vec = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && (a.ldc % 4) == 0) ? 1 : 0;
   p.tile_base = 0;
   const long long tiles = (long long)p.tiles_m * p.tiles_n;
   if (tiles <= 0) return cudaSuccess;
-  if (tiles * kTailSplit > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  if (a.bias != nullptr || a.act != kActNone)
-    return launch_plan<true>(mapA, mapB, p, tiles, num_sms, s, k_split);
-  return launch_plan<false>(mapA, mapB, p, tiles, num_sms, s, k_split);
+  if (tiles * 4 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const bool epi = a.bias != nullptr || a.act != kActNone;
+  cudaError_t e;
+  if (plan.tn == 16)
+    e = epi ? launch_plan<16, true>(mapA, mapB, p, tiles, plan, num_sms, s)
+            : launch_plan<16, false>(mapA, mapB, p, tiles, plan, num_sms, s);
+  else if (plan.tn == 8)
+    e = epi ? launch_plan<8, true>(mapA, mapB, p, tiles, plan, num_sms, s)
+            : launch_plan<8, false>(mapA, mapB, p, tiles, plan, num_sms, s);
+  else
+    return cudaErrorInvalidValue;
+  if (e == cudaSuccess) *k_split = plan.split;
+  return e;
 }
 
 }  // namespace g3

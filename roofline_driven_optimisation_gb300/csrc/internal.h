@@ -86,12 +86,19 @@ enum WaitSite : int {
 int launch_generic(const GemmArgs& a, cudaStream_t s);
 
 // FP32 SIMT kernel: TMA tiles of A (16 k x 128 m, 64-byte swizzle) and
-// B (128 n x 16 k).
-// The tiles of a partial last wave may run as a second launch, K split over
-// clusters of four CTAs (*k_split = 4; 1 otherwise).
+// B (bn n x 16 k), bn = 128 (8 x 8 register tiles, two CTAs per SM) or 256
+// (8 x 16 register tiles, one CTA per SM).  plan_f32_simt picks the tile
+// width (forced_tn 8 or 16 pins it, 0 lets the wave model choose) and
+// whether the tiles of a partial last wave run as a second launch, K split
+// over clusters of `split` CTAs (*k_split receives it; 1 otherwise).
+struct SimtPlan {
+  int tn = 8;     // register-tile width: 8 or 16 (C tiles of 128 x 16*tn)
+  int split = 1;  // 1, 2 (wide only) or 4
+};
+int plan_f32_simt(int M, int N, int K, int num_sms, int forced_tn, SimtPlan* out);
 int launch_f32_simt(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
-                    int num_sms, cudaStream_t s, int* k_split);
-constexpr int kSimtBM = 128, kSimtBN = 128, kSimtBK = 16;
+                    const SimtPlan& plan, int num_sms, cudaStream_t s, int* k_split);
+constexpr int kSimtBM = 128, kSimtBK = 16, kSimtBN8 = 128, kSimtBN16 = 256;
 
 // BF16 tcgen05 kernel: TMA tiles of A (64 k x 128 m) and B (64 n x 64 k),
 // 128-byte swizzle; C tiles of 128 x bn with bn from choose_tc_bn().

@@ -93,6 +93,82 @@ inline bool simt_split(long long tiles, int k_tiles, int num_sms, int max_cluste
          rounds_time(rest, 1.0, slots, num_sms);
 }
 
+// FP32 SIMT kernel: one candidate configuration and its estimated time.
+// `time` is in units of one 128 x 128 x K tile computed by a whole SM at the
+// narrow kernel's rate; `split` is 1 (whole tiles only) or the cluster size
+// that shares the K range of each tile past the last whole wave.
+struct SimtOption {
+  double time = 1e300;
+  int split = 1;
+};
+
+// Per-SM rate of the wide configuration (8 x 16 register tiles, 128 x 256 C
+// tiles, one CTA per SM) relative to the narrow one (8 x 8, 128 x 128, two
+// CTAs per SM): the bare inner loops retire 0.816 and 0.759 of the FP32 peak
+// on one GB300.
+constexpr double kSimtWideRate = 1.075;
+// The wide configuration is chosen only when its estimate is below this
+// fraction of the narrow one (the estimates' error at short K: 2560 x 2048 x
+// 1024 modelled 4 % faster on wide tiles, measured 7 % slower).
+constexpr double kSimtWideMargin = 0.97;
+
+// The estimate for register-tile width `tn` (8: narrow, 16: wide) with
+// `tiles` C tiles of that configuration.  max_clusters2/4: clusters of 2 and
+// of 4 CTAs of its split kernel resident at once (0: none, or not queried);
+// each rank needs at least `min_k_tiles` K-slices.
+//   narrow: a wave is two tiles per SM; the partial last wave either runs
+//           whole (rounds_time: about 0.53 of a wave when it is at most one
+//           CTA per SM) or K-split over clusters of four, as simt_split
+//           decides (its tenth-of-a-tile margin is part of the decision, not
+//           of the estimate);
+//   wide:   a wave is one tile per SM and a partial round costs a whole one;
+//           the partial last wave either runs whole or K-split over clusters
+//           of 2 or 4 (the rounds of 1/s tiles that the resident clusters
+//           need, plus 0.02 of a tile for the reduction).
+// Measured on one GB300 (waves of 0.699 ms narrow and 0.655 ms wide at K =
+// 4096): 4096^3 3.37 narrow waves split / 3.49 wide waves split in two
+// (estimates 3.38 / 3.52); 2048^2 x 4096 0.874 narrow waves split / 1.01
+// wide waves whole (0.88 / 1.0).
+inline SimtOption simt_option(int tn, long long tiles, int k_tiles, int num_sms, int max_clusters2,
+                              int max_clusters4, int min_k_tiles, bool split_allowed) {
+  SimtOption o;
+  if (tiles <= 0 || num_sms <= 0) {
+    o.time = 0.0;
+    return o;
+  }
+  if (tn == 8) {
+    const long long slots = 2LL * num_sms;
+    const double wave = 2.0;  // two tiles per SM
+    if (simt_split(tiles, k_tiles, num_sms, max_clusters4, 4, min_k_tiles, split_allowed)) {
+      const long long rest = tiles % slots;
+      o.split = 4;
+      o.time = wave * ((double)(tiles / slots) +
+                       rounds_time(rest * 4, 0.25, 4LL * max_clusters4, num_sms));
+    } else {
+      o.time = wave * rounds_time(tiles, 1.0, slots, num_sms);
+    }
+    return o;
+  }
+  const long long slots = num_sms;
+  const double wave = 2.0 / kSimtWideRate;  // one 128 x 256 tile per SM
+  const long long whole = tiles / slots, rest = tiles % slots;
+  o.time = wave * (double)(whole + (rest > 0 ? 1 : 0));
+  if (!split_allowed || rest == 0) return o;
+  static const int splits[] = {2, 4};
+  for (int split : splits) {
+    const int clusters = split == 2 ? max_clusters2 : max_clusters4;
+    if (clusters <= 0 || k_tiles < split * min_k_tiles) continue;
+    const long long per_round = (long long)split * clusters;
+    const long long rounds = (rest * split + per_round - 1) / per_round;
+    const double t = wave * ((double)whole + (double)rounds / split + 0.02);
+    if (t < o.time) {
+      o.time = t;
+      o.split = split;
+    }
+  }
+  return o;
+}
+
 // Decode kernels: CTAs of a cluster that share one column slab's K range.  The
 // largest power of two up to `max_split` whose grid still fits two CTAs per
 // SM, and no more than the K units there are; `forced` (1, 2, 4 or 8)

@@ -5,6 +5,7 @@
 //   bn M N sms                                  -> "bn"
 //   simt tiles k_tiles sms max_clusters split min_k_tiles split_allowed -> 0 or 1
 //   cluster tiles_n k_units sms forced max_split -> split
+//   simtopt tn tiles k_tiles sms clusters2 clusters4 min_k_tiles split_allowed -> "time split"
 #include <cstdio>
 #include <cstring>
 
@@ -30,6 +31,15 @@ int main() {
         return 2;
       std::printf("%d\n",
                   g3::plan::simt_split(tiles, k_tiles, sms, clusters, split, min_k, allowed != 0) ? 1 : 0);
+    } else if (!std::strcmp(op, "simtopt")) {
+      long long tiles;
+      int tn, k_tiles, sms, c2, c4, min_k, allowed;
+      if (std::scanf("%d %lld %d %d %d %d %d %d", &tn, &tiles, &k_tiles, &sms, &c2, &c4, &min_k,
+                     &allowed) != 8)
+        return 2;
+      const g3::plan::SimtOption o =
+          g3::plan::simt_option(tn, tiles, k_tiles, sms, c2, c4, min_k, allowed != 0);
+      std::printf("%.4f %d\n", o.time, o.split);
     } else if (!std::strcmp(op, "cluster")) {
       int tiles_n, k_units, sms, forced, max_split;
       if (std::scanf("%d %d %d %d %d", &tiles_n, &k_units, &sms, &forced, &max_split) != 5) return 2;

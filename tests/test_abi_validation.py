@@ -61,6 +61,8 @@ CASES = [
      "bad scale"),
     ("gemm_attention", (1, 4, 4, 16, 16, 64, P + 1, P, P, P, 0.0, 0, S), "GEMM_ERR_MISALIGNED",
      "aligned"),
+    ("gemm_attention", (2048, 64, 8, 16, 16, 64, P, P, P, P, 0.0, 0, S), "GEMM_ERR_UNSUPPORTED",
+     "exceeds 65535"),
 ]
 
 

@@ -33,6 +33,7 @@ def short_limit(cuda_lib):
         g.test_stall(0)
         g.set_wait_timeout_ns(0)
         g.force_tc_pair(0)
+        g.force_tile_n(0)
 
 
 def stalled_call(A, B, C0, alpha, beta, out):
@@ -72,12 +73,17 @@ def test_skinny_split_abort_then_recovers(short_limit):
     assert path == g.PATH_SKINNY and g.last_k_split() > 1
 
 
-@pytest.mark.parametrize("M,N,K", [(300, 260, 1024),     # split launch only (6 tiles)
-                                   (2560, 2048, 1024)])  # whole wave, then the split launch
-def test_simt_split_abort_then_recovers(short_limit, M, N, K):
+@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("M,N,K", [(300, 260, 1024),     # split launch only (6 or 3 tiles)
+                                   (2560, 2048, 1024)])  # whole waves, then the split launch
+def test_simt_split_abort_then_recovers(short_limit, bn, M, N, K):
     c = inputs.make("fp32_4096", M=M, N=N, K=K)
-    status, where, (path, split, _) = stalled_call(c.A, c.B, c.C0, 1.5, 0.5, F32)
-    assert path == g.PATH_F32_SIMT and split == 4
-    assert (status, where) == (g.GEMM_ERR_DEVICE_TIMEOUT, SITE_SIMT_CONSUMER)
-    err, path = check(c.A, c.B, c.C0, 1.5, 0.5, F32)
-    assert path == g.PATH_F32_SIMT and g.last_k_split() == 4
+    g.force_tile_n(bn)
+    try:
+        status, where, (path, split, _) = stalled_call(c.A, c.B, c.C0, 1.5, 0.5, F32)
+        assert path == g.PATH_F32_SIMT and split > 1 and g.last_tile_n() == bn
+        assert (status, where) == (g.GEMM_ERR_DEVICE_TIMEOUT, SITE_SIMT_CONSUMER)
+        err, path = check(c.A, c.B, c.C0, 1.5, 0.5, F32)
+        assert path == g.PATH_F32_SIMT and g.last_k_split() > 1
+    finally:
+        g.force_tile_n(0)

@@ -46,19 +46,23 @@ def _run(case, out, alpha, beta, with_bias, act, *, path=None, pair=None, bn=Non
 def test_fp32_simt_and_generic(cuda_lib, act, with_bias):
     c = inputs.make("fp32_4096", M=200, N=264, K=128)
     assert _run(c, F32, 1.5, 0.5, with_bias, act) == g.PATH_F32_SIMT
+    for bn in (128, 256):   # both register tiles
+        assert _run(c, F32, 1.5, 0.5, with_bias, act, bn=bn) == g.PATH_F32_SIMT
     assert _run(c, F32, 1.0, 0.0, with_bias, act, path=g.PATH_GENERIC) == g.PATH_GENERIC
     c2 = inputs.make("fp32_4096", M=70, N=90, K=52)   # N not a multiple of 4: scalar tail
     _run(c2, F32, 1.5, 0.5, with_bias, act)
 
 
 @pytest.mark.parametrize("act", ACTS)
-def test_fp32_split_last_wave(cuda_lib, act):
-    # nine tiles with K = 1024: each tile's K range is split over four CTAs,
-    # and the rank that sums a row block applies beta, bias and activation
+@pytest.mark.parametrize("bn", [128, 256])
+def test_fp32_split_last_wave(cuda_lib, act, bn):
+    # nine (six) tiles with K = 1024: each tile's K range is split over four
+    # (two or four) CTAs, and the rank that sums a row block applies beta,
+    # bias and activation
     c = inputs.make("fp32_4096", M=300, N=264, K=1024)
-    assert _run(c, F32, 1.5, 0.5, True, act) == g.PATH_F32_SIMT
-    assert g.last_k_split() == 4
-    _run(c, F32, 1.0, 0.0, False, act)
+    assert _run(c, F32, 1.5, 0.5, True, act, bn=bn) == g.PATH_F32_SIMT
+    assert g.last_k_split() == 4 if bn == 128 else g.last_k_split() in (2, 4)
+    _run(c, F32, 1.0, 0.0, False, act, bn=bn)
 
 
 @pytest.mark.parametrize("act", ACTS)

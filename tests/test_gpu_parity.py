@@ -45,6 +45,34 @@ def test_fp32_ragged(cuda_lib, M, N, K):
     assert path == expected_path(M, N, K, "f32")
 
 
+@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("M,N,K", [(7, 12, 16), (129, 260, 36), (128, 256, 16), (255, 516, 200),
+                                   (300, 1000, 332), (513, 388, 96), (64, 4100, 20)])
+def test_fp32_each_tile_width(cuda_lib, bn, M, N, K):
+    # 128: 8 x 8 register tiles on 128 x 128 C tiles, two CTAs per SM;
+    # 256: 8 x 16 register tiles on 128 x 256 C tiles, one CTA per SM
+    c = inputs.make("fp32_4096", M=M, N=N, K=K)
+    g.force_tile_n(bn)
+    try:
+        err, path = check(c.A, c.B, c.C0, 1.5, 0.5, F32)
+        assert path == g.PATH_F32_SIMT and g.last_tile_n() == bn
+        err, path = check(c.A, c.B, None, 1.0, 0.0, F32, c_fill=float("nan"))
+        assert g.last_tile_n() == bn
+    finally:
+        g.force_tile_n(0)
+
+
+def test_fp32_forced_widths_other_than_128_and_256_are_refused(cuda_lib):
+    c = inputs.make("fp32_4096", M=64, N=64, K=16)
+    g.force_tile_n(192)
+    try:
+        with pytest.raises(g.GemmError) as e:
+            run_abi(c.A, c.B, None, 1.0, 0.0, F32)
+        assert e.value.code == g.GEMM_ERR_UNSUPPORTED
+    finally:
+        g.force_tile_n(0)
+
+
 @pytest.mark.parametrize("alpha,beta", [(0.0, 0.0), (1.0, 0.0), (-1.0, 0.5), (1.5, 1.0), (1.0, 0.5)])
 def test_fp32_alpha_beta_grid(cuda_lib, alpha, beta):
     c = inputs.make("fp32_4096", M=200, N=160, K=64)
@@ -94,55 +122,113 @@ def test_fp32_forced_generic_matches_oracle(cuda_lib):
     assert path == g.PATH_GENERIC
 
 
-def test_fp32_4096_full_size_sampled(cuda_lib):
+@pytest.mark.parametrize("bn", [0, 128, 256])
+def test_fp32_4096_full_size_sampled(cuda_lib, bn):
+    # bn 0: the dispatcher's choice (the bench's launch configuration)
     c = inputs.make("fp32_4096")
     A, B, C = c.A.cuda(), c.B.cuda(), c.C0.cuda()
-    g.gemm(A, B, C, 1.5, 0.5)
-    torch.cuda.synchronize()
+    g.force_tile_n(bn)
+    try:
+        g.gemm(A, B, C, 1.5, 0.5)
+        torch.cuda.synchronize()
+    finally:
+        g.force_tile_n(0)
     assert g.last_path() == g.PATH_F32_SIMT
-    # 1024 tiles = 3 waves of 304 + 112; whether the 112 split depends on how
-    # many clusters of four fit at once
-    assert g.last_k_split() in (1, 4)
+    assert bn == 0 or g.last_tile_n() == bn
+    # 128-wide: 1024 tiles = 3 waves of 304 + 112; 256-wide: 512 tiles = 3
+    # waves of 152 + 56; whether the rest splits depends on how many clusters
+    # fit at once
+    assert g.last_k_split() in (1, 2, 4)
     gen = np.random.default_rng(11)
     rows = np.sort(gen.choice(4096, 24, replace=False))
     cols = np.sort(gen.choice(4096, 24, replace=False))
     sampled_check(A, B, C, c.A, c.B, c.C0, 1.5, 0.5, oracle.TOL_F32, rows, cols, strict=True)
 
 
+# The splits each width takes for these shapes on GB300 (152 SMs): 128-wide
+# tiles split four ways (at least 64 clusters of four fit at once); 256-wide
+# tiles split two or four ways, four when every rank keeps 16 K-slices.
+WIDE_SPLITS = (2, 4)
+
+
+def _expect_split(bn, split):
+    return split == 4 if bn == 128 else split in WIDE_SPLITS
+
+
+@pytest.mark.parametrize("bn", [128, 256])
 @pytest.mark.parametrize("M,N,K,pad", [(1024, 1024, 1024, (0, 0, 0)), (2560, 2048, 1024, (0, 0, 0)),
                                        (1000, 1004, 1001, (3, 0, 0)), (300, 200, 1000, (0, 0, 0))])
-def test_fp32_split_last_wave(cuda_lib, M, N, K, pad):
-    # 1024^2: 64 tiles, all in the split launch; 2560 x 2048: 320 tiles, the
-    # 16 past two whole waves of 2 x 152 split; 1000 x 1004 x 1001: ragged M,
-    # N and K (63 K-slices, ranks take 15/16/16/16); 300 x 200: six tiles.
-    # Each partial wave holds at most 64 tiles, which the dispatcher splits
-    # whenever at least 64 clusters of four fit at once.
+def test_fp32_split_last_wave(cuda_lib, bn, M, N, K, pad):
+    # 128-wide: 1024^2: 64 tiles, all in the split launch; 2560 x 2048: 320
+    # tiles, the 16 past two whole waves of 2 x 152 split; 1000 x 1004 x 1001:
+    # ragged M, N and K (63 K-slices, ranks take 15/16/16/16); 300 x 200: six
+    # tiles.  256-wide: 32, 160 (8 past one wave of 152), 32 and 3 tiles; 63
+    # K-slices are too few for four ranks of 16, so that shape splits in two.
     c = inputs.make("fp32_4096", M=M, N=N, K=K)
-    err, path = check(c.A, c.B, c.C0, 1.5, 0.5, F32, pad=pad)
-    assert path == g.PATH_F32_SIMT and g.last_k_split() == 4
-    # partial sums are added in rank order: repeated calls give the same bits
-    a = run_abi(c.A, c.B, c.C0, 1.5, 0.5, F32, pad=pad)[0]
-    b = run_abi(c.A, c.B, c.C0, 1.5, 0.5, F32, pad=pad)[0]
-    assert torch.equal(a, b)
-    g.force_split_tiles(0)
+    g.force_tile_n(bn)
     try:
-        check(c.A, c.B, c.C0, 1.5, 0.5, F32, pad=pad)
-        assert g.last_k_split() == 1
+        err, path = check(c.A, c.B, c.C0, 1.5, 0.5, F32, pad=pad)
+        assert path == g.PATH_F32_SIMT and _expect_split(bn, g.last_k_split())
+        if bn == 256 and K == 1001:
+            # no 256-wide four-way split: its ranks would get fewer than 16
+            # K-slices
+            assert g.last_k_split() == 2
+        # partial sums are added in rank order: repeated calls give the same bits
+        a = run_abi(c.A, c.B, c.C0, 1.5, 0.5, F32, pad=pad)[0]
+        b = run_abi(c.A, c.B, c.C0, 1.5, 0.5, F32, pad=pad)[0]
+        assert torch.equal(a, b)
+        g.force_split_tiles(0)
+        try:
+            check(c.A, c.B, c.C0, 1.5, 0.5, F32, pad=pad)
+            assert g.last_k_split() == 1
+        finally:
+            g.force_split_tiles(1)
     finally:
-        g.force_split_tiles(1)
+        g.force_tile_n(0)
 
 
-def test_fp32_split_unaligned_c_and_nan_c(cuda_lib):
+@pytest.mark.parametrize("N", [1024, 1000, 900, 800])
+def test_fp32_wide_tiles_ragged_n_split(cuda_lib, N):
+    # 256-wide tiles with the last column of tiles partly outside C (N = 1000,
+    # 900: the right half holds 232 or 132 columns; 800: 32), every tile in
+    # the split launch (2048 x N: 16 x 4 tiles, fewer than one wave of 152)
+    c = inputs.make("fp32_4096", M=2048, N=N, K=1024)
+    g.force_tile_n(256)
+    try:
+        err, path = check(c.A, c.B, c.C0, 1.5, 0.5, F32)
+        assert path == g.PATH_F32_SIMT and g.last_tile_n() == 256 and g.last_k_split() in (2, 4)
+        err, path = check(c.A, c.B, None, 1.0, 0.0, F32, c_fill=float("nan"), pad=(0, 0, 4))
+    finally:
+        g.force_tile_n(0)
+
+
+def test_fp32_4096_configuration(cuda_lib):
+    # the bench's shape at a shorter K: on 152 SMs the wave model picks the
+    # 256-wide tiles (512 tiles = 3 waves of 152 + 56, the 56 split in two)
+    c = inputs.make("fp32_4096", M=4096, N=4096, K=1024)
+    check(c.A, c.B, c.C0, 1.5, 0.5, F32)
+    assert g.last_path() == g.PATH_F32_SIMT
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert (g.last_tile_n(), g.last_k_split()) == (256, 2)
+
+
+@pytest.mark.parametrize("bn", [128, 256])
+def test_fp32_split_unaligned_c_and_nan_c(cuda_lib, bn):
     # the split epilogue's scalar path (C one element past an aligned base,
     # ldc not a multiple of 4), and beta = 0 over a NaN-filled C
     c = inputs.make("fp32_4096", M=300, N=200, K=1000)
-    err, path = check(c.A, c.B, c.C0, 1.5, 0.5, F32, offset=(0, 0, 1), pad=(0, 0, 3))
-    assert path == g.PATH_F32_SIMT and g.last_k_split() == 4
-    C, _, _ = run_abi(c.A, c.B, None, 1.0, 0.0, F32, c_fill=float("nan"))
-    assert g.last_k_split() == 4 and torch.isfinite(C).all()
+    g.force_tile_n(bn)
+    try:
+        err, path = check(c.A, c.B, c.C0, 1.5, 0.5, F32, offset=(0, 0, 1), pad=(0, 0, 3))
+        assert path == g.PATH_F32_SIMT and _expect_split(bn, g.last_k_split())
+        C, _, _ = run_abi(c.A, c.B, None, 1.0, 0.0, F32, c_fill=float("nan"))
+        assert _expect_split(bn, g.last_k_split()) and torch.isfinite(C).all()
+    finally:
+        g.force_tile_n(0)
 
 
-def test_fp32_split_result_feeds_next_call(cuda_lib):
+@pytest.mark.parametrize("bn", [128, 256])
+def test_fp32_split_result_feeds_next_call(cuda_lib, bn):
     # the split launch overlaps the end of the whole-wave launch; a GEMM queued
     # right after must still read every tile of C1 final (C1 starts as NaN)
     c = inputs.make("fp32_4096", M=2560, N=2048, K=1024)
@@ -152,8 +238,12 @@ def test_fp32_split_result_feeds_next_call(cuda_lib):
     C2 = torch.empty(2560, 512, device="cuda")
     for _ in range(3):
         C1.fill_(float("nan"))
-        g.gemm(A, B, C1, 1.0, 0.0)
-        assert g.last_k_split() == 4
+        g.force_tile_n(bn)
+        try:
+            g.gemm(A, B, C1, 1.0, 0.0)
+            assert _expect_split(bn, g.last_k_split())
+        finally:
+            g.force_tile_n(0)
         g.gemm(C1, D, C2, 1.0, 0.0)
     torch.cuda.synchronize()
     assert g.device_status()[0] == 0

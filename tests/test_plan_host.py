@@ -99,3 +99,54 @@ def test_decode_cluster_split(plan):
     # a forced split, still clamped to the K units there are
     assert plan(("cluster", 250, 64, SMS, 4, 8), ("cluster", 32, 3, SMS, 0, 8),
                 ("cluster", 32, 3, SMS, 8, 8)) == ["4", "2", "2"]
+
+
+def simtopt(plan, tn, M, N, K, c2, c4, allowed=1):
+    bn = 16 * tn
+    tiles = -(-M // 128) * -(-N // bn)
+    min_k = 10 if tn == 8 else 16   # two rounds of the 5- or 8-stage ring
+    t, split = plan(("simtopt", tn, tiles, -(-K // 16), SMS, c2, c4, min_k, allowed))[0].split()
+    return float(t), int(split)
+
+
+def test_fp32_wide_tile_model(plan):
+    # 4096^3 with 128 x 256 tiles: 512 tiles = 3 waves of 152 + 56; the 56
+    # run as 112 half-K tiles in one round (0.5 of a tile) rather than a
+    # whole round, or as 224 quarter tiles in two rounds of 36 clusters of 4
+    t, split = simtopt(plan, 16, 4096, 4096, 4096, 76, 36)
+    assert split == 2
+    assert t == pytest.approx(2 / 1.075 * (3 + 0.5 + 0.02), rel=1e-3)
+    # forbidden split: a whole fourth round
+    assert simtopt(plan, 16, 4096, 4096, 4096, 76, 36, allowed=0) == \
+        (pytest.approx(2 / 1.075 * 4, rel=1e-3), 1)
+    # few tiles: quarter tiles fit in one round and win over halves
+    assert simtopt(plan, 16, 1024, 1024, 1024, 76, 36)[1] == 4
+    # 63 K-slices: too few for four ranks of 16, two ranks of 31/32
+    assert simtopt(plan, 16, 1000, 1004, 1001, 76, 36)[1] == 2
+    # too little K for any split (fewer than 2 x 16 K-slices)
+    assert simtopt(plan, 16, 1024, 1024, 496, 76, 36)[1] == 1
+    # whole waves only (608 tiles = 4 x 152): nothing to split
+    assert simtopt(plan, 16, 4864, 4096, 4096, 76, 36) == (pytest.approx(2 / 1.075 * 4, rel=1e-3), 1)
+
+
+def test_fp32_narrow_tile_model_matches_the_split_rule(plan):
+    # the 128 x 128 option is the wave model of simt_split: 4096^3 splits
+    t, split = simtopt(plan, 8, 4096, 4096, 4096, 0, 76)
+    assert split == 4
+    assert t == pytest.approx(2 * (3 + 0.25 + 0.25 * 0.53), rel=1e-3)
+    assert simtopt(plan, 8, 8192, 8192, 4096, 0, 76)[1] == 1
+
+
+def test_fp32_tile_choice(plan):
+    # the dispatcher takes the wide tiles when their estimate is below 0.97 of
+    # the narrow one; the choices the GB300 timings favour (narrow / wide,
+    # ms): 4096^3 2.339 / 2.285, 8192^2 x 4096 9.356 / 8.816, 4096 x 3584 x
+    # 4096 2.115 / 1.971 on the wide tiles; 2048^2 x 4096 0.602 / 0.662,
+    # 2560 x 2048 x 1024 0.210 / 0.224 and 256^3 (4 narrow tiles, one CTA
+    # per SM) on the narrow ones
+    def wide(M, N, K):
+        return simtopt(plan, 16, M, N, K, 76, 36)[0] < 0.97 * simtopt(plan, 8, M, N, K, 0, 76)[0]
+    for M, N, K in ((4096, 4096, 4096), (8192, 8192, 4096), (4096, 3584, 4096)):
+        assert wide(M, N, K), (M, N, K)
+    for M, N, K in ((2048, 2048, 4096), (2560, 2048, 1024), (256, 256, 256)):
+        assert not wide(M, N, K), (M, N, K)
