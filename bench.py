@@ -681,13 +681,17 @@ def measure_w4_decode(g, torch, dev, hbm, iters=20):
             "flops": int(sum(2 * m * N * K for m, N, K, *_ in calls))}
 
 
-def measure_attention(g, torch, dev, bf16_peak_tflops, reps=7):
+def measure_attention(g, torch, dev, bf16_peak_tflops, reps=7, batch=8):
     """Attention forward: one LLaMA-7B layer's prefill (32 heads of 128, 2048
     tokens, causal) and a 4096-token non-causal case.  FLOPs = 4 * D * (the
     query-key pairs a query sees), i.e. both products; against the measured
-    bf16 peak.  Events around each call, median of `reps`.  Not part of the
-    step."""
+    bf16 peak.  Events around each call, median of `reps` (each call pays a
+    launch from an idle stream); and `back_to_back`: `batch` calls queued
+    behind a hold kernel with events around the batch, per call (as the
+    layers of a model's forward pass run).  Not part of the step."""
+    import bench_probe
     from roofline_driven_optimisation_gb300 import inputs
+    bench_probe.build()
     stream = torch.cuda.current_stream(dev)
     out = {"peak_tflops": round(bf16_peak_tflops, 1)}
     for name, S, causal in (("llama7b_prefill_2048_causal", 2048, True), ("s4096_noncausal", 4096, False)):
@@ -704,10 +708,24 @@ def measure_attention(g, torch, dev, bf16_peak_tflops, reps=7):
             evs.append((e0, e1))
         torch.cuda.synchronize(dev)
         ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+        bb = []
+        for _ in range(3):
+            bench_probe.probe_hold(5_000_000, stream.cuda_stream)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(batch):
+                g.attention(Q, K, V, O, causal=causal)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            bb.append(e0.elapsed_time(e1) / batch)
+        ms_bb = min(bb)
         pairs = S * (S + 1) // 2 if causal else S * S
         flops = 4 * 32 * 128 * pairs
         tf = flops / (ms * 1e-3) / 1e12
-        out[name] = {"ms": round(ms, 4), "tflops": round(tf, 1), "frac": round(tf / bf16_peak_tflops, 4)}
+        tf_bb = flops / (ms_bb * 1e-3) / 1e12
+        out[name] = {"ms": round(ms, 4), "tflops": round(tf, 1), "frac": round(tf / bf16_peak_tflops, 4),
+                     "back_to_back": {"ms": round(ms_bb, 4), "tflops": round(tf_bb, 1),
+                                      "frac": round(tf_bb / bf16_peak_tflops, 4), "calls": batch}}
         del Q, K, V, O
     status, where = g.device_status(stream.cuda_stream)
     if status != 0:

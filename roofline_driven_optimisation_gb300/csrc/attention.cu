@@ -24,7 +24,10 @@
 //   * O += P_j V_j accumulates in TMEM (M = 128, N = d); a warp whose rows
 //     need no rescale releases P_j before the previous P V has finished, so
 //     the P V MMAs run back to back; after the last tile each row is divided
-//     by l and written as bf16.
+//     by l and written as bf16;
+//   * programmatic dependent launch: a CTA's set-up (barriers, tensor
+//     memory) overlaps the previous kernel, and the next kernel's CTAs take
+//     SM slots as this grid's CTAs leave.
 // Masked scores (causal, or keys past Sk) are -inf before the softmax.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -198,6 +201,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // launched with programmatic stream serialization: the set-up above
+  // overlaps the end of the previous kernel on the stream; every read of Q,
+  // K, V and every write of O comes after this wait.  The next kernel may be
+  // scheduled as this grid's CTAs leave (it waits for this grid to finish
+  // before touching memory).
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
   auto fail_wait = [&](int site) {
     if (!*abort_flag) report_status(p.status, 5, site);
     *abort_flag = 1;
@@ -522,8 +532,18 @@ int launch_fast(const AttnParams& p, const CUtensorMap* mQ, const CUtensorMap* m
   static std::atomic<uint64_t> smem_set{0};
   cudaError_t e = set_smem_once(smem_set, attention_kernel<D>, AttnCfg<D>::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)((p.Sq + BM - 1) / BM), (unsigned)(p.B * p.Hq));
-  attention_kernel<D><<<grid, THREADS, AttnCfg<D>::SMEM_BYTES, s>>>(*mQ, *mK, *mV, p);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3((unsigned)((p.Sq + BM - 1) / BM), (unsigned)(p.B * p.Hq));
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = AttnCfg<D>::SMEM_BYTES;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, attention_kernel<D>, *mQ, *mK, *mV, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
