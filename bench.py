@@ -919,6 +919,10 @@ def run_case(a):
     from roofline_driven_optimisation_gb300 import inputs
 
     g.load()
+    if a.tc_pair:
+        g.force_tc_pair(a.tc_pair)
+    if a.tile_n:
+        g.force_tile_n(a.tile_n)
     if a.swiglu is not None:
         return case_swiglu(g, torch, inputs, a)
     if a.fp8 is not None:
@@ -1069,6 +1073,9 @@ def main():
                     help="INT4-weight decode GEMM with M rows (K 4096, N 32000 unless given; group 128)")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--out", default="auto", choices=["auto", "bf16", "f32"])
+    ap.add_argument("--tc-pair", type=int, choices=[1, 2],
+                    help="pin the tensor-core kernel to single CTAs (1) or CTA pairs (2)")
+    ap.add_argument("--tile-n", type=int, help="pin the C tile width (gemm_force_tile_n)")
     ap.add_argument("--M", type=int)
     ap.add_argument("--N", type=int)
     ap.add_argument("--K", type=int)
