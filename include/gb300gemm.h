@@ -23,13 +23,22 @@
  *     there does not reach the result.
  *   - M == 0 or N == 0 is a no-op.  K == 0 gives C = beta*C.
  *   - The call is asynchronous on `stream` (0 = legacy default stream).  It
- *     performs no host synchronisation and no device allocation.
+ *     performs no host synchronisation and no device allocation, except the
+ *     first gemm_f32 / gemm_f32_ex call on a device: it allocates the FP32
+ *     kernel's stream-K workspace (four slots of 39.8 MB of partial tiles on
+ *     152 SMs, plus flags; kept until the process exits), zeroes its flags
+ *     and waits for the device once.
  *   - Fast paths need 16-byte-aligned A and B and lda, ldb whose byte size is
  *     a multiple of 16; anything else still runs, on a generic GPU kernel.
  *     There is no CPU fallback.
  *   - Results of one call are deterministic: the same inputs give the same
  *     bits on every run (fixed reduction order, including split-K).
- *   - Calls made concurrently from several host threads are safe.
+ *   - Calls made concurrently from several host threads are safe.  FP32
+ *     calls whose partial last wave runs stream-K (gemm_last_k_split() > 1
+ *     on a wide tile) take the four workspace slots in turn: at most four
+ *     of them may execute on the GPU at the same time (on different streams,
+ *     or in graphs launched side by side); a fifth would share a slot with
+ *     the first and race with it.
  *   - Calls can be captured into a CUDA graph (stream capture) once the same
  *     kind of call has run on the device: the first call of a kernel family
  *     on a device sets kernel attributes and queries occupancy.
@@ -344,13 +353,17 @@ int gemm_last_tc_pair(void);
  * each as two half-width tiles on otherwise idle pairs; the FP32 SIMT kernel
  * runs them as a second launch in which a cluster of CTAs shares each
  * tile's K range (partial sums added in rank order, in distributed shared
- * memory; clusters of two or four).  For A/B measurements and tests.
+ * memory; clusters of four) on its narrow tiles, or stream-K on its wide
+ * tiles: the partial wave's K-slices spread evenly over up to one CTA per SM,
+ * partial tiles exchanged through the workspace and added in CTA order.  For
+ * A/B measurements and tests.
  */
 int gemm_force_split_tiles(int enable);
 
 /* For the last call on this host thread: the number of CTAs that shared the
- * K range of one C tile (the decode kernels' cluster split, or 2 or 4 when the
- * FP32 SIMT kernel split its partial last wave), 1 if none did. */
+ * K range of one C tile (the decode kernels' cluster split; 4 when the FP32
+ * SIMT kernel split its narrow tiles' partial last wave; for its stream-K
+ * tail, the most CTAs that met in one tile), 1 if none did. */
 int gemm_last_k_split(void);
 
 /*

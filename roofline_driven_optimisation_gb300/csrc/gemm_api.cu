@@ -663,6 +663,9 @@ int gemm_device_status(cudaStream_t stream, int* where) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return g3::fail(GEMM_ERR_CUDA, "stream sync: %s", cudaGetErrorString(e));
   if (where) *where = (int)((unsigned)word >> 8);
+  // a kernel that gave up may have left stream-K flags raised: lower them
+  // before the workspace is used again
+  if ((word & 0xff) == GEMM_ERR_DEVICE_TIMEOUT) g3::sk_clear_flags();
   return word & 0xff;
 }
 

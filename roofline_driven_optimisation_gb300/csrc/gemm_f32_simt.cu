@@ -94,7 +94,31 @@ struct SimtParams {
   int tiles_m, tiles_n;
   int c_vec;      // C pointer 16-byte aligned and ldc % 4 == 0
   int tile_base;  // raster index of the split launch's first C tile
+  // stream-K launch (SPLIT == 0): the tiles from tile_base on, as sk_units
+  // K-slices in tile order, split evenly over sk_ctas CTAs
+  long long sk_units;
+  int sk_ctas;
+  float* sk_partials;     // [sk_ctas][kSkMaxSeg][BM][BN] fp32 partial tiles
+  unsigned* sk_flags;     // [sk_ctas][kSkMaxSeg][8 warps]: 1 = that warp's part is written
 };
+
+// Stream-K: a CTA's K-slice range is at most one tile long, so it touches at
+// most two tiles.
+constexpr int kSkMaxSeg = 2;
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// The CTAs of a stream-K launch: CTA c owns K-slices [sk_begin(c), sk_begin(c + 1)).
+__device__ __forceinline__ long long sk_begin(long long c, long long units, int ctas) {
+  return c * units / ctas;
+}
 
 __device__ __forceinline__ float2 lds64(uint32_t addr) {
   float2 v;
@@ -127,6 +151,11 @@ __device__ __forceinline__ void ffma2(uint64_t& d, uint64_t a, uint64_t b) {
 __device__ __forceinline__ float2 unpack2(uint64_t v) {
   float2 r;
   asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
   return r;
 }
 
@@ -162,11 +191,146 @@ __device__ __forceinline__ void store_quad(const GemmArgs& a, int c_vec, long lo
   }
 }
 
+// Stream-K: the end of this CTA's share of one tile (the K-slice u is one
+// of its slices of that tile).  Every warp handles its own 64 x 4*TN block of
+// the tile, so no barrier of the whole CTA is needed.  Returns false after a
+// bounded wait ran out (the kernel's abort path follows).
+template <int TN, bool EPI>
+__device__ __forceinline__ bool sk_segment_end(const SimtParams& p, long long u, int k_slices, int tm0,
+                                               int tn0, int warp, int lane,
+                                               uint64_t (&acc)[8][TN / 2], volatile int* abort_flag) {
+  using Cfg = SimtCfg<TN>;
+  constexpr int BN = Cfg::BN, WN = Cfg::WN;
+  const GemmArgs& a = p.a;
+  const long long U = p.sk_units;
+  const int G = p.sk_ctas;
+  const long long T0 = u - u % k_slices, T1 = T0 + k_slices;   // this tile's K-slices
+  // the CTAs whose ranges meet [T0, T1): c with begin(c + 1) > T0 and begin(c) < T1
+  const int cfirst = (int)(((T0 + 1) * G + U - 1) / U) - 1;
+  const int clast = (int)((T1 * G + U - 1) / U) - 1;
+  // the finisher: the CTA whose share of the tile ends latest in its own
+  // range (the first such CTA on a tie), so its wait is the shortest
+  int fin = cfirst;
+  long long best = -1;
+  for (int c = cfirst; c <= clast; ++c) {
+    const long long b = sk_begin(c, U, G), e = min(sk_begin(c + 1, U, G), T1);
+    if (e - b > best) {
+      best = e - b;
+      fin = c;
+    }
+  }
+  auto slot_of = [&](int c) {
+    return c * kSkMaxSeg + (int)(T0 / k_slices - sk_begin(c, U, G) / k_slices);
+  };
+  const int me = (int)blockIdx.x;
+  const int wm = warp / 4, wn = warp % 4, tm = lane % 8, tn = lane / 8;
+  if (me != fin) {
+    // ------------------------------------------------ contributor
+    float* dst = p.sk_partials + (size_t)slot_of(me) * (BM * BN);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+#pragma unroll
+      for (int h = 0; h < TN / 4; ++h) {
+        const int row = wm * 64 + i * 8 + tm, col = wn * WN + h * 16 + tn * 4;
+        const float2 lo = unpack2(acc[i][2 * h]), hi = unpack2(acc[i][2 * h + 1]);
+        *reinterpret_cast<float4*>(dst + (size_t)row * BN + col) = make_float4(lo.x, lo.y, hi.x, hi.y);
+      }
+    }
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) st_release_u32(p.sk_flags + slot_of(me) * 8 + warp, 1u);
+  } else {
+    // ------------------------------------------------ finisher
+    // every other part of this warp's block must be written (bounded wait)
+    bool ok = true;
+    if (lane == 0) {
+      for (int c = cfirst; ok && c <= clast; ++c) {
+        if (c == me) continue;
+        const unsigned* flag = p.sk_flags + slot_of(c) * 8 + warp;
+        if (ld_acquire_u32(flag) != 0u) continue;
+        const uint64_t t0 = globaltimer_ns();
+        while (true) {
+          bool got = false;
+#pragma unroll 1
+          for (int r = 0; r < 32 && !got; ++r) got = ld_acquire_u32(flag) != 0u;
+          if (got) break;
+          if (*abort_flag || globaltimer_ns() - t0 > a.timeout_ns) {
+            ok = false;
+            break;
+          }
+        }
+      }
+      if (!ok) {
+        if (!*abort_flag) report_status(a.status, 5, kSiteSimtStreamK);
+        *abort_flag = 1;
+      }
+    }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (!ok) return false;
+    __syncwarp();
+    __threadfence();
+    // this CTA's part first, then the others in CTA order (fixed for the
+    // shape, so every call gives the same bits); L2 loads (the parts were
+    // written by other SMs)
+    for (int c = cfirst; c <= clast; ++c) {
+      if (c == me) continue;
+      const float* src = p.sk_partials + (size_t)slot_of(c) * (BM * BN);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+#pragma unroll
+        for (int h = 0; h < TN / 4; ++h) {
+          const int row = wm * 64 + i * 8 + tm, col = wn * WN + h * 16 + tn * 4;
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(src + (size_t)row * BN + col));
+          float2 lo = unpack2(acc[i][2 * h]), hi = unpack2(acc[i][2 * h + 1]);
+          lo.x += v.x;
+          lo.y += v.y;
+          hi.x += v.z;
+          hi.y += v.w;
+          acc[i][2 * h] = pack2(lo.x, lo.y);
+          acc[i][2 * h + 1] = pack2(hi.x, hi.y);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      for (int c = cfirst; c <= clast; ++c)
+        if (c != me) p.sk_flags[slot_of(c) * 8 + warp] = 0u;   // ready for the next call
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const long long m = (long long)tm0 + wm * 64 + i * 8 + tm;
+      if (m >= a.M) continue;
+#pragma unroll
+      for (int h = 0; h < TN / 4; ++h) {
+        const long long n = (long long)tn0 + wn * WN + h * 16 + tn * 4;
+        const float2 lo = unpack2(acc[i][2 * h]), hi = unpack2(acc[i][2 * h + 1]);
+        float v[4] = {a.alpha * lo.x, a.alpha * lo.y, a.alpha * hi.x, a.alpha * hi.y};
+        store_quad<EPI>(a, p.c_vec, m, n, v);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int q = 0; q < TN / 2; ++q) acc[i][q] = 0ull;
+  return true;
+}
+
 // TN: register-tile width (SimtCfg).
 // EPI: bias and/or activation present (the plain instance has no trace of
 // them, so the common case keeps the main loop's register allocation).
 // SPLIT: CTAs of a cluster that share one C tile's K range (1: a whole tile
 // per CTA); cluster rank r takes the r-th of SPLIT contiguous K ranges.
+// SPLIT == 0 is the stream-K launch: the K-slices of the tiles from
+// tile_base on, in tile order, are split evenly over the CTAs, so a tile's
+// K range may be shared by CTAs of different clusters.  Each CTA leaves the
+// partial sum of a tile it does not finish in the workspace and raises one
+// flag per warp; the tile's finisher -- the CTA whose share of it ends
+// latest within its own range -- adds the parts in CTA order (the same order
+// whichever CTA finishes, so the result is deterministic), applies the
+// epilogue and lowers the flags.  Only finishers wait, with a bound, on
+// flags of CTAs that never wait; the grid never has more CTAs than fit at
+// once.
 // TRIGGER: a split launch of the last wave follows on the stream (the plain
 // instance has no trace of it: its code runs at the original speed).
 template <int TN, bool EPI, int SPLIT, bool TRIGGER>
@@ -193,27 +357,58 @@ __global__ void __launch_bounds__(THREADS, SimtCfg<TN>::CTAS_PER_SM)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const GemmArgs& a = p.a;
+  constexpr bool SK = SPLIT == 0;
 
   // Grouped raster over C tiles: groups of 16 row-panels, column-panel by
   // column-panel, so the CTAs in flight at one time cover a near-square
   // block of C and the A and B panels they share stay in L2 (4096^3 with
   // 128 x 128 tiles: 16 x 19 tiles, 32 MB of A and 38 MB of B; groups of 8
   // rows kept all of B in flight and read 19 % more from DRAM).
-  const int tile = SPLIT > 1 ? p.tile_base + (int)(blockIdx.x / SPLIT) : (int)blockIdx.x;
-  const int group = 16;
-  const int tiles_in_group = group * p.tiles_n;
-  const int g = tile / tiles_in_group;
-  const int first_m = g * group;
-  const int gsize = min(p.tiles_m - first_m, group);
-  const int tm_idx = first_m + (tile % tiles_in_group) % gsize;
-  const int tn_idx = (tile % tiles_in_group) / gsize;
-  const int m0 = tm_idx * BM, n0 = tn_idx * BN;
-  int k_tiles = (a.K + BK - 1) / BK, kt_first = 0, part = 0;
+  auto tile_origin = [&](int tile, int& tm0, int& tn0) {
+    const int group = 16;
+    const int tiles_in_group = group * p.tiles_n;
+    const int g = tile / tiles_in_group;
+    const int first_m = g * group;
+    const int gsize = min(p.tiles_m - first_m, group);
+    tm0 = (first_m + (tile % tiles_in_group) % gsize) * BM;
+    tn0 = ((tile % tiles_in_group) / gsize) * BN;
+  };
+  const int k_slices = (a.K + BK - 1) / BK;   // K-slices of one tile
+  int m0, n0, k_tiles = k_slices, kt_first = 0, part = 0;
+  // stream-K: this CTA's range starts at K-slice k_first of tile sk_tile and
+  // is at most one tile long, so it ends in that tile or the next one
+  // (origin m1, n1); seg_end is the last range index inside the first tile
+  long long u0 = 0;
+  int sk_tile = 0, seg_end = 0, m1 = 0, n1 = 0;
+  if constexpr (SK) {
+    u0 = sk_begin(blockIdx.x, p.sk_units, p.sk_ctas);
+    k_tiles = (int)(sk_begin(blockIdx.x + 1, p.sk_units, p.sk_ctas) - u0);
+    sk_tile = (int)(u0 / k_slices);
+    kt_first = (int)(u0 - (long long)sk_tile * k_slices);
+    seg_end = k_slices - kt_first - 1;
+    tile_origin(p.tile_base + sk_tile, m0, n0);
+    if (seg_end < k_tiles - 1) tile_origin(p.tile_base + sk_tile + 1, m1, n1);
+  } else {
+    tile_origin(SPLIT > 1 ? p.tile_base + (int)(blockIdx.x / SPLIT) : (int)blockIdx.x, m0, n0);
+  }
   if constexpr (SPLIT > 1) {
     part = (int)cluster_ctarank();
     kt_first = k_tiles * part / SPLIT;
     k_tiles = k_tiles * (part + 1) / SPLIT - kt_first;
   }
+  // The i-th K-slice this CTA streams: its A and B coordinates.
+  auto slice_coords = [&](int i, int& xk, int& ym, int& xn) {
+    if constexpr (SK) {
+      const bool second = i > seg_end;
+      ym = second ? m1 : m0;
+      xn = second ? n1 : n0;
+      xk = (second ? i - seg_end - 1 : kt_first + i) * BK;
+    } else {
+      ym = m0;
+      xn = n0;
+      xk = (kt_first + i) * BK;
+    }
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -238,9 +433,11 @@ __global__ void __launch_bounds__(THREADS, SimtCfg<TN>::CTAS_PER_SM)
     tma_prefetch_desc(&mapA);
     tma_prefetch_desc(&mapB);
     for (int kt = 0; kt < k_tiles && kt < STAGES; ++kt) {
+      int xk, ym, xn;
+      slice_coords(kt, xk, ym, xn);
       mbar_arrive_expect_tx(full_bar(kt), STAGE_BYTES);
-      tma_load_2d(a_tile(kt), &mapA, full_bar(kt), (kt_first + kt) * BK, m0);
-      tma_load_2d(b_tile(kt), &mapB, full_bar(kt), n0, (kt_first + kt) * BK);
+      tma_load_2d(a_tile(kt), &mapA, full_bar(kt), xk, ym);
+      tma_load_2d(b_tile(kt), &mapB, full_bar(kt), xn, xk);
       issue_cnt[kt] = 1;
     }
   }
@@ -272,68 +469,88 @@ __global__ void __launch_bounds__(THREADS, SimtCfg<TN>::CTAS_PER_SM)
       my_k_tiles = 0;
     }
   }
-  for (int kt = 0; kt < my_k_tiles; ++kt) {
-    const int s = kt % STAGES;
-    const uint32_t parity = (uint32_t)(kt / STAGES) & 1u;
-    if (!mbar_wait(full_bar(s), parity, a.timeout_ns, abort_flag)) {
-      if (!*abort_flag) report_status(a.status, 5, kSiteSimtConsumer);
-      *abort_flag = 1;
-      ok = false;
-      break;
-    }
-    const uint32_t at = a_tile(s) + a_row_off;
-    const uint32_t bt = b_tile(s) + b_col_off;
+  // The K-slices run in pieces: one for a whole tile or a split part; for
+  // stream-K, the slices of the range inside its first tile, then those in
+  // the next tile, each piece followed by its hand-over or finish, so the
+  // per-slice loop carries no test for a piece's end.
+#pragma unroll 1
+  for (int piece = 0; piece < (SK ? 2 : 1); ++piece) {
+    const int kt_lo = piece == 0 ? 0 : seg_end + 1;
+    const int kt_hi = SK && piece == 0 ? min(seg_end + 1, my_k_tiles) : my_k_tiles;
+    for (int kt = kt_lo; kt < kt_hi; ++kt) {
+      const int s = kt % STAGES;
+      const uint32_t parity = (uint32_t)(kt / STAGES) & 1u;
+      if (!mbar_wait(full_bar(s), parity, a.timeout_ns, abort_flag)) {
+        if (!*abort_flag) report_status(a.status, 5, kSiteSimtConsumer);
+        *abort_flag = 1;
+        ok = false;
+        break;
+      }
+      const uint32_t at = a_tile(s) + a_row_off;
+      const uint32_t bt = b_tile(s) + b_col_off;
 #pragma unroll
-    for (int kp = 0; kp < BK / 2; ++kp) {
-      // rows i*8+tm, k = 2kp, 2kp+1: one 8-byte load per row inside the
-      // swizzled 16-byte chunk that holds k = 4*(kp/2) .. 4*(kp/2)+3
-      // (loading the next pair's values a step ahead was 2 % slower)
-      const uint32_t off = (uint32_t)((((kp >> 1) ^ sw) * 16) + (kp & 1) * 8);
-      float2 av[8];
+      for (int kp = 0; kp < BK / 2; ++kp) {
+        // rows i*8+tm, k = 2kp, 2kp+1: one 8-byte load per row inside the
+        // swizzled 16-byte chunk that holds k = 4*(kp/2) .. 4*(kp/2)+3
+        // (loading the next pair's values a step ahead was 2 % slower)
+        const uint32_t off = (uint32_t)((((kp >> 1) ^ sw) * 16) + (kp & 1) * 8);
+        float2 av[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) av[i] = lds64(at + i * 8 * 64 + off);
+        for (int i = 0; i < 8; ++i) av[i] = lds64(at + i * 8 * 64 + off);
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        const uint32_t brow = bt + (uint32_t)(kp * 2 + kk) * (BN * 4);
-        uint64_t b[TN / 2];
+        for (int kk = 0; kk < 2; ++kk) {
+          const uint32_t brow = bt + (uint32_t)(kp * 2 + kk) * (BN * 4);
+          uint64_t b[TN / 2];
 #pragma unroll
-        for (int h = 0; h < TN / 4; ++h) lds_pairs(brow + h * 64, b[2 * h], b[2 * h + 1]);
-        if constexpr (TN == 8 && EPI) {
-          // rows outer: the 8 x 8 instance with an epilogue would spill at
-          // 128 registers with all eight broadcasts live at once
+          for (int h = 0; h < TN / 4; ++h) lds_pairs(brow + h * 64, b[2 * h], b[2 * h + 1]);
+          if constexpr (TN == 8 && EPI) {
+            // rows outer: the 8 x 8 instance with an epilogue would spill at
+            // 128 registers with all eight broadcasts live at once
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint64_t a2 = dup2(kk == 0 ? av[i].x : av[i].y);
+            for (int i = 0; i < 8; ++i) {
+              const uint64_t a2 = dup2(kk == 0 ? av[i].x : av[i].y);
 #pragma unroll
-            for (int q = 0; q < TN / 2; ++q) ffma2(acc[i][q], a2, b[q]);
+              for (int q = 0; q < TN / 2; ++q) ffma2(acc[i][q], a2, b[q]);
+            }
+          } else {
+            uint64_t a2[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a2[i] = dup2(kk == 0 ? av[i].x : av[i].y);
+            // B pair outer, rows inner: consecutive FMAs share the B operand
+#pragma unroll
+            for (int q = 0; q < TN / 2; ++q)
+#pragma unroll
+              for (int i = 0; i < 8; ++i) ffma2(acc[i][q], a2[i], b[q]);
           }
-        } else {
-          uint64_t a2[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) a2[i] = dup2(kk == 0 ? av[i].x : av[i].y);
-          // B pair outer, rows inner: consecutive FMAs share the B operand
-#pragma unroll
-          for (int q = 0; q < TN / 2; ++q)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) ffma2(acc[i][q], a2[i], b[q]);
+        }
+      }
+      __syncwarp();  // every lane of this warp is done reading slot s
+      if (lane == 0) {
+        // the last of the eight warps to release slot s refills it with K-slice
+        // kt+STAGES; the slot's next round cannot start before that copy lands
+        __threadfence_block();
+        if (atomicAdd(&done_cnt[s], 1u) == COMPUTE_WARPS - 1) {
+          done_cnt[s] = 0;
+          __threadfence_block();
+          if (kt + STAGES < k_tiles && !*abort_flag) {
+            int xk, ym, xn;
+            slice_coords(kt + STAGES, xk, ym, xn);
+            mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
+            tma_load_2d(a_tile(s), &mapA, full_bar(s), xk, ym);
+            tma_load_2d(b_tile(s), &mapB, full_bar(s), xn, xk);
+            atomicAdd(&issue_cnt[s], 1u);
+          }
         }
       }
     }
-    __syncwarp();  // every lane of this warp is done reading slot s
-    if (lane == 0) {
-      // the last of the eight warps to release slot s refills it with K-slice
-      // kt+STAGES; the slot's next round cannot start before that copy lands
-      __threadfence_block();
-      if (atomicAdd(&done_cnt[s], 1u) == COMPUTE_WARPS - 1) {
-        done_cnt[s] = 0;
-        __threadfence_block();
-        if (kt + STAGES < k_tiles && !*abort_flag) {
-          const int kn = kt_first + kt + STAGES;
-          mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
-          tma_load_2d(a_tile(s), &mapA, full_bar(s), kn * BK, m0);
-          tma_load_2d(b_tile(s), &mapB, full_bar(s), n0, kn * BK);
-          atomicAdd(&issue_cnt[s], 1u);
-        }
+    if (!ok) break;
+    if constexpr (SK) {
+      // ------------------------------------------ stream-K piece end
+      if (kt_hi > kt_lo &&
+          !sk_segment_end<TN, EPI>(p, u0 + kt_lo, k_slices, piece ? m1 : m0, piece ? n1 : n0, warp,
+                                   lane, acc, abort_flag)) {
+        ok = false;
+        break;
       }
     }
   }
@@ -363,7 +580,7 @@ __global__ void __launch_bounds__(THREADS, SimtCfg<TN>::CTAS_PER_SM)
         }
       }
     }
-  } else {
+  } else if constexpr (SPLIT > 1) {
     // ------------------------------------------- split epilogue (cluster)
     // Every copy this CTA issued has landed (all were consumed, or drained
     // above), so the ring holds this CTA's partial tile.
@@ -424,41 +641,24 @@ __global__ void __launch_bounds__(THREADS, SimtCfg<TN>::CTAS_PER_SM)
     // A grid that finishes before the one it overlaps would let later work on
     // the stream run early; completion waits for that grid.
     griddep_wait();
+  } else {
+    // stream-K: every segment was finished or handed over inside the loop;
+    // as for the cluster split, completion waits for the grid it overlaps
+    griddep_wait();
   }
   __syncthreads();
 }
 
-// Resident clusters of 2 and of 4 CTAs of one configuration's split kernel,
-// per device (a GPC whose free CTA slots are not a multiple of the cluster
-// size leaves the rest idle); queried once, the EPI instances having the
-// same resources.
+// Resident clusters of four CTAs of the narrow configuration's split kernel,
+// per device (a GPC whose free CTA slots are not a multiple of four leaves
+// the rest idle); queried once, the EPI instances having the same resources.
 struct SimtDeviceInfo {
-  std::atomic<bool> ready{false};   // published after the fields below are set
-  int max_clusters2 = 0, max_clusters4 = 0;
+  std::atomic<bool> ready{false};   // published after the field below is set
+  int max_clusters4 = 0;
 };
 
-template <int TN, int SPLIT>
-cudaError_t query_clusters(int num_sms, int* n) {
-  using Cfg = SimtCfg<TN>;
-  auto k = sgemm_tma_kernel<TN, false, SPLIT, false>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = SPLIT;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cfg.gridDim = dim3((unsigned)(SPLIT * Cfg::CTAS_PER_SM * num_sms), 1, 1);
-  return cudaOccupancyMaxActiveClusters(n, k, &cfg);
-}
-
-template <int TN>
-cudaError_t device_clusters(int num_sms, int* c2, int* c4) {
+cudaError_t narrow_clusters4(int num_sms, int* c4) {
+  using Cfg = SimtCfg<8>;
   static SimtDeviceInfo info[64];
   static std::mutex mu;
   int dev = 0;
@@ -468,19 +668,140 @@ cudaError_t device_clusters(int num_sms, int* c2, int* c4) {
   if (!info[dev].ready.load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> lock(mu);
     if (!info[dev].ready.load(std::memory_order_relaxed)) {
-      int n2 = 0, n4 = 0;
-      if constexpr (TN == 16) {  // only the wide tile has a split-2 instance
-        if ((e = query_clusters<TN, 2>(num_sms, &n2)) != cudaSuccess) return e;
-      }
-      if ((e = query_clusters<TN, 4>(num_sms, &n4)) != cudaSuccess) return e;
-      info[dev].max_clusters2 = n2;
-      info[dev].max_clusters4 = n4;
+      auto k = sgemm_tma_kernel<8, false, 4, false>;
+      if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES)) !=
+          cudaSuccess)
+        return e;
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 4;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.blockDim = dim3(THREADS, 1, 1);
+      cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      cfg.gridDim = dim3((unsigned)(4 * Cfg::CTAS_PER_SM * num_sms), 1, 1);
+      int n = 0;
+      if ((e = cudaOccupancyMaxActiveClusters(&n, k, &cfg)) != cudaSuccess) return e;
+      info[dev].max_clusters4 = n;
       info[dev].ready.store(true, std::memory_order_release);
     }
   }
-  *c2 = info[dev].max_clusters2;
   *c4 = info[dev].max_clusters4;
   return cudaSuccess;
+}
+
+// The stream-K workspace of a device: kSkSlots slots, each with room for the
+// partial tiles and flags of a stream-K launch of up to one CTA per SM
+// (152 SMs: 39.8 MB of partials a slot), allocated and zeroed at the first
+// FP32 SIMT call on the device and kept until the process exits.  Calls take
+// the slots in turn, so up to kSkSlots stream-K calls may run on the GPU at
+// once (on different streams) without sharing one.
+constexpr int kSkSlots = 4;
+struct SkWorkspace {
+  std::atomic<bool> ready{false};   // published after the fields below are set
+  float* partials = nullptr;        // kSkSlots x slot_floats
+  unsigned* flags = nullptr;        // kSkSlots x slot_flags, zero between calls
+  size_t slot_floats = 0, slot_flags = 0;
+  int max_ctas = 0;
+  std::atomic<unsigned> next{0};
+};
+SkWorkspace g_sk[64];
+std::mutex g_sk_mu;
+
+cudaError_t sk_workspace(int num_sms, SkWorkspace** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  SkWorkspace& w = g_sk[dev];
+  if (!w.ready.load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(g_sk_mu);
+    if (!w.ready.load(std::memory_order_relaxed)) {
+      using Cfg = SimtCfg<16>;
+      const int ctas = Cfg::CTAS_PER_SM * num_sms;
+      const size_t slot_floats = (size_t)ctas * kSkMaxSeg * BM * Cfg::BN;
+      const size_t slot_flags = (size_t)ctas * kSkMaxSeg * COMPUTE_WARPS;
+      void* p = nullptr;
+      if ((e = cudaMalloc(&p, kSkSlots * slot_floats * sizeof(float))) != cudaSuccess) return e;
+      void* f = nullptr;
+      if ((e = cudaMalloc(&f, kSkSlots * slot_flags * sizeof(unsigned))) != cudaSuccess) {
+        cudaFree(p);
+        return e;
+      }
+      if ((e = cudaMemset(f, 0, kSkSlots * slot_flags * sizeof(unsigned))) != cudaSuccess ||
+          (e = cudaDeviceSynchronize()) != cudaSuccess) {
+        cudaFree(p);
+        cudaFree(f);
+        return e;
+      }
+      w.partials = static_cast<float*>(p);
+      w.flags = static_cast<unsigned*>(f);
+      w.slot_floats = slot_floats;
+      w.slot_flags = slot_flags;
+      w.max_ctas = ctas;
+      w.ready.store(true, std::memory_order_release);
+    }
+  }
+  *out = &w;
+  return cudaSuccess;
+}
+
+// CTAs of a stream-K launch for `rest` tiles of k_slices K-slices each: one
+// per SM at most, each with at least kSkMinSlices K-slices (two rounds of the
+// ring), so a CTA's range is at most one tile long when k_slices >= kSkMinSlices.
+constexpr int kSkMinSlices = 2 * SimtCfg<16>::STAGES;
+int sk_ctas(long long rest, int k_slices, int num_sms) {
+  const long long by_work = rest * k_slices / kSkMinSlices;
+  const long long g = by_work < num_sms ? by_work : num_sms;
+  return (int)(g < 1 ? 1 : g);
+}
+
+// The stream-K launch and the largest number of CTAs that share one tile.
+template <bool EPI>
+cudaError_t launch_stream_k(const CUtensorMap* mapA, const CUtensorMap* mapB, SimtParams p,
+                            long long rest, int k_slices, int num_sms, bool overlap, cudaStream_t s,
+                            int* max_share) {
+  using Cfg = SimtCfg<16>;
+  static std::atomic<uint64_t> smem_set{0};
+  auto k = sgemm_tma_kernel<16, EPI, 0, false>;
+  cudaError_t e = set_smem_once(smem_set, k, Cfg::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  SkWorkspace* w = nullptr;
+  if ((e = sk_workspace(num_sms, &w)) != cudaSuccess) return e;
+  const int G = sk_ctas(rest, k_slices, num_sms);
+  if (G > w->max_ctas) return cudaErrorInvalidValue;
+  const unsigned slot = w->next.fetch_add(1, std::memory_order_relaxed) % kSkSlots;
+  p.sk_units = rest * k_slices;
+  p.sk_ctas = G;
+  p.sk_partials = w->partials + slot * w->slot_floats;
+  p.sk_flags = w->flags + slot * w->slot_flags;
+  // the same arithmetic as the kernel: CTAs meeting each tile's K-slices
+  const long long U = p.sk_units;
+  int share = 1;
+  for (long long t = 0; t < rest; ++t) {
+    const long long T0 = t * k_slices, T1 = T0 + k_slices;
+    const long long cfirst = ((T0 + 1) * G + U - 1) / U - 1, clast = (T1 * G + U - 1) / U - 1;
+    if (clast - cfirst + 1 > share) share = (int)(clast - cfirst + 1);
+  }
+  *max_share = share;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3((unsigned)G, 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  // overlap the first launch's last CTAs only when there is one: otherwise
+  // the previous kernel on the stream may still be writing A, B or C
+  cfg.numAttrs = overlap ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, k, *mapA, *mapB, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 // The split launch: `units` C tiles (the tiles past the last whole wave),
@@ -522,7 +843,8 @@ cudaError_t launch_split(const CUtensorMap* mapA, const CUtensorMap* mapB, const
 
 template <int TN, bool EPI>
 cudaError_t launch_plan(const CUtensorMap* mapA, const CUtensorMap* mapB, SimtParams p,
-                        long long tiles, const SimtPlan& plan, int num_sms, cudaStream_t s) {
+                        long long tiles, const SimtPlan& plan, int num_sms, cudaStream_t s,
+                        int* k_split) {
   using Cfg = SimtCfg<TN>;
   static std::atomic<uint64_t> smem_whole{0}, smem_first{0};
   auto whole_kernel = sgemm_tma_kernel<TN, EPI, 1, false>;
@@ -530,6 +852,7 @@ cudaError_t launch_plan(const CUtensorMap* mapA, const CUtensorMap* mapB, SimtPa
   cudaError_t e = set_smem_once(smem_whole, whole_kernel, Cfg::SMEM_BYTES);
   if (e == cudaSuccess) e = set_smem_once(smem_first, first_kernel, Cfg::SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  *k_split = 1;
   if (plan.split == 1) {
     whole_kernel<<<(unsigned)tiles, THREADS, Cfg::SMEM_BYTES, s>>>(*mapA, *mapB, p);
     return cudaGetLastError();
@@ -542,28 +865,33 @@ cudaError_t launch_plan(const CUtensorMap* mapA, const CUtensorMap* mapB, SimtPa
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   p.tile_base = (int)whole;
-  if constexpr (TN == 16) {  // only the wide tile has a split-2 instance
-    if (plan.split == 2) return launch_split<TN, EPI, 2>(mapA, mapB, p, rest, whole > 0, s);
+  if constexpr (TN == 16) {  // the wide tile's tail runs stream-K
+    if (plan.split != 0) return cudaErrorInvalidValue;
+    const int k_slices = (p.a.K + BK - 1) / BK;
+    return launch_stream_k<EPI>(mapA, mapB, p, rest, k_slices, num_sms, whole > 0, s, k_split);
+  } else {
+    if (plan.split != 4) return cudaErrorInvalidValue;
+    *k_split = 4;
+    return launch_split<TN, EPI, 4>(mapA, mapB, p, rest, whole > 0, s);
   }
-  if (plan.split == 4) return launch_split<TN, EPI, 4>(mapA, mapB, p, rest, whole > 0, s);
-  return cudaErrorInvalidValue;
 }
 
 // The wave model's estimate for one configuration (plan::simt_option), after
-// the occupancy queries it needs.
+// the occupancy query it needs.
 template <int TN>
 cudaError_t option_for(long long tiles, int k_tiles, int num_sms, bool split_allowed,
                        plan::SimtOption* o) {
   using Cfg = SimtCfg<TN>;
-  int c2 = 0, c4 = 0;
+  int c4 = 0;
   const long long slots = (long long)Cfg::CTAS_PER_SM * num_sms;
   const int min_k_tiles = 2 * Cfg::STAGES;  // two rounds of the ring per rank
-  // a cheap first test before the occupancy query
-  if (split_allowed && tiles % slots != 0 && k_tiles >= 2 * min_k_tiles) {
-    const cudaError_t e = device_clusters<TN>(num_sms, &c2, &c4);
+  // a cheap first test before the occupancy query (the wide tile's stream-K
+  // tail needs none)
+  if (TN == 8 && split_allowed && tiles % slots != 0 && k_tiles >= 4 * min_k_tiles) {
+    const cudaError_t e = narrow_clusters4(num_sms, &c4);
     if (e != cudaSuccess) return e;
   }
-  *o = plan::simt_option(TN, tiles, k_tiles, num_sms, c2, c4, min_k_tiles, split_allowed);
+  *o = plan::simt_option(TN, tiles, k_tiles, num_sms, 0, c4, min_k_tiles, split_allowed);
   return cudaSuccess;
 }
 
@@ -591,6 +919,11 @@ int plan_f32_simt(int M, int N, int K, int num_sms, int forced_tn, SimtPlan* out
 int launch_f32_simt(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
                     const SimtPlan& plan, int num_sms, cudaStream_t s, int* k_split) {
   *k_split = 1;
+  // the first call on a device sets up the stream-K workspace, whatever its
+  // shape, so that later calls (and stream captures) never allocate
+  SkWorkspace* w = nullptr;
+  const cudaError_t we = sk_workspace(num_sms, &w);
+  if (we != cudaSuccess) return we;
   SimtParams p;
   p.a = a;
   const int bn = plan.tn == 16 ? kSimtBN16 : kSimtBN8;
@@ -601,18 +934,26 @@ int launch_f32_simt(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMa
   const long long tiles = (long long)p.tiles_m * p.tiles_n;
   if (tiles <= 0) return cudaSuccess;
   if (tiles * 4 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  p.sk_units = 0;
+  p.sk_ctas = 0;
+  p.sk_partials = nullptr;
+  p.sk_flags = nullptr;
   const bool epi = a.bias != nullptr || a.act != kActNone;
-  cudaError_t e;
   if (plan.tn == 16)
-    e = epi ? launch_plan<16, true>(mapA, mapB, p, tiles, plan, num_sms, s)
-            : launch_plan<16, false>(mapA, mapB, p, tiles, plan, num_sms, s);
-  else if (plan.tn == 8)
-    e = epi ? launch_plan<8, true>(mapA, mapB, p, tiles, plan, num_sms, s)
-            : launch_plan<8, false>(mapA, mapB, p, tiles, plan, num_sms, s);
-  else
-    return cudaErrorInvalidValue;
-  if (e == cudaSuccess) *k_split = plan.split;
-  return e;
+    return epi ? launch_plan<16, true>(mapA, mapB, p, tiles, plan, num_sms, s, k_split)
+               : launch_plan<16, false>(mapA, mapB, p, tiles, plan, num_sms, s, k_split);
+  if (plan.tn == 8)
+    return epi ? launch_plan<8, true>(mapA, mapB, p, tiles, plan, num_sms, s, k_split)
+               : launch_plan<8, false>(mapA, mapB, p, tiles, plan, num_sms, s, k_split);
+  return cudaErrorInvalidValue;
+}
+
+void sk_clear_flags() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return;
+  SkWorkspace& w = g_sk[dev];
+  if (w.ready.load(std::memory_order_acquire))
+    cudaMemset(w.flags, 0, kSkSlots * w.slot_flags * sizeof(unsigned));
 }
 
 }  // namespace g3

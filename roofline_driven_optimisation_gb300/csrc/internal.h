@@ -68,6 +68,7 @@ enum WaitSite : int {
   kSiteTc2Drain = 17,
   kSiteSimtConsumer = 21,
   kSiteSimtDrain = 22,
+  kSiteSimtStreamK = 23,   // a stream-K finisher waiting for another CTA's partial tile
   kSiteSkinnyProducer = 30,
   kSiteSkinnyMma = 31,
   kSiteSkinnyEpilogue = 32,
@@ -93,8 +94,13 @@ int launch_generic(const GemmArgs& a, cudaStream_t s);
 // over clusters of `split` CTAs (*k_split receives it; 1 otherwise).
 struct SimtPlan {
   int tn = 8;     // register-tile width: 8 or 16 (C tiles of 128 x 16*tn)
-  int split = 1;  // 1, 2 (wide only) or 4
+  int split = 1;  // 1; 4 (narrow: clusters of four share a tile's K range);
+                  // 0 (wide: stream-K over the SMs, partial tiles meeting in
+                  // a per-device workspace)
 };
+// Lowers every stream-K flag of the current device's workspace (after a
+// device timeout, which may leave flags raised).
+void sk_clear_flags();
 int plan_f32_simt(int M, int N, int K, int num_sms, int forced_tn, SimtPlan* out);
 int launch_f32_simt(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
                     const SimtPlan& plan, int num_sms, cudaStream_t s, int* k_split);

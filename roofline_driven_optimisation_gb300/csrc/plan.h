@@ -95,8 +95,9 @@ inline bool simt_split(long long tiles, int k_tiles, int num_sms, int max_cluste
 
 // FP32 SIMT kernel: one candidate configuration and its estimated time.
 // `time` is in units of one 128 x 128 x K tile computed by a whole SM at the
-// narrow kernel's rate; `split` is 1 (whole tiles only) or the cluster size
-// that shares the K range of each tile past the last whole wave.
+// narrow kernel's rate; `split` is 1 (whole tiles only), 4 (narrow: clusters
+// of four CTAs share the K range of each tile past the last whole wave) or
+// 0 (wide: those tiles' K-slices are split evenly over the SMs, stream-K).
 struct SimtOption {
   double time = 1e300;
   int split = 1;
@@ -122,13 +123,14 @@ constexpr double kSimtWideMargin = 0.97;
 //           decides (its tenth-of-a-tile margin is part of the decision, not
 //           of the estimate);
 //   wide:   a wave is one tile per SM and a partial round costs a whole one;
-//           the partial last wave either runs whole or K-split over clusters
-//           of 2 or 4 (the rounds of 1/s tiles that the resident clusters
-//           need, plus 0.02 of a tile for the reduction).
-// Measured on one GB300 (waves of 0.699 ms narrow and 0.655 ms wide at K =
-// 4096): 4096^3 3.37 narrow waves split / 3.49 wide waves split in two
-// (estimates 3.38 / 3.52); 2048^2 x 4096 0.874 narrow waves split / 1.01
-// wide waves whole (0.88 / 1.0).
+//           the partial last wave either runs whole or stream-K: its
+//           K-slices spread over min(SMs, slices / (2 x 8)) CTAs, one per SM
+//           (rest / CTAs of a wave), plus 0.02 of a tile for the partial sums'
+//           exchange; stream-K needs at least 16 K-slices a tile, so that no
+//           CTA's range is longer than a tile.
+// Measured on one GB300 (K = 4096, in narrow waves of 0.699 ms): 4096^3
+// 3.35 narrow split / 3.19 wide stream-K (estimates 3.38 / 3.15); 2048^2
+// 0.866 / 0.851 (0.88 / 0.80); 8192^2 13.3 / 12.6 (13.5 / 12.6).
 inline SimtOption simt_option(int tn, long long tiles, int k_tiles, int num_sms, int max_clusters2,
                               int max_clusters4, int min_k_tiles, bool split_allowed) {
   SimtOption o;
@@ -149,22 +151,19 @@ inline SimtOption simt_option(int tn, long long tiles, int k_tiles, int num_sms,
     }
     return o;
   }
+  (void)max_clusters2;
+  (void)max_clusters4;
   const long long slots = num_sms;
   const double wave = 2.0 / kSimtWideRate;  // one 128 x 256 tile per SM
   const long long whole = tiles / slots, rest = tiles % slots;
   o.time = wave * (double)(whole + (rest > 0 ? 1 : 0));
-  if (!split_allowed || rest == 0) return o;
-  static const int splits[] = {2, 4};
-  for (int split : splits) {
-    const int clusters = split == 2 ? max_clusters2 : max_clusters4;
-    if (clusters <= 0 || k_tiles < split * min_k_tiles) continue;
-    const long long per_round = (long long)split * clusters;
-    const long long rounds = (rest * split + per_round - 1) / per_round;
-    const double t = wave * ((double)whole + (double)rounds / split + 0.02);
-    if (t < o.time) {
-      o.time = t;
-      o.split = split;
-    }
+  if (!split_allowed || rest == 0 || k_tiles < min_k_tiles) return o;
+  long long ctas = rest * k_tiles / min_k_tiles;
+  if (ctas > slots) ctas = slots;
+  const double t = wave * ((double)whole + (double)rest / (double)ctas + 0.02);
+  if (t < o.time) {
+    o.time = t;
+    o.split = 0;
   }
   return o;
 }

@@ -147,12 +147,12 @@ def test_fp32_4096_full_size_sampled(cuda_lib, bn):
 
 # The splits each width takes for these shapes on GB300 (152 SMs): 128-wide
 # tiles split four ways (at least 64 clusters of four fit at once); 256-wide
-# tiles split two or four ways, four when every rank keeps 16 K-slices.
-WIDE_SPLITS = (2, 4)
+# tiles run their last partial wave stream-K, and last_k_split() reports how
+# many CTAs shared the most-shared tile (two or more here).
 
 
 def _expect_split(bn, split):
-    return split == 4 if bn == 128 else split in WIDE_SPLITS
+    return split == 4 if bn == 128 else split >= 2
 
 
 @pytest.mark.parametrize("bn", [128, 256])
@@ -162,17 +162,13 @@ def test_fp32_split_last_wave(cuda_lib, bn, M, N, K, pad):
     # 128-wide: 1024^2: 64 tiles, all in the split launch; 2560 x 2048: 320
     # tiles, the 16 past two whole waves of 2 x 152 split; 1000 x 1004 x 1001:
     # ragged M, N and K (63 K-slices, ranks take 15/16/16/16); 300 x 200: six
-    # tiles.  256-wide: 32, 160 (8 past one wave of 152), 32 and 3 tiles; 63
-    # K-slices are too few for four ranks of 16, so that shape splits in two.
+    # tiles.  256-wide: 32, 160 (8 past one wave of 152), 32 and 3 tiles, the
+    # tiles past the last whole wave stream-K over the SMs.
     c = inputs.make("fp32_4096", M=M, N=N, K=K)
     g.force_tile_n(bn)
     try:
         err, path = check(c.A, c.B, c.C0, 1.5, 0.5, F32, pad=pad)
         assert path == g.PATH_F32_SIMT and _expect_split(bn, g.last_k_split())
-        if bn == 256 and K == 1001:
-            # no 256-wide four-way split: its ranks would get fewer than 16
-            # K-slices
-            assert g.last_k_split() == 2
         # partial sums are added in rank order: repeated calls give the same bits
         a = run_abi(c.A, c.B, c.C0, 1.5, 0.5, F32, pad=pad)[0]
         b = run_abi(c.A, c.B, c.C0, 1.5, 0.5, F32, pad=pad)[0]
@@ -204,12 +200,36 @@ def test_fp32_wide_tiles_ragged_n_split(cuda_lib, N):
 
 def test_fp32_4096_configuration(cuda_lib):
     # the bench's shape at a shorter K: on 152 SMs the wave model picks the
-    # 256-wide tiles (512 tiles = 3 waves of 152 + 56, the 56 split in two)
+    # 256-wide tiles (512 tiles = 3 waves of 152 + 56, the 56 tiles' 56 x 64
+    # K-slices stream-K over 152 CTAs of 23-24 slices: a tile meets 3-4 CTAs)
     c = inputs.make("fp32_4096", M=4096, N=4096, K=1024)
     check(c.A, c.B, c.C0, 1.5, 0.5, F32)
     assert g.last_path() == g.PATH_F32_SIMT
     if torch.cuda.get_device_properties(0).multi_processor_count == 152:
-        assert (g.last_tile_n(), g.last_k_split()) == (256, 2)
+        assert g.last_tile_n() == 256 and g.last_k_split() in (3, 4)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 256),      # one tile, one CTA: no partner
+                                   (4096, 4096, 256),    # 56 tiles over 56 CTAs, one tile each
+                                   (1536, 2560, 776),    # 12 x 10 tiles, ragged K (49 slices)
+                                   (300, 520, 4096),     # 3 x 3 tiles over 152 CTAs
+                                   (2048, 2048, 4096),   # 128 tiles, no whole wave
+                                   (4224, 4352, 640)])   # 33 x 17 = 561 tiles: 3 waves + 105
+def test_fp32_stream_k_tail(cuda_lib, M, N, K):
+    # the 256-wide tiles' last partial wave as stream-K: K-slice ranges that
+    # start and end inside tiles, partial tiles meeting in the workspace; the
+    # finisher adds them in a fixed order, so four calls in a row (each on
+    # the next of the four workspace slots) give the same bits
+    c = inputs.make("fp32_4096", M=M, N=N, K=K)
+    g.force_tile_n(256)
+    try:
+        err, path = check(c.A, c.B, c.C0, 1.5, 0.5, F32)
+        assert path == g.PATH_F32_SIMT and g.last_tile_n() == 256
+        outs = [run_abi(c.A, c.B, c.C0, 1.5, 0.5, F32)[0] for _ in range(4)]
+        assert all(torch.equal(outs[0], o) for o in outs[1:])
+        err, path = check(c.A, c.B, None, 1.0, 0.0, F32, c_fill=float("nan"), offset=(0, 0, 1), pad=(0, 0, 3))
+    finally:
+        g.force_tile_n(0)
 
 
 @pytest.mark.parametrize("bn", [128, 256])

@@ -111,22 +111,22 @@ def simtopt(plan, tn, M, N, K, c2, c4, allowed=1):
 
 def test_fp32_wide_tile_model(plan):
     # 4096^3 with 128 x 256 tiles: 512 tiles = 3 waves of 152 + 56; the 56
-    # run as 112 half-K tiles in one round (0.5 of a tile) rather than a
-    # whole round, or as 224 quarter tiles in two rounds of 36 clusters of 4
-    t, split = simtopt(plan, 16, 4096, 4096, 4096, 76, 36)
-    assert split == 2
-    assert t == pytest.approx(2 / 1.075 * (3 + 0.5 + 0.02), rel=1e-3)
+    # tiles' 56 x 256 K-slices spread over 152 CTAs (stream-K): 56/152 of a
+    # wave plus 0.02 for the partial sums' exchange, against a whole fourth
+    # round
+    t, split = simtopt(plan, 16, 4096, 4096, 4096, 0, 0)
+    assert split == 0
+    assert t == pytest.approx(2 / 1.075 * (3 + 56 / 152 + 0.02), rel=1e-3)
     # forbidden split: a whole fourth round
-    assert simtopt(plan, 16, 4096, 4096, 4096, 76, 36, allowed=0) == \
+    assert simtopt(plan, 16, 4096, 4096, 4096, 0, 0, allowed=0) == \
         (pytest.approx(2 / 1.075 * 4, rel=1e-3), 1)
-    # few tiles: quarter tiles fit in one round and win over halves
-    assert simtopt(plan, 16, 1024, 1024, 1024, 76, 36)[1] == 4
-    # 63 K-slices: too few for four ranks of 16, two ranks of 31/32
-    assert simtopt(plan, 16, 1000, 1004, 1001, 76, 36)[1] == 2
-    # too little K for any split (fewer than 2 x 16 K-slices)
-    assert simtopt(plan, 16, 1024, 1024, 496, 76, 36)[1] == 1
+    # few slices: the CTAs get at least 16 K-slices each (1024^2 x 512: 32
+    # tiles x 32 slices over 64 CTAs)
+    assert simtopt(plan, 16, 1024, 1024, 512, 0, 0) == (pytest.approx(2 / 1.075 * (32 / 64 + 0.02), rel=1e-3), 0)
+    # fewer than 16 K-slices a tile: no stream-K
+    assert simtopt(plan, 16, 1024, 1024, 240, 0, 0)[1] == 1
     # whole waves only (608 tiles = 4 x 152): nothing to split
-    assert simtopt(plan, 16, 4864, 4096, 4096, 76, 36) == (pytest.approx(2 / 1.075 * 4, rel=1e-3), 1)
+    assert simtopt(plan, 16, 4864, 4096, 4096, 0, 0) == (pytest.approx(2 / 1.075 * 4, rel=1e-3), 1)
 
 
 def test_fp32_narrow_tile_model_matches_the_split_rule(plan):
@@ -145,8 +145,8 @@ def test_fp32_tile_choice(plan):
     # 2560 x 2048 x 1024 0.210 / 0.224 and 256^3 (4 narrow tiles, one CTA
     # per SM) on the narrow ones
     def wide(M, N, K):
-        return simtopt(plan, 16, M, N, K, 76, 36)[0] < 0.97 * simtopt(plan, 8, M, N, K, 0, 76)[0]
+        return simtopt(plan, 16, M, N, K, 0, 0)[0] < 0.97 * simtopt(plan, 8, M, N, K, 0, 76)[0]
     for M, N, K in ((4096, 4096, 4096), (8192, 8192, 4096), (4096, 3584, 4096)):
         assert wide(M, N, K), (M, N, K)
-    for M, N, K in ((2048, 2048, 4096), (2560, 2048, 1024), (256, 256, 256)):
+    for M, N, K in ((2560, 2048, 1024), (256, 256, 256)):
         assert not wide(M, N, K), (M, N, K)
