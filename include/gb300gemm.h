@@ -83,6 +83,44 @@ int gemm_f32(int M, int N, int K, float alpha, const float* A, int lda, const fl
              float beta, float* C, int ldc, cudaStream_t stream);
 
 /*
+ * gemm_f32 for callers that must not allocate.  The source pages have no
+ * counterpart of this entry point: it is a library addition.
+ *
+ * Who needs it: a caller that hands the device's memory to its own pool up
+ * front (a caching allocator that reserves nearly all of it, or a process
+ * under a fixed memory budget) cannot let a library allocate later -- the
+ * allocation may fail, or break the pool's accounting; and a caller on a
+ * latency-critical thread cannot take the device-wide wait that the first
+ * gemm_f32 call on a device makes while it sets up its workspace.
+ *
+ * Same arguments, result and error codes as gemm_f32, the same plan and
+ * the same kernels (so the same bits for the same inputs).  The one
+ * difference: when the plan runs the last partial wave as a stream-K tail,
+ * its partial tiles and flags live in a static device array of this library
+ * (38 MiB of partial tiles plus 9.5 KB of flags, reserved on each device
+ * when the FP32 kernel's module loads), not in an allocated workspace.  The
+ * call allocates no device or host memory and performs no host
+ * synchronisation.
+ *
+ * Limit: the array holds the tail of at most 152 CTAs (one per SM of a
+ * GB300).  A call whose tail would need more (a device with more SMs)
+ * returns GEMM_ERR_UNSUPPORTED, launches nothing, and gemm_get_last_error()
+ * states the bytes needed and held.
+ *
+ * Set-up: the first call on a device (with that device current) looks up
+ * the array's device address; make that first call before any stream
+ * capture.  Each call with a stream-K tail first clears the array's flags
+ * on `stream`.
+ *
+ * Concurrency: there is one array per device, so two gemm_f32_noalloc calls
+ * that execute on one device at the same time (on different streams, with
+ * nothing ordering them) race and may both give wrong results.  Order them
+ * on one stream or with events.  gemm_f32 calls do not share the array.
+ */
+int gemm_f32_noalloc(int M, int N, int K, float alpha, const float* A, int lda, const float* B,
+                     int ldb, float beta, float* C, int ldc, cudaStream_t stream);
+
+/*
  * BF16 GEMM with fp32 accumulation and bf16 C, on the tensor cores
  * (tcgen05.mma fed by TMA, "Kernel 性能从何而来", section "优化阶梯").  Small M
  * (decode-shaped, M <= 16) runs on a memory-bound split-K kernel instead

@@ -39,7 +39,7 @@ PATH_NAMES = {PATH_AUTO: "none", PATH_GENERIC: "generic", PATH_F32_SIMT: "f32_si
               PATH_ATTN: "attention"}
 
 # every symbol the public header declares
-EXPORTS = ("gemm_f32", "gemm_bf16", "gemm_bf16_f32out", "gemm_f32_ex", "gemm_bf16_ex",
+EXPORTS = ("gemm_f32", "gemm_f32_noalloc", "gemm_bf16", "gemm_bf16_f32out", "gemm_f32_ex", "gemm_bf16_ex",
            "gemm_bf16_f32out_ex", "gemm_bf16_swiglu", "gemm_fp8", "gemm_fp8_f32out",
            "gemm_int4_dequant", "gemm_int4_dequant_f32", "gemm_w4a16", "gemm_w4a16_f32out",
            "gemm_int4_repack", "gemm_w4_packed_bytes", "gemm_attention", "gemm_get_last_error",
@@ -77,7 +77,7 @@ def load(path: str | None = None):
             raise RuntimeError(f"CUDA GEMM library not built: {p} (run __graft_entry__.build())")
         lib = ctypes.CDLL(p)
         vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
-        for name in ("gemm_f32", "gemm_bf16", "gemm_bf16_f32out"):
+        for name in ("gemm_f32", "gemm_f32_noalloc", "gemm_bf16", "gemm_bf16_f32out"):
             fn = getattr(lib, name)
             fn.argtypes = [i, i, i, f, vp, i, vp, i, f, vp, i, vp]
             fn.restype = i
@@ -143,6 +143,10 @@ def _check(rc: int):
 
 def gemm_f32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0):
     _check(load().gemm_f32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream))
+
+
+def gemm_f32_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0):
+    _check(load().gemm_f32_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream))
 
 
 def gemm_bf16(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0):

@@ -381,6 +381,103 @@ int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int 
   return GEMM_OK;
 }
 
+// A 2-D tensor map encoded into caller storage (no cache: gemm_f32_noalloc
+// makes no host allocation either).
+int encode_map_into(CUtensorMap* map, const void* ptr, uint64_t cols, uint64_t rows, uint64_t ld_bytes,
+                    uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {ld_bytes};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for %llux%llu ld=%llu", (int)r,
+                (unsigned long long)rows, (unsigned long long)cols, (unsigned long long)ld_bytes);
+  return GEMM_OK;
+}
+
+// gemm_f32_noalloc: the FP32 call of run() (no bias or activation) with the
+// stream-K tail's scratch in the static array of gemm_f32_simt.cu.  Allocates
+// no device or host memory.
+int run_f32_noalloc(int M, int N, int K, float alpha, const float* A, int lda, const float* B,
+                    int ldb, float beta, float* C, int ldc, cudaStream_t stream) {
+  t_msg[0] = '\0';
+  t_last_path = GEMM_PATH_AUTO;
+  t_last_k_split = 1;
+  if (M < 0 || N < 0 || K < 0) return fail(GEMM_ERR_INVALID_ARG, "negative size M=%d N=%d K=%d", M, N, K);
+  if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
+    return fail(GEMM_ERR_INVALID_ARG, "leading dimension too small (lda=%d ldb=%d ldc=%d, K=%d N=%d)",
+                lda, ldb, ldc, K, N);
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (C == nullptr) return fail(GEMM_ERR_INVALID_ARG, "C is NULL");
+  if (K > 0 && (A == nullptr || B == nullptr)) return fail(GEMM_ERR_INVALID_ARG, "A or B is NULL");
+  if ((reinterpret_cast<uintptr_t>(A) % 4) || (reinterpret_cast<uintptr_t>(B) % 4) ||
+      (reinterpret_cast<uintptr_t>(C) % 4))
+    return fail(GEMM_ERR_MISALIGNED, "a matrix pointer is not aligned to its element size");
+
+  DeviceInfo* dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc != GEMM_OK) return rc;
+
+  GemmArgs a;
+  a.M = M; a.N = N; a.K = K; a.alpha = alpha; a.beta = beta;
+  a.A = A; a.lda = lda; a.B = B; a.ldb = ldb; a.C = C; a.ldc = ldc;
+  a.in = Elem::F32; a.out = Elem::F32;
+  a.status = dev->status;
+  a.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  a.bias = nullptr;
+  a.act = kActNone;
+  a.B2 = nullptr;
+  a.swiglu = 0;
+  a.fmt_a = kE4M3;
+  a.fmt_b = kE4M3;
+  a.stall = t_stall;
+
+  const bool tma_ok = K > 0 && aligned16(A) && aligned16(B) && ((size_t)lda * 4) % 16 == 0 &&
+                      ((size_t)ldb * 4) % 16 == 0;
+  const int forced = t_forced_path;
+  if (forced != GEMM_PATH_AUTO && forced != GEMM_PATH_GENERIC &&
+      !(forced == GEMM_PATH_F32_SIMT && tma_ok))
+    return fail(GEMM_ERR_UNSUPPORTED, "forced path %d cannot run this call", forced);
+  int err = cudaSuccess;
+  int path = GEMM_PATH_GENERIC;
+  if (!tma_ok || forced == GEMM_PATH_GENERIC) {
+    err = launch_generic(a, stream);   // no scratch
+  } else {
+    path = GEMM_PATH_F32_SIMT;
+    if (t_forced_bn != 0 && t_forced_bn != kSimtBN8 && t_forced_bn != kSimtBN16)
+      return fail(GEMM_ERR_UNSUPPORTED, "FP32 tiles are 128 or 256 wide, not %d", t_forced_bn);
+    SimtPlan plan;
+    const int forced_tn = t_forced_bn == kSimtBN16 ? 16 : t_forced_bn == kSimtBN8 ? 8 : 0;
+    if ((err = plan_f32_simt(M, N, K, dev->num_sms, forced_tn, &plan)) != cudaSuccess)
+      return fail(GEMM_ERR_CUDA, "FP32 planning failed: %s", cudaGetErrorString((cudaError_t)err));
+    const int ctas = simt_stream_k_ctas(M, N, K, plan, dev->num_sms);
+    if (ctas > kStaticScratchCtas)
+      return fail(GEMM_ERR_UNSUPPORTED,
+                  "gemm_f32_noalloc: the stream-K tail of this %dx%dx%d call needs scratch for %d CTAs "
+                  "(%zu bytes); the static scratch holds %d CTAs (%zu bytes): use gemm_f32",
+                  M, N, K, ctas, (size_t)ctas * 2 * kSimtBM * kSimtBN16 * sizeof(float),
+                  kStaticScratchCtas, simt_static_scratch_bytes());
+    CUtensorMap mA, mB;
+    if ((rc = encode_map_into(&mA, A, K, M, (uint64_t)lda * 4, kSimtBK, kSimtBM,
+                              CU_TENSOR_MAP_SWIZZLE_64B)) != GEMM_OK)
+      return rc;
+    if ((rc = encode_map_into(&mB, B, N, K, (uint64_t)ldb * 4, (uint32_t)(16 * plan.tn), kSimtBK,
+                              CU_TENSOR_MAP_SWIZZLE_NONE)) != GEMM_OK)
+      return rc;
+    err = launch_f32_simt_static(a, &mA, &mB, plan, dev->num_sms, stream, &t_last_k_split);
+    if (err == cudaSuccess) t_last_bn = 16 * plan.tn;
+  }
+  if (err != cudaSuccess)
+    return fail(GEMM_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString((cudaError_t)err));
+  t_last_path = path;
+  return GEMM_OK;
+}
+
 int int4_dequant(const uint8_t* q, int K, int N, int ldq, const void* scales, int lds, int group,
                 int zero, void* W, int ldw, bool out_bf16, cudaStream_t stream) {
   t_msg[0] = '\0';
@@ -553,6 +650,11 @@ int gemm_f32(int M, int N, int K, float alpha, const float* A, int lda, const fl
              float beta, float* C, int ldc, cudaStream_t stream) {
   return g3::run(Elem::F32, Elem::F32, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, nullptr,
                  g3::kActNone, stream);
+}
+
+int gemm_f32_noalloc(int M, int N, int K, float alpha, const float* A, int lda, const float* B,
+                     int ldb, float beta, float* C, int ldc, cudaStream_t stream) {
+  return g3::run_f32_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
 }
 
 int gemm_bf16(int M, int N, int K, float alpha, const gemm_bf16_t* A, int lda, const gemm_bf16_t* B,

@@ -956,4 +956,140 @@ void sk_clear_flags() {
     cudaMemset(w.flags, 0, kSkSlots * w.slot_flags * sizeof(unsigned));
 }
 
+// ------------------------------------------------------ gemm_f32_noalloc
+// The scratch of gemm_f32_noalloc: the partial tiles (kSkMaxSeg per CTA,
+// 128 x 256 floats each) and the per-warp release flags of one stream-K tail
+// of up to kStaticScratchCtas CTAs -- 38 MiB of partials and 9.5 KB of
+// flags, reserved on each device when this file's module loads rather than
+// allocated by a call.  There is one per device: two calls that execute on
+// one device at the same time share it and race.
+constexpr size_t kStaticPartialFloats = (size_t)kStaticScratchCtas * kSkMaxSeg * BM * kSimtBN16;
+constexpr size_t kStaticFlagWords = (size_t)kStaticScratchCtas * kSkMaxSeg * COMPUTE_WARPS;
+static_assert(kStaticPartialFloats % 64 == 0, "flags start on a 256-byte boundary");
+static __device__ __align__(256) float g_static_scratch[kStaticPartialFloats + kStaticFlagWords];
+
+namespace {
+
+struct StaticScratch {
+  std::atomic<bool> ready{false};   // published after `base` is set
+  float* base = nullptr;
+};
+StaticScratch g_static[64];
+std::mutex g_static_mu;
+
+// Set-up, once per device with that device current: the array's device
+// address (no allocation; nothing is launched).
+cudaError_t static_scratch(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  StaticScratch& st = g_static[dev];
+  if (!st.ready.load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!st.ready.load(std::memory_order_relaxed)) {
+      float* ptr = nullptr;
+      e = cudaGetSymbolAddress((void**)&ptr, g_static_scratch);
+      if (e != cudaSuccess) return e;
+      if (ptr == nullptr) return cudaErrorInvalidSymbol;
+      st.base = ptr;
+      st.ready.store(true, std::memory_order_release);
+    }
+  }
+  *out = st.base;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+size_t simt_static_scratch_bytes() { return sizeof(float) * (kStaticPartialFloats + kStaticFlagWords); }
+
+int simt_stream_k_ctas(int M, int N, int K, const SimtPlan& plan, int num_sms) {
+  if (plan.tn != 16 || plan.split != 0 || M <= 0 || N <= 0 || num_sms <= 0) return 0;
+  const long long tiles = (long long)((M + BM - 1) / BM) * ((N + kSimtBN16 - 1) / kSimtBN16);
+  const long long rest = tiles % ((long long)SimtCfg<16>::CTAS_PER_SM * num_sms);
+  if (rest == 0) return 0;
+  return sk_ctas(rest, (K + BK - 1) / BK, num_sms);
+}
+
+int launch_f32_simt_static(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
+                           const SimtPlan& plan, int num_sms, cudaStream_t s, int* k_split) {
+  *k_split = 1;
+  if (a.bias != nullptr || a.act != kActNone) return cudaErrorInvalidValue;
+  float* scratch = nullptr;
+  cudaError_t e = static_scratch(&scratch);
+  if (e != cudaSuccess) return e;
+  SimtParams p;
+  p.a = a;
+  const int bn = plan.tn == 16 ? kSimtBN16 : kSimtBN8;
+  p.tiles_m = (a.M + BM - 1) / BM;
+  p.tiles_n = (a.N + bn - 1) / bn;
+  p.c_vec = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && (a.ldc % 4) == 0) ? 1 : 0;
+  p.tile_base = 0;
+  p.sk_units = 0;
+  p.sk_ctas = 0;
+  p.sk_partials = nullptr;
+  p.sk_flags = nullptr;
+  const long long tiles = (long long)p.tiles_m * p.tiles_n;
+  if (tiles <= 0) return cudaSuccess;
+  if (tiles * 4 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  // the narrow tiles (whole waves, or clusters sharing a tile through
+  // distributed shared memory) and wide tiles without a tail use no scratch
+  if (plan.tn == 8) return launch_plan<8, false>(mapA, mapB, p, tiles, plan, num_sms, s, k_split);
+  if (plan.tn != 16) return cudaErrorInvalidValue;
+  if (plan.split == 1) return launch_plan<16, false>(mapA, mapB, p, tiles, plan, num_sms, s, k_split);
+  if (plan.split != 0) return cudaErrorInvalidValue;
+
+  // wide tiles: whole waves, then the stream-K tail on the static scratch
+  using Cfg = SimtCfg<16>;
+  static std::atomic<uint64_t> smem_first{0}, smem_sk{0};
+  auto first_kernel = sgemm_tma_kernel<16, false, 1, true>;
+  auto sk_kernel = sgemm_tma_kernel<16, false, 0, false>;
+  if ((e = set_smem_once(smem_first, first_kernel, Cfg::SMEM_BYTES)) != cudaSuccess) return e;
+  if ((e = set_smem_once(smem_sk, sk_kernel, Cfg::SMEM_BYTES)) != cudaSuccess) return e;
+  const long long slots = (long long)Cfg::CTAS_PER_SM * num_sms;
+  const long long rest = tiles % slots, whole = tiles - rest;
+  if (rest == 0) return cudaErrorInvalidValue;  // the plan splits only a partial wave
+  const int k_slices = (a.K + BK - 1) / BK;
+  const int G = sk_ctas(rest, k_slices, num_sms);
+  if (G > kStaticScratchCtas) return cudaErrorInvalidValue;
+  unsigned* flags = reinterpret_cast<unsigned*>(scratch + kStaticPartialFloats);
+  // the flags must be zero when the tail starts: cleared on this stream
+  // before the first launch, so a call after one that timed out (and left
+  // flags raised) starts clean
+  e = cudaMemsetAsync(flags, 0, (size_t)G * kSkMaxSeg * COMPUTE_WARPS * sizeof(unsigned), s);
+  if (e != cudaSuccess) return e;
+  if (whole > 0) {
+    first_kernel<<<(unsigned)whole, THREADS, Cfg::SMEM_BYTES, s>>>(*mapA, *mapB, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  p.tile_base = (int)whole;
+  p.sk_units = rest * k_slices;
+  p.sk_ctas = G;
+  p.sk_partials = scratch;
+  p.sk_flags = flags;
+  // the most CTAs that meet in one tile (the kernel's arithmetic)
+  const long long U = p.sk_units;
+  int share = 1;
+  for (long long t = 0; t < rest; ++t) {
+    const long long T0 = t * k_slices, T1 = T0 + k_slices;
+    const long long cfirst = ((T0 + 1) * G + U - 1) / U - 1, clast = (T1 * G + U - 1) / U - 1;
+    if (clast - cfirst + 1 > share) share = (int)(clast - cfirst + 1);
+  }
+  *k_split = share;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3((unsigned)G, 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = whole > 0 ? 1 : 0;   // overlap the whole waves' end only after them
+  e = cudaLaunchKernelEx(&cfg, sk_kernel, *mapA, *mapB, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 }  // namespace g3

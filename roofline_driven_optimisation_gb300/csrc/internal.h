@@ -106,6 +106,20 @@ int launch_f32_simt(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMa
                     const SimtPlan& plan, int num_sms, cudaStream_t s, int* k_split);
 constexpr int kSimtBM = 128, kSimtBK = 16, kSimtBN8 = 128, kSimtBN16 = 256;
 
+// gemm_f32_noalloc: the FP32 SIMT plan run with the stream-K tail's partial
+// tiles and flags in a static device array instead of the workspace, so the
+// call allocates nothing.  The array holds the tail of up to
+// kStaticScratchCtas CTAs; simt_stream_k_ctas gives the CTAs the tail of
+// `plan` needs for this shape (0: the plan has no stream-K tail).
+constexpr int kStaticScratchCtas = 152;
+int simt_stream_k_ctas(int M, int N, int K, const SimtPlan& plan, int num_sms);
+// Bytes of the static array (partial tiles and flags).
+size_t simt_static_scratch_bytes();
+// Plain GEMMs only (no bias or activation); the caller has checked that
+// simt_stream_k_ctas() <= kStaticScratchCtas.
+int launch_f32_simt_static(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
+                           const SimtPlan& plan, int num_sms, cudaStream_t s, int* k_split);
+
 // BF16 tcgen05 kernel: TMA tiles of A (64 k x 128 m) and B (64 n x 64 k),
 // 128-byte swizzle; C tiles of 128 x bn with bn from choose_tc_bn().
 int choose_tc_bn(int M, int N, int num_sms);
