@@ -24,8 +24,9 @@
  *   - M == 0 or N == 0 is a no-op.  K == 0 gives C = beta*C.
  *   - The call is asynchronous on `stream` (0 = legacy default stream).  It
  *     performs no host synchronisation and no device allocation, except the
- *     first gemm_f32 / gemm_f32_ex call on a device: it allocates the FP32
- *     kernel's stream-K workspace (four slots of 39.8 MB of partial tiles on
+ *     first GEMM call (gemm_f32*, gemm_bf16*, gemm_fp8*) on a device: it
+ *     allocates the stream-K workspace that the FP32 SIMT and CTA-pair
+ *     tensor-core kernels share (four slots of 39.8 MB of partial tiles on
  *     152 SMs, plus flags; kept until the process exits), zeroes its flags
  *     and waits for the device once.
  *   - Fast paths need 16-byte-aligned A and B and lda, ldb whose byte size is
@@ -33,12 +34,12 @@
  *     There is no CPU fallback.
  *   - Results of one call are deterministic: the same inputs give the same
  *     bits on every run (fixed reduction order, including split-K).
- *   - Calls made concurrently from several host threads are safe.  FP32
- *     calls whose partial last wave runs stream-K (gemm_last_k_split() > 1
- *     on a wide tile) take the four workspace slots in turn: at most four
- *     of them may execute on the GPU at the same time (on different streams,
- *     or in graphs launched side by side); a fifth would share a slot with
- *     the first and race with it.
+ *   - Calls made concurrently from several host threads are safe.  Calls
+ *     whose partial last wave runs stream-K (FP32: gemm_last_k_split() > 1
+ *     on a wide tile; tensor core: gemm_last_tc_pair() == 6) take the four
+ *     workspace slots in turn: at most four of them may execute on the GPU
+ *     at the same time (on different streams, or in graphs launched side by
+ *     side); a fifth would share a slot with the first and race with it.
  *   - Calls can be captured into a CUDA graph (stream capture) once the same
  *     kind of call has run on the device: the first call of a kernel family
  *     on a device sets kernel attributes and queries occupancy.
@@ -382,19 +383,24 @@ int gemm_force_tc_pair(int mode);
 
 /* For the last tensor-core call on this host thread: 1 if it ran on single
  * CTAs, 2 on CTA pairs, 4 on CTA pairs with the tiles of the last partial
- * wave split into half-width tiles, 0 if there was none. */
+ * wave split into half-width tiles, 6 on CTA pairs with those tiles run
+ * stream-K, 0 if there was none. */
 int gemm_last_tc_pair(void);
 
 /*
  * Allow (1, the default) or forbid (0), for later calls on this host thread,
- * that the tiles of a partial last wave run split: the CTA-pair kernel runs
- * each as two half-width tiles on otherwise idle pairs; the FP32 SIMT kernel
- * runs them as a second launch in which a cluster of CTAs shares each
- * tile's K range (partial sums added in rank order, in distributed shared
- * memory; clusters of four) on its narrow tiles, or stream-K on its wide
- * tiles: the partial wave's K-slices spread evenly over up to one CTA per SM,
- * partial tiles exchanged through the workspace and added in CTA order.  For
- * A/B measurements and tests.
+ * that the tiles of a partial last wave run split.  The CTA-pair kernel's
+ * 256-wide tiles run them either as two half-width tiles each on otherwise
+ * idle pairs (bf16 only) or stream-K: the tail's K-steps spread evenly over
+ * the pairs, each tile's partial sums added by one pair in pair order; a
+ * wave model picks one.  The FP32 SIMT kernel runs them as a second launch
+ * in which a cluster of four CTAs shares each tile's K range (partial sums
+ * added in rank order, in distributed shared memory) on its narrow tiles,
+ * or stream-K on its wide tiles (the K-slices over up to one CTA per SM).
+ * 2 pins the CTA-pair kernel's stream-K tail and 3 its half-width tail
+ * wherever the shape has a partial wave (and, for 3, the half tiles fit in
+ * the pairs); the FP32 kernel treats 2 and 3 as 1.  Stream-K partial tiles
+ * meet in the device's stream-K workspace.  For A/B measurements and tests.
  */
 int gemm_force_split_tiles(int enable);
 

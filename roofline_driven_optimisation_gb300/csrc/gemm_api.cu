@@ -251,6 +251,11 @@ int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int 
   DeviceInfo* dev = nullptr;
   int rc = device_info(&dev);
   if (rc != GEMM_OK) return rc;
+  // the first GEMM call on a device sets up the stream-K workspace, whatever
+  // its shape, so that later calls (and stream captures) never allocate
+  const cudaError_t we = stream_k_setup(dev->num_sms);
+  if (we != cudaSuccess)
+    return fail(GEMM_ERR_CUDA, "stream-K workspace: %s", cudaGetErrorString(we));
 
   GemmArgs a;
   a.M = M; a.N = N; a.K = K; a.alpha = alpha; a.beta = beta;
@@ -316,10 +321,11 @@ int run(Elem in, Elem out, int M, int N, int K, float alpha, const void* A, int 
         if ((rc = make_map(B, N, K, (uint64_t)ldb, 128, kF8BK, CU_TENSOR_MAP_DATA_TYPE_UINT8,
                            CU_TENSOR_MAP_SWIZZLE_128B, &mB)) != GEMM_OK)
           return rc;
-        err = launch_fp8_tc_pair(a, mA, mB, dev->num_sms, stream);
+        int schedule = 2;
+        err = launch_fp8_tc_pair(a, mA, mB, dev->num_sms, stream, &schedule);
         if (err == cudaSuccess) {
           t_last_bn = 256;
-          t_last_pair = 2;
+          t_last_pair = schedule;
         }
         break;
       }
@@ -639,6 +645,7 @@ __global__ void selftest_wait_kernel(int* status, uint64_t timeout_ns) {
 }  // namespace
 
 bool split_tiles_enabled() { return t_split_tiles != 0; }
+int split_tiles_mode() { return t_split_tiles; }
 
 }  // namespace g3
 
@@ -798,7 +805,7 @@ int gemm_force_tc_pair(int mode) {
 int gemm_last_tc_pair(void) { return g3::t_last_pair; }
 
 int gemm_force_split_tiles(int enable) {
-  if (enable != 0 && enable != 1) return g3::fail(GEMM_ERR_INVALID_ARG, "enable must be 0 or 1");
+  if (enable < 0 || enable > 3) return g3::fail(GEMM_ERR_INVALID_ARG, "enable must be 0, 1, 2 or 3");
   g3::t_split_tiles = enable;
   return GEMM_OK;
 }

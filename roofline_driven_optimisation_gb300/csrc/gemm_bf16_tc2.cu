@@ -48,7 +48,9 @@
 #include <mutex>
 
 #include "internal.h"
+#include "plan.h"
 #include "ptx.cuh"
+#include "stream_k.cuh"
 #include "tc_epilogue.cuh"
 
 namespace g3 {
@@ -106,13 +108,164 @@ __device__ __forceinline__ void pair_tile_coords(int tile, const TcParams& p, in
   n0 = (local / gsize) * BN;
 }
 
+// TMEM -> registers for one warp's 32 accumulator rows, `chunks` chunks of
+// 32 columns from t_row, each handed to use(c, r); arrives on the
+// accumulator-empty barrier `tempty` as soon as the last load has landed.
+// (Keeping the next chunk's load in flight while a chunk is stored, and
+// staging chunks through shared memory for row-contiguous stores, were both
+// timed on GB300 and changed nothing.)
+template <typename Use>
+__device__ __forceinline__ void drain_chunks(uint32_t t_row, int chunks, uint32_t tempty, Use&& use) {
+#pragma unroll 1
+  for (int c = 0; c < chunks; ++c) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(t_row + c * 32, r);
+    tc_wait_ld();
+    if (c == chunks - 1) {
+      tc_fence_before();
+      mbar_arrive_remote(tempty);
+    }
+    use(c, r);
+  }
+}
+
+// Stream-K piece end in the epilogue of one warp (32 rows of one CTA's 128):
+// a contributor leaves its rows of the partial tile in its workspace slot and
+// raises its flag; the finisher waits (bounded) for the other pairs' flags of
+// the same rows, adds their parts to its own in pair order (fixed by the
+// shape, so every call gives the same bits), stores C through the usual
+// epilogue and lowers the flags.  A warp's part is laid out chunk by chunk
+// (32 columns = 8 float4 per row), each float4 of the 32 rows contiguous, so
+// every warp access is 512 contiguous bytes.  t_row: this warp's accumulator
+// row in TMEM; tempty: the accumulator-empty barrier to arrive on once TMEM
+// is read.  Returns false after a bounded wait ran out.
+constexpr int kSkMaxWorkers = 16;   // pairs meeting in one tile (at most 5 in practice)
+template <int BN, bool OUT_BF16>
+__device__ __forceinline__ bool sk_piece_end(const TcParams& p, long long u, int pair_id,
+                                             uint32_t rank, int quarter, int lane, long long m,
+                                             int n0, uint32_t t_row, uint32_t tempty,
+                                             volatile int* abort_flag) {
+  const GemmArgs& a = p.a;
+  const long long U = p.sk_units;
+  const int G = p.sk_pairs;
+  const long long T0 = u - u % p.k_tiles, T1 = T0 + p.k_tiles;
+  int cfirst, clast, fin;
+  sk_tile_workers(T0, T1, U, G, &cfirst, &clast, &fin);
+  auto slot_of = [&](int c) {
+    return c * 2 + (int)(T0 / p.k_tiles - sk_begin(c, U, G) / p.k_tiles);
+  };
+  const int flag_idx = (int)rank * 4 + quarter;
+  // this warp's block of a slot: 32 rows x BN floats
+  auto block = [&](int c) {
+    return reinterpret_cast<float4*>(p.sk_partials + (size_t)slot_of(c) * (BM * BN) +
+                                     (size_t)flag_idx * (32 * BN));
+  };
+  if (pair_id != fin) {
+    // ------------------------------------------------ contributor
+    float4* dst = block(pair_id);
+    drain_chunks(t_row, BN / 32, tempty, [&](int c, uint32_t (&r)[32]) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        dst[(c * 8 + q) * 32 + lane] =
+            make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                        __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+    });
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) st_release_u32(p.sk_flags + slot_of(pair_id) * 8 + flag_idx, 1u);
+    return true;
+  }
+  // -------------------------------------------------- finisher
+  bool ok = clast - cfirst < kSkMaxWorkers;
+  if (lane == 0 && ok) {
+    for (int c = cfirst; ok && c <= clast; ++c) {
+      if (c == pair_id) continue;
+      const unsigned* flag = p.sk_flags + slot_of(c) * 8 + flag_idx;
+      if (ld_acquire_u32(flag) != 0u) continue;
+      const uint64_t t0 = globaltimer_ns();
+      while (true) {
+        bool got = false;
+#pragma unroll 1
+        for (int i = 0; i < 32 && !got; ++i) got = ld_acquire_u32(flag) != 0u;
+        if (got) break;
+        if (*abort_flag || globaltimer_ns() - t0 > a.timeout_ns) {
+          ok = false;
+          break;
+        }
+      }
+    }
+  }
+  if (lane == 0 && !ok) {
+    if (!*abort_flag) report_status(a.status, 5, kSiteTc2StreamK);
+    *abort_flag = 1;
+  }
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  if (!ok) {
+    // TMEM is still handed back, so the MMA issuer's own wait is not the
+    // one that runs out
+    tc_fence_before();
+    mbar_arrive_remote(tempty);
+    return false;
+  }
+  __syncwarp();
+  __threadfence();
+  // the other parts in pair order: the j-th is pair cfirst + j, skipping this one
+  const int n_src = clast - cfirst;
+  auto src_of = [&](int j) -> const float4* {
+    const int c = cfirst + j;
+    return block(c >= pair_id ? c + 1 : c);
+  };
+  drain_chunks(t_row, BN / 32, tempty, [&](int c, uint32_t (&r)[32]) {
+    // two parts' loads in flight at a time (L2 loads: other SMs wrote them),
+    // added in order after this pair's own part
+#pragma unroll 1
+    for (int j = 0; j < n_src; j += 2) {
+      const bool two = j + 1 < n_src;
+      const float4* s0 = src_of(j) + c * 8 * 32 + lane;
+      const float4* s1 = two ? src_of(j + 1) + c * 8 * 32 + lane : s0;
+      float4 v0[8], v1[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        v0[q] = __ldcg(s0 + q * 32);
+        v1[q] = __ldcg(s1 + q * 32);
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        r[4 * q] = __float_as_uint(__uint_as_float(r[4 * q]) + v0[q].x);
+        r[4 * q + 1] = __float_as_uint(__uint_as_float(r[4 * q + 1]) + v0[q].y);
+        r[4 * q + 2] = __float_as_uint(__uint_as_float(r[4 * q + 2]) + v0[q].z);
+        r[4 * q + 3] = __float_as_uint(__uint_as_float(r[4 * q + 3]) + v0[q].w);
+      }
+      if (two) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          r[4 * q] = __float_as_uint(__uint_as_float(r[4 * q]) + v1[q].x);
+          r[4 * q + 1] = __float_as_uint(__uint_as_float(r[4 * q + 1]) + v1[q].y);
+          r[4 * q + 2] = __float_as_uint(__uint_as_float(r[4 * q + 2]) + v1[q].z);
+          r[4 * q + 3] = __float_as_uint(__uint_as_float(r[4 * q + 3]) + v1[q].w);
+        }
+      }
+    }
+    if (m < a.M && n0 + c * 32 < a.N) store_row32<OUT_BF16>(p, m, (long long)n0 + c * 32, r);
+  });
+  __syncwarp();
+  if (lane == 0) {
+    for (int c = cfirst; c <= clast; ++c)
+      if (c != pair_id) p.sk_flags[slot_of(c) * 8 + flag_idx] = 0u;   // ready for the next call
+  }
+  return true;
+}
+
 // mapB2 is read only by the SwiGLU variant (the up-projection).
-template <int BN, bool OUT_BF16, bool SW, bool F8>
+// SK: the tiles past the whole waves run stream-K (bf16 and FP8 instances of
+// the 256-wide tile; the plain instances have no trace of it).
+template <int BN, bool OUT_BF16, bool SW, bool F8, bool SK = false>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_bf16_tc2_kernel(const __grid_constant__ CUtensorMap mapA,
                          const __grid_constant__ CUtensorMap mapB,
                          const __grid_constant__ CUtensorMap mapB2, const TcParams p) {
   static_assert(!SW || (BN == 256 && OUT_BF16 && !F8), "SwiGLU runs on the 256-wide bf16 instance");
+  static_assert(!SK || (BN == 256 && !SW), "stream-K runs on the 256-wide plain and FP8 instances");
   constexpr int OUT_BN = SW ? BN / 2 : BN;  // C columns per tile
   using Cfg = PairCfg<BN, F8>;
   using G = Geom<F8>;
@@ -148,11 +301,45 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int pair_id = blockIdx.x >> 1;
   const int num_pairs = gridDim.x >> 1;
   // this pair's work items: whole tiles, then at most one half-width item
+  // or (SK) the pieces of its stream-K range: units [sk_b, sk_e) of the
+  // tail, in tile sk_t0 and, past its end, in the next tile
   const int n_dp = pair_id < p.dp_tiles ? (p.dp_tiles - pair_id + num_pairs - 1) / num_pairs : 0;
-  const int n_items = n_dp + (pair_id < p.half_tiles ? 1 : 0);
+  long long sk_b = 0, sk_e = 0;
+  int sk_t0 = 0, sk_pieces = 0;
+  if constexpr (SK) {
+    if (pair_id < p.sk_pairs) {
+      sk_b = sk_begin(pair_id, p.sk_units, p.sk_pairs);
+      sk_e = sk_begin(pair_id + 1, p.sk_units, p.sk_pairs);
+      sk_t0 = (int)(sk_b / p.k_tiles);
+      sk_pieces = sk_e <= sk_b ? 0 : sk_e > (long long)(sk_t0 + 1) * p.k_tiles ? 2 : 1;
+    }
+  }
+  const int n_items = n_dp + (SK ? sk_pieces : (pair_id < p.half_tiles ? 1 : 0));
+  // K-steps [k_lo, k_hi) of item i; u: its first unit in the stream-K run
+  auto item_k = [&](int i, int& k_lo, int& k_hi, long long& u) {
+    k_lo = 0;
+    k_hi = p.k_tiles;
+    u = 0;
+    if constexpr (SK) {
+      if (i >= n_dp) {
+        const long long t0_unit = (long long)sk_t0 * p.k_tiles;
+        if (i == n_dp) {
+          u = sk_b;
+          k_lo = (int)(sk_b - t0_unit);
+          k_hi = (int)((sk_e < t0_unit + p.k_tiles ? sk_e : t0_unit + p.k_tiles) - t0_unit);
+        } else {
+          u = t0_unit + p.k_tiles;
+          k_hi = (int)(sk_e - u);
+        }
+      }
+    }
+  };
   auto item = [&](int i, int& m0, int& n0, int& bn) {
     if (i < n_dp) {
       pair_tile_coords<OUT_BN>(pair_id + i * num_pairs, p, m0, n0);
+      bn = BN;
+    } else if constexpr (SK) {
+      pair_tile_coords<OUT_BN>(p.dp_tiles + sk_t0 + (i - n_dp), p, m0, n0);
       bn = BN;
     } else {
       pair_tile_coords<OUT_BN>(p.dp_tiles + pair_id / 2, p, m0, n0);
@@ -195,13 +382,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int i = 0; ok && i < n_items; ++i) {
-        int m0, n0, bn;
+        int m0, n0, bn, k_lo, k_hi;
+        long long u;
         item(i, m0, n0, bn);
+        item_k(i, k_lo, k_hi, u);
         const int a_row = m0 + (int)rank * BM_CTA;
         const int b_col = n0 + (int)rank * (SW ? OUT_BN / 2 : bn / 2);
         const int b_boxes = bn / 2 / G::BOX_N;
         const uint32_t tx_bytes = 2u * (A_STAGE_BYTES + b_boxes * B_BOX_BYTES);
-        for (int kt = 0; kt < p.k_tiles; ++kt) {
+        for (int kt = k_lo; kt < k_hi; ++kt) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, a.timeout_ns, abort_flag)) {
             if (!*abort_flag) report_status(a.status, 5, kSiteTc2Producer);
             *abort_flag = 1;
@@ -257,7 +446,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           ok = false;
         }
         for (int i = 0; ok && i < n_items; ++i) {
-          const uint32_t idesc = i < n_dp ? idesc_full : idesc_half;
+          // stream-K pieces are whole-width tiles; only the half-width tail
+          // (bf16 instances without SK; never FP8) uses the 128-wide descriptor
+          const uint32_t idesc = (SK || F8 || i < n_dp) ? idesc_full : idesc_half;
           if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, a.timeout_ns, abort_flag)) {
             if (!*abort_flag) report_status(a.status, 5, kSiteTc2Mma);
             *abort_flag = 1;
@@ -265,7 +456,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-          for (int kt = 0; kt < p.k_tiles; ++kt) {
+          int k_lo, k_hi;
+          long long u;
+          item_k(i, k_lo, k_hi, u);
+          for (int kt = k_lo; kt < k_hi; ++kt) {
             if (!mbar_wait(full_bar(stage), phase, a.timeout_ns, abort_flag)) {
               if (!*abort_flag) report_status(a.status, 5, kSiteTc2Mma);
               *abort_flag = 1;
@@ -278,10 +472,11 @@ __global__ void __launch_bounds__(THREADS, 1)
               const uint64_t adesc = smem_desc_sw128(a_tile(stage) + kk * G::A_KSTEP, 16, 1024);
               const uint64_t bdesc =
                   smem_desc_sw128(b_tile(stage) + kk * G::B_KSTEP, B_BOX_BYTES, 1024);
+              const uint32_t accumulate = (kt != k_lo || kk != 0) ? 1u : 0u;
               if constexpr (F8)
-                tc_mma_f8_pair(d_tmem, adesc, bdesc, idesc, (kt | kk) != 0 ? 1u : 0u);
+                tc_mma_f8_pair(d_tmem, adesc, bdesc, idesc, accumulate);
               else
-                tc_mma_f16_pair(d_tmem, adesc, bdesc, idesc, (kt | kk) != 0 ? 1u : 0u);
+                tc_mma_f16_pair(d_tmem, adesc, bdesc, idesc, accumulate);
             }
             issued_any = true;
             tc_commit_pair_mc(empty_bar(stage), kBothCtas);  // frees the stage in both CTAs
@@ -322,7 +517,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const long long m = (long long)m0 + rank * BM_CTA + quarter * 32 + lane;
       const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-      if constexpr (SW) {
+      if (SK && i >= n_dp) {
+        // ------------------------------------------ stream-K piece end
+        int k_lo, k_hi;
+        long long u;
+        item_k(i, k_lo, k_hi, u);
+        if (!sk_piece_end<BN, OUT_BF16>(p, u, pair_id, rank, quarter, lane, m, n0, t_row,
+                                        acc == 0 ? lead_tempty0 : lead_tempty1, abort_flag))
+          break;
+      } else if constexpr (SW) {
 #pragma unroll 1
         for (int c = 0; c < OUT_BN / 32; ++c) {
           // output columns n0 + 32c .. +32: gate at accumulator column
@@ -342,17 +545,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (m < a.M && n0 + c * 32 < a.N) store_row32<OUT_BF16>(p, m, (long long)n0 + c * 32, r);
         }
       } else {
-#pragma unroll 1
-        for (int c = 0; c < bn / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(t_row + c * 32, r);
-          tc_wait_ld();
-          if (c == bn / 32 - 1) {
-            tc_fence_before();
-            mbar_arrive_remote(acc == 0 ? lead_tempty0 : lead_tempty1);
-          }
-          if (m < a.M && n0 + c * 32 < a.N) store_row32<OUT_BF16>(p, m, (long long)n0 + c * 32, r);
-        }
+        drain_chunks(t_row, bn / 32, acc == 0 ? lead_tempty0 : lead_tempty1,
+                     [&](int c, uint32_t (&r)[32]) {
+                       if (m < a.M && n0 + c * 32 < a.N)
+                         store_row32<OUT_BF16>(p, m, (long long)n0 + c * 32, r);
+                     });
       }
       if (++acc == 2) {
         acc = 0;
@@ -426,8 +623,45 @@ int launch_pair_impl(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorM
   p.c_vec = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && ((a.ldc * out_bytes) % 16) == 0) ? 1 : 0;
   const int pairs = info[dev].max_clusters;
   const long long rem = tiles % pairs;
+  // the tiles past the last whole wave: whole (0), as half-width tiles (1)
+  // or stream-K over the pairs (2), as the tail model or the hook says
+  int tail = 0, sk_pairs = 0;
+  const int mode = split_tiles_mode();
+  if (!SW && BN == 256 && mode != 0 && rem > 0) {
+    const bool half_ok = !F8 && 2 * rem <= pairs;
+    sk_pairs = plan::tc_sk_pairs(rem, p.k_tiles, pairs);
+    if (mode == 2) tail = sk_pairs > 0 ? 2 : 0;
+    else if (mode == 3) tail = half_ok ? 1 : 0;
+    else tail = plan::tc_tail(rem, pairs, half_ok, sk_pairs);
+  }
   int clusters;
-  if (!SW && !F8 && BN == 256 && split_tiles_enabled() && rem > 0 && 2 * rem <= pairs) {
+  if constexpr (!SW && BN == 256) {
+    if (tail == 2) {
+      static std::atomic<uint64_t> smem_sk{0};
+      auto sk_kernel = gemm_bf16_tc2_kernel<BN, OUT_BF16, SW, F8, true>;
+      cudaError_t e = set_smem_once(smem_sk, sk_kernel, Cfg::SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+      float* partials = nullptr;
+      unsigned* flags = nullptr;
+      size_t slot_floats = 0, slot_flags = 0;
+      if ((e = stream_k_slot(num_sms, &partials, &flags, &slot_floats, &slot_flags)) != cudaSuccess)
+        return e;
+      if ((size_t)sk_pairs * 2 * BM * BN > slot_floats || (size_t)sk_pairs * 2 * 8 > slot_flags)
+        return cudaErrorInvalidValue;
+      p.dp_tiles = (int)(tiles - rem);
+      p.half_tiles = 0;
+      p.sk_pairs = sk_pairs;
+      p.sk_units = rem * p.k_tiles;
+      p.sk_partials = partials;
+      p.sk_flags = flags;
+      *schedule = 6;
+      cfg.gridDim = dim3(2 * pairs, 1, 1);
+      e = cudaLaunchKernelEx(&cfg, sk_kernel, *mapA, *mapB, *mapB, p);
+      if (e != cudaSuccess) return e;
+      return cudaGetLastError();
+    }
+  }
+  if (tail == 1) {
     p.dp_tiles = (int)(tiles - rem);
     p.half_tiles = (int)(2 * rem);
     clusters = pairs;
@@ -459,12 +693,11 @@ int launch_bf16_tc_pair(const GemmArgs& a, const CUtensorMap* mapA, const CUtens
 }
 
 int launch_fp8_tc_pair(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
-                       int num_sms, cudaStream_t s) {
+                       int num_sms, cudaStream_t s, int* schedule) {
   if (a.in != Elem::FP8 || a.swiglu) return cudaErrorInvalidValue;
-  int schedule = 0;
   return a.out == Elem::BF16
-             ? launch_pair_impl<256, true, false, true>(a, mapA, mapB, nullptr, num_sms, s, &schedule)
-             : launch_pair_impl<256, false, false, true>(a, mapA, mapB, nullptr, num_sms, s, &schedule);
+             ? launch_pair_impl<256, true, false, true>(a, mapA, mapB, nullptr, num_sms, s, schedule)
+             : launch_pair_impl<256, false, false, true>(a, mapA, mapB, nullptr, num_sms, s, schedule);
 }
 
 int launch_bf16_swiglu_pair(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,

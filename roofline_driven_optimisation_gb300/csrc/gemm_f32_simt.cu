@@ -59,6 +59,7 @@
 #include "internal.h"
 #include "plan.h"
 #include "ptx.cuh"
+#include "stream_k.cuh"
 
 namespace g3 {
 namespace {
@@ -105,20 +106,6 @@ struct SimtParams {
 // Stream-K: a CTA's K-slice range is at most one tile long, so it touches at
 // most two tiles.
 constexpr int kSkMaxSeg = 2;
-
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// The CTAs of a stream-K launch: CTA c owns K-slices [sk_begin(c), sk_begin(c + 1)).
-__device__ __forceinline__ long long sk_begin(long long c, long long units, int ctas) {
-  return c * units / ctas;
-}
 
 __device__ __forceinline__ float2 lds64(uint32_t addr) {
   float2 v;
@@ -191,6 +178,65 @@ __device__ __forceinline__ void store_quad(const GemmArgs& a, int c_vec, long lo
   }
 }
 
+// alpha * acc (+ beta * C_old, bias, activation) for this thread's 8 rows x
+// TN columns of the C tile at (tm0, tn0).  With beta != 0 the old C of four
+// rows' quads is loaded before any of them is stored: as far as the compiler
+// knows a store to C may alias a later load from C, so the load-store pairs
+// of store_quad alone would wait out the memory latency once per quad (32
+// times per wide tile, with one CTA per SM and nothing else to run).
+template <int TN, bool EPI>
+__device__ __forceinline__ void store_tile(const GemmArgs& a, int c_vec, long long tm0, long long tn0,
+                                           int wm, int wn, int tm, int tn,
+                                           const uint64_t (&acc)[8][TN / 2]) {
+  constexpr int WN = SimtCfg<TN>::WN;
+  constexpr int ROWS = TN == 16 ? 4 : 2;   // rows of quads loaded per batch (registers allowing)
+  const bool beta_nz = a.beta != 0.f;
+  const float* C = static_cast<const float*>(a.C);
+#pragma unroll
+  for (int i0 = 0; i0 < 8; i0 += ROWS) {
+    float4 old[ROWS][TN / 4];
+#pragma unroll
+    for (int ii = 0; ii < ROWS; ++ii) {
+      const long long m = tm0 + wm * 64 + (i0 + ii) * 8 + tm;
+#pragma unroll
+      for (int h = 0; h < TN / 4; ++h) {
+        const long long n = tn0 + wn * WN + h * 16 + tn * 4;
+        old[ii][h] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (beta_nz && m < a.M && c_vec && n + 3 < a.N)
+          old[ii][h] = *reinterpret_cast<const float4*>(C + m * a.ldc + n);
+      }
+    }
+#pragma unroll
+    for (int ii = 0; ii < ROWS; ++ii) {
+      const int i = i0 + ii;
+      const long long m = tm0 + wm * 64 + i * 8 + tm;
+      if (m >= a.M) continue;
+#pragma unroll
+      for (int h = 0; h < TN / 4; ++h) {
+        const long long n = tn0 + wn * WN + h * 16 + tn * 4;
+        const float2 lo = unpack2(acc[i][2 * h]), hi = unpack2(acc[i][2 * h + 1]);
+        float v[4] = {a.alpha * lo.x, a.alpha * lo.y, a.alpha * hi.x, a.alpha * hi.y};
+        if (c_vec && n + 3 < a.N) {
+          if (beta_nz) {
+            v[0] = fmaf(a.beta, old[ii][h].x, v[0]);
+            v[1] = fmaf(a.beta, old[ii][h].y, v[1]);
+            v[2] = fmaf(a.beta, old[ii][h].z, v[2]);
+            v[3] = fmaf(a.beta, old[ii][h].w, v[3]);
+          }
+          if (EPI) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = finish(a, v[j], n + j);
+          }
+          *reinterpret_cast<float4*>(static_cast<float*>(a.C) + m * a.ldc + n) =
+              make_float4(v[0], v[1], v[2], v[3]);
+        } else {
+          store_quad<EPI>(a, c_vec, m, n, v);   // ragged or unaligned: element by element
+        }
+      }
+    }
+  }
+}
+
 // Stream-K: the end of this CTA's share of one tile (the K-slice u is one
 // of its slices of that tile).  Every warp handles its own 64 x 4*TN block of
 // the tile, so no barrier of the whole CTA is needed.  Returns false after a
@@ -205,20 +251,8 @@ __device__ __forceinline__ bool sk_segment_end(const SimtParams& p, long long u,
   const long long U = p.sk_units;
   const int G = p.sk_ctas;
   const long long T0 = u - u % k_slices, T1 = T0 + k_slices;   // this tile's K-slices
-  // the CTAs whose ranges meet [T0, T1): c with begin(c + 1) > T0 and begin(c) < T1
-  const int cfirst = (int)(((T0 + 1) * G + U - 1) / U) - 1;
-  const int clast = (int)((T1 * G + U - 1) / U) - 1;
-  // the finisher: the CTA whose share of the tile ends latest in its own
-  // range (the first such CTA on a tie), so its wait is the shortest
-  int fin = cfirst;
-  long long best = -1;
-  for (int c = cfirst; c <= clast; ++c) {
-    const long long b = sk_begin(c, U, G), e = min(sk_begin(c + 1, U, G), T1);
-    if (e - b > best) {
-      best = e - b;
-      fin = c;
-    }
-  }
+  int cfirst, clast, fin;
+  sk_tile_workers(T0, T1, U, G, &cfirst, &clast, &fin);
   auto slot_of = [&](int c) {
     return c * kSkMaxSeg + (int)(T0 / k_slices - sk_begin(c, U, G) / k_slices);
   };
@@ -296,18 +330,7 @@ __device__ __forceinline__ bool sk_segment_end(const SimtParams& p, long long u,
       for (int c = cfirst; c <= clast; ++c)
         if (c != me) p.sk_flags[slot_of(c) * 8 + warp] = 0u;   // ready for the next call
     }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const long long m = (long long)tm0 + wm * 64 + i * 8 + tm;
-      if (m >= a.M) continue;
-#pragma unroll
-      for (int h = 0; h < TN / 4; ++h) {
-        const long long n = (long long)tn0 + wn * WN + h * 16 + tn * 4;
-        const float2 lo = unpack2(acc[i][2 * h]), hi = unpack2(acc[i][2 * h + 1]);
-        float v[4] = {a.alpha * lo.x, a.alpha * lo.y, a.alpha * hi.x, a.alpha * hi.y};
-        store_quad<EPI>(a, p.c_vec, m, n, v);
-      }
-    }
+    store_tile<TN, EPI>(a, p.c_vec, tm0, tn0, wm, wn, tm, tn, acc);
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i)
@@ -565,21 +588,7 @@ __global__ void __launch_bounds__(THREADS, SimtCfg<TN>::CTAS_PER_SM)
   }
 
   if constexpr (SPLIT == 1) {
-    if (ok) {
-      // ---------------------------------------------------------- epilogue
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const long long m = (long long)m0 + wm * 64 + i * 8 + tm;
-        if (m >= a.M) continue;
-#pragma unroll
-        for (int h = 0; h < TN / 4; ++h) {
-          const long long n = (long long)n0 + wn * WN + h * 16 + tn * 4;
-          const float2 lo = unpack2(acc[i][2 * h]), hi = unpack2(acc[i][2 * h + 1]);
-          float v[4] = {a.alpha * lo.x, a.alpha * lo.y, a.alpha * hi.x, a.alpha * hi.y};
-          store_quad<EPI>(a, p.c_vec, m, n, v);
-        }
-      }
-    }
+    if (ok) store_tile<TN, EPI>(a, p.c_vec, m0, n0, wm, wn, tm, tn, acc);   // epilogue
   } else if constexpr (SPLIT > 1) {
     // ------------------------------------------- split epilogue (cluster)
     // Every copy this CTA issued has landed (all were consumed, or drained
@@ -693,12 +702,14 @@ cudaError_t narrow_clusters4(int num_sms, int* c4) {
   return cudaSuccess;
 }
 
-// The stream-K workspace of a device: kSkSlots slots, each with room for the
-// partial tiles and flags of a stream-K launch of up to one CTA per SM
-// (152 SMs: 39.8 MB of partials a slot), allocated and zeroed at the first
-// FP32 SIMT call on the device and kept until the process exits.  Calls take
-// the slots in turn, so up to kSkSlots stream-K calls may run on the GPU at
-// once (on different streams) without sharing one.
+// The stream-K workspace of a device, shared with the CTA-pair tensor-core
+// kernel: kSkSlots slots, each with room for the partial tiles and flags of
+// a stream-K launch of up to one CTA per SM (152 SMs: 39.8 MB of partials a
+// slot; the same room holds two 256 x 256 partial tiles per SM pair),
+// allocated and zeroed at the first call of either kernel on the device and
+// kept until the process exits.  Calls take the slots in turn, so up to
+// kSkSlots stream-K calls may run on the GPU at once (on different streams)
+// without sharing one.
 constexpr int kSkSlots = 4;
 struct SkWorkspace {
   std::atomic<bool> ready{false};   // published after the fields below are set
@@ -749,6 +760,28 @@ cudaError_t sk_workspace(int num_sms, SkWorkspace** out) {
   return cudaSuccess;
 }
 
+}  // namespace
+
+cudaError_t stream_k_setup(int num_sms) {
+  SkWorkspace* w = nullptr;
+  return sk_workspace(num_sms, &w);
+}
+
+cudaError_t stream_k_slot(int num_sms, float** partials, unsigned** flags, size_t* slot_floats,
+                          size_t* slot_flags) {
+  SkWorkspace* w = nullptr;
+  const cudaError_t e = sk_workspace(num_sms, &w);
+  if (e != cudaSuccess) return e;
+  const unsigned slot = w->next.fetch_add(1, std::memory_order_relaxed) % kSkSlots;
+  *partials = w->partials + slot * w->slot_floats;
+  *flags = w->flags + slot * w->slot_flags;
+  *slot_floats = w->slot_floats;
+  *slot_flags = w->slot_flags;
+  return cudaSuccess;
+}
+
+namespace {
+
 // CTAs of a stream-K launch for `rest` tiles of k_slices K-slices each: one
 // per SM at most, each with at least kSkMinSlices K-slices (two rounds of the
 // ring), so a CTA's range is at most one tile long when k_slices >= kSkMinSlices.
@@ -769,24 +802,18 @@ cudaError_t launch_stream_k(const CUtensorMap* mapA, const CUtensorMap* mapB, Si
   auto k = sgemm_tma_kernel<16, EPI, 0, false>;
   cudaError_t e = set_smem_once(smem_set, k, Cfg::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  SkWorkspace* w = nullptr;
-  if ((e = sk_workspace(num_sms, &w)) != cudaSuccess) return e;
   const int G = sk_ctas(rest, k_slices, num_sms);
-  if (G > w->max_ctas) return cudaErrorInvalidValue;
-  const unsigned slot = w->next.fetch_add(1, std::memory_order_relaxed) % kSkSlots;
+  float* partials = nullptr;
+  unsigned* flags = nullptr;
+  size_t slot_floats = 0, slot_flags = 0;
+  if ((e = stream_k_slot(num_sms, &partials, &flags, &slot_floats, &slot_flags)) != cudaSuccess) return e;
+  if ((size_t)G * kSkMaxSeg * BM * Cfg::BN > slot_floats || (size_t)G * kSkMaxSeg * COMPUTE_WARPS > slot_flags)
+    return cudaErrorInvalidValue;
   p.sk_units = rest * k_slices;
   p.sk_ctas = G;
-  p.sk_partials = w->partials + slot * w->slot_floats;
-  p.sk_flags = w->flags + slot * w->slot_flags;
-  // the same arithmetic as the kernel: CTAs meeting each tile's K-slices
-  const long long U = p.sk_units;
-  int share = 1;
-  for (long long t = 0; t < rest; ++t) {
-    const long long T0 = t * k_slices, T1 = T0 + k_slices;
-    const long long cfirst = ((T0 + 1) * G + U - 1) / U - 1, clast = (T1 * G + U - 1) / U - 1;
-    if (clast - cfirst + 1 > share) share = (int)(clast - cfirst + 1);
-  }
-  *max_share = share;
+  p.sk_partials = partials;
+  p.sk_flags = flags;
+  *max_share = sk_max_share(rest, k_slices, G);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -919,11 +946,6 @@ int plan_f32_simt(int M, int N, int K, int num_sms, int forced_tn, SimtPlan* out
 int launch_f32_simt(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
                     const SimtPlan& plan, int num_sms, cudaStream_t s, int* k_split) {
   *k_split = 1;
-  // the first call on a device sets up the stream-K workspace, whatever its
-  // shape, so that later calls (and stream captures) never allocate
-  SkWorkspace* w = nullptr;
-  const cudaError_t we = sk_workspace(num_sms, &w);
-  if (we != cudaSuccess) return we;
   SimtParams p;
   p.a = a;
   const int bn = plan.tn == 16 ? kSimtBN16 : kSimtBN8;
@@ -1068,15 +1090,7 @@ int launch_f32_simt_static(const GemmArgs& a, const CUtensorMap* mapA, const CUt
   p.sk_ctas = G;
   p.sk_partials = scratch;
   p.sk_flags = flags;
-  // the most CTAs that meet in one tile (the kernel's arithmetic)
-  const long long U = p.sk_units;
-  int share = 1;
-  for (long long t = 0; t < rest; ++t) {
-    const long long T0 = t * k_slices, T1 = T0 + k_slices;
-    const long long cfirst = ((T0 + 1) * G + U - 1) / U - 1, clast = (T1 * G + U - 1) / U - 1;
-    if (clast - cfirst + 1 > share) share = (int)(clast - cfirst + 1);
-  }
-  *k_split = share;
+  *k_split = sk_max_share(rest, k_slices, G);   // the most CTAs that meet in one tile
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

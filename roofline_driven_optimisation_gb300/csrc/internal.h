@@ -66,6 +66,7 @@ enum WaitSite : int {
   kSiteTc2Mma = 15,
   kSiteTc2Epilogue = 16,
   kSiteTc2Drain = 17,
+  kSiteTc2StreamK = 18,    // a stream-K finisher pair waiting for another pair's partial tile
   kSiteSimtConsumer = 21,
   kSiteSimtDrain = 22,
   kSiteSimtStreamK = 23,   // a stream-K finisher waiting for another CTA's partial tile
@@ -101,6 +102,14 @@ struct SimtPlan {
 // Lowers every stream-K flag of the current device's workspace (after a
 // device timeout, which may leave flags raised).
 void sk_clear_flags();
+// The per-device stream-K workspace shared by the FP32 SIMT and CTA-pair
+// kernels: stream_k_setup allocates and zeroes it at the first call on a
+// device (a device-wide wait); stream_k_slot hands out its four slots in
+// turn -- partial tiles (slot_floats floats, num_sms x 65536) and flags
+// (slot_flags words, num_sms x 16, zero between calls).
+cudaError_t stream_k_setup(int num_sms);
+cudaError_t stream_k_slot(int num_sms, float** partials, unsigned** flags, size_t* slot_floats,
+                          size_t* slot_flags);
 int plan_f32_simt(int M, int N, int K, int num_sms, int forced_tn, SimtPlan* out);
 int launch_f32_simt(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
                     const SimtPlan& plan, int num_sms, cudaStream_t s, int* k_split);
@@ -132,17 +141,21 @@ constexpr int kTcBM = 128, kTcBK = 64;
 // The same GEMM on CTA pairs (clusters of two, cta_group::2): C tiles of
 // 256 x bn, bn in {128, 256}; each CTA loads 128 rows of A and bn/2 columns
 // of B with the same tensor maps as the single-CTA kernel.
-// *schedule receives 2 (whole tiles) or 4 (the tiles of a partial last wave
-// run as two half-width tiles each).
+// *schedule receives 2 (whole tiles), 4 (the tiles of a partial last wave
+// run as two half-width tiles each) or 6 (they run stream-K over the pairs).
 bool split_tiles_enabled();
+// gemm_force_split_tiles: 0 forbid, 1 automatic, 2 pin the CTA-pair
+// kernel's stream-K tail, 3 pin its half-width tail (where each exists).
+int split_tiles_mode();
 int launch_bf16_tc_pair(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB, int bn,
                         int num_sms, cudaStream_t s, int* schedule);
 // SwiGLU on CTA pairs (a.swiglu): C tiles of 256 x 128; each CTA's B operand
 // is 64 columns of Bgate (mapB) and the same 64 columns of Bup (mapB2).
 // FP8 inputs (in == FP8) on CTA pairs, 256 x 256 C tiles: TMA tiles of A
 // (128 k x 128 m bytes) and B (128 n x 128 k bytes), 128-byte swizzle.
+// *schedule as for launch_bf16_tc_pair (2 or 6: no half-width tiles).
 int launch_fp8_tc_pair(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,
-                       int num_sms, cudaStream_t s);
+                       int num_sms, cudaStream_t s, int* schedule);
 constexpr int kF8BK = 128;
 
 int launch_bf16_swiglu_pair(const GemmArgs& a, const CUtensorMap* mapA, const CUtensorMap* mapB,

@@ -67,6 +67,42 @@ inline void tc_config(int M, int N, int num_sms, bool split_allowed, int* pair, 
   }
 }
 
+// CTA-pair kernel, 256-wide tiles, `rem` tiles past the last whole wave of
+// `pairs`: the pairs of a stream-K tail, min(pairs, K-steps / 8), so that
+// each pair streams at least 8 K-steps; 0 (no stream-K) when a tile has
+// fewer than 8 K-steps, since then a pair's range could span three tiles.
+constexpr int kTcSkMinSteps = 8;
+inline int tc_sk_pairs(long long rem, int k_tiles, int pairs) {
+  if (rem <= 0 || pairs <= 0 || k_tiles < kTcSkMinSteps) return 0;
+  const long long by_work = rem * k_tiles / kTcSkMinSteps;
+  const long long g = by_work < pairs ? by_work : pairs;
+  return g < rem ? 0 : (int)g;
+}
+
+// How those `rem` tiles run, in tile-times: whole tiles (0) cost one;
+// half-width tiles (1, when 2 rem <= pairs) cost kTcHalfTile; stream-K over
+// sk_pairs pairs (2) costs rem / sk_pairs of a tile plus kTcSkExchange for
+// writing, waiting for and adding the partial tiles.  Measured on GB300 the
+// exchange costs more than a whole tile: each finisher warp adds the other
+// pairs' parts to its accumulator chunk by chunk after its own piece, and
+// that fix-up (15-30 us) is on the critical path (bf16 4096^3: 78.5 us with
+// half-width tiles, 84.6 whole, 101.0 stream-K; 2048 x 4096 x 4096: 47.8
+// whole, 64.1 stream-K; 8192^3: 578 half, 595 stream-K), so the model
+// never picks it; gemm_force_split_tiles(2) still runs it.
+constexpr double kTcHalfTile = 0.58;
+constexpr double kTcSkExchange = 1.0;
+inline int tc_tail(long long rem, int pairs, bool half_ok, int sk_pairs) {
+  if (rem <= 0 || pairs <= 0) return 0;
+  int best = 0;
+  double t = 1.0;
+  if (half_ok && kTcHalfTile < t) {
+    best = 1;
+    t = kTcHalfTile;
+  }
+  if (sk_pairs > 0 && (double)rem / sk_pairs + kTcSkExchange < t) best = 2;
+  return best;
+}
+
 // Time of `units` CTAs, each `unit` of a whole tile, with `slots` resident at
 // once, in tiles run two to an SM; a round of at most one CTA per SM runs
 // about 1.9x as fast (FP32 SIMT kernel on GB300, 4096^3 slices: 304 tiles two

@@ -22,6 +22,12 @@ struct TcParams {
   // tiles run as half_tiles items of half the width, one per pair
   int dp_tiles;
   int half_tiles;
+  // or (stream-K instance) the K-steps of tiles [dp_tiles, num_tiles) run
+  // end to end over sk_pairs pairs, partial tiles meeting in a workspace slot
+  int sk_pairs = 0;
+  long long sk_units = 0;
+  float* sk_partials = nullptr;   // [pair][2 pieces][256 rows][BN] fp32
+  unsigned* sk_flags = nullptr;   // [pair][2 pieces][2 CTAs x 4 epilogue warps]
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

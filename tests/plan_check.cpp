@@ -6,6 +6,8 @@
 //   simt tiles k_tiles sms max_clusters split min_k_tiles split_allowed -> 0 or 1
 //   cluster tiles_n k_units sms forced max_split -> split
 //   simtopt tn tiles k_tiles sms clusters2 clusters4 min_k_tiles split_allowed -> "time split"
+//   tcsk rem k_tiles pairs                       -> stream-K pairs
+//   tctail rem pairs half_ok sk_pairs            -> 0 whole, 1 half-width, 2 stream-K
 #include <cstdio>
 #include <cstring>
 
@@ -40,6 +42,16 @@ int main() {
       const g3::plan::SimtOption o =
           g3::plan::simt_option(tn, tiles, k_tiles, sms, c2, c4, min_k, allowed != 0);
       std::printf("%.4f %d\n", o.time, o.split);
+    } else if (!std::strcmp(op, "tcsk")) {
+      long long rem;
+      int k_tiles, pairs;
+      if (std::scanf("%lld %d %d", &rem, &k_tiles, &pairs) != 3) return 2;
+      std::printf("%d\n", g3::plan::tc_sk_pairs(rem, k_tiles, pairs));
+    } else if (!std::strcmp(op, "tctail")) {
+      long long rem;
+      int pairs, half_ok, sk;
+      if (std::scanf("%lld %d %d %d", &rem, &pairs, &half_ok, &sk) != 4) return 2;
+      std::printf("%d\n", g3::plan::tc_tail(rem, pairs, half_ok != 0, sk));
     } else if (!std::strcmp(op, "cluster")) {
       int tiles_n, k_units, sms, forced, max_split;
       if (std::scanf("%d %d %d %d %d", &tiles_n, &k_units, &sms, &forced, &max_split) != 5) return 2;

@@ -56,11 +56,33 @@ def test_tc2_pair_abort_then_recovers(short_limit):
     c = inputs.make("bf16_4096", M=512, N=512, K=256)
     g.force_tc_pair(2)
     status, where, (path, _, pair) = stalled_call(c.A, c.B, None, 1.0, 0.0, BF16)
-    assert path == g.PATH_BF16_TC and pair in (2, 4)
+    assert path == g.PATH_BF16_TC and pair in (2, 4, 6)
     assert (status, where) == (g.GEMM_ERR_DEVICE_TIMEOUT, SITE_TC2_MMA)
     assert g.device_status()[0] == 0          # taken once
     err, path = check(c.A, c.B, None, 1.0, 0.0, BF16)
-    assert path == g.PATH_BF16_TC and g.last_tc_pair() in (2, 4)
+    assert path == g.PATH_BF16_TC and g.last_tc_pair() in (2, 4, 6)
+
+
+def test_tc2_stream_k_abort_then_recovers(short_limit):
+    # every tile in the stream-K tail (6 tiles, 64 K-steps, 48 pairs): the
+    # first pair's MMA issuer stalls, so it never hands over its partial
+    # tiles; the finishers waiting for them give up and the flags the other
+    # pairs raised are lowered when the status is read.  Five later calls
+    # (every workspace slot) match the oracle.
+    c = inputs.make("bf16_4096", M=300, N=520, K=4096)
+    g.force_tc_pair(2)
+    g.force_tile_n(256)
+    g.force_split_tiles(2)
+    try:
+        status, where, (path, _, pair) = stalled_call(c.A, c.B, None, 1.0, 0.0, BF16)
+        assert path == g.PATH_BF16_TC and pair == 6
+        assert (status, where) == (g.GEMM_ERR_DEVICE_TIMEOUT, SITE_TC2_MMA)
+        assert g.device_status()[0] == 0
+        for _ in range(5):
+            check(c.A, c.B, None, 1.0, 0.0, BF16)
+            assert g.last_tc_pair() == 6
+    finally:
+        g.force_split_tiles(1)
 
 
 def test_skinny_split_abort_then_recovers(short_limit):

@@ -82,6 +82,20 @@ def test_bf16_pair_half_width_schedule(cuda_lib, act):
     assert g.last_tc_pair() == 4
 
 
+@pytest.mark.parametrize("act", [g.ACT_RELU, g.ACT_GELU])
+@pytest.mark.parametrize("out", [BF16, F32])
+def test_bf16_pair_stream_k_schedule(cuda_lib, act, out):
+    # the finisher of a stream-K tile applies beta, bias and the activation
+    # once, after the partial tiles are added
+    c = inputs.make("decode_m16_o", M=1536, N=1280, K=1024)
+    g.force_split_tiles(2)
+    try:
+        _run(c, out, 1.5, 0.5, True, act, pair=2, bn=256)
+        assert g.last_tc_pair() == 6
+    finally:
+        g.force_split_tiles(1)
+
+
 @pytest.mark.parametrize("act", ACTS)
 @pytest.mark.parametrize("m,N", [(4, 512), (16, 520), (1, 20480), (16, 20480)])
 def test_skinny(cuda_lib, act, m, N):

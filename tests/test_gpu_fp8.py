@@ -77,7 +77,26 @@ def test_tiles_and_tails(cuda_lib, M, N, K):
     c = inputs.make_fp8(M, N, K, E4, E4, seed=M, beta=0.5)
     for out in (BF16, F32):
         _, ran = _check(c, out)
-        assert ran == g.PATH_BF16_TC and g.last_tc_pair() == 2
+        assert ran == g.PATH_BF16_TC and g.last_tc_pair() in (2, 6)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 4096, 2048), (2048, 4096, 1024), (1000, 1008, 1040),
+                                   (4096, 4096, 1152)])
+def test_fp8_stream_k_tail(cuda_lib, M, N, K):
+    # the FP8 pair kernel's tail runs stream-K (it has no half-width tiles):
+    # (256, 4096): 16 tiles, all in the tail; (2048, 4096): 52 of 128;
+    # (1000, 1008): 9 K-steps of 128 a tile; (4096, 4096): 28 of 256
+    c = inputs.make_fp8(M, N, K, E4, E5, seed=K, beta=0.5)
+    g.force_split_tiles(2)
+    try:
+        for out in (BF16, F32):
+            _, ran = _check(c, out)
+            assert ran == g.PATH_BF16_TC and g.last_tc_pair() == 6, g.last_tc_pair()
+        a = _run(c, F32)[0]
+        b = _run(c, F32)[0]
+        assert torch.equal(a, b)
+    finally:
+        g.force_split_tiles(1)
 
 
 def test_fp8_4096_sampled(cuda_lib):

@@ -318,7 +318,7 @@ def test_bf16_tc_pair(cuda_lib, bn, M, N, K):
     try:
         for out, alpha, beta in ((BF16, 1.0, 0.0), (F32, 1.5, 0.5)):
             err, path = check(c.A, c.B, c.C0, alpha, beta, out)
-            assert path == g.PATH_BF16_TC and g.last_tc_pair() in (2, 4) and g.last_tile_n() == bn
+            assert path == g.PATH_BF16_TC and g.last_tc_pair() in (2, 4, 6) and g.last_tile_n() == bn
     finally:
         g.force_tc_pair(0)
         g.force_tile_n(0)
@@ -351,6 +351,7 @@ def test_bf16_tc_half_width_last_wave(cuda_lib, M, N, K):
     c = inputs.make("decode_m16_o", M=M, N=N, K=K)
     g.force_tc_pair(2)
     g.force_tile_n(256)
+    g.force_split_tiles(3)   # pin the half-width tail
     try:
         for out, alpha, beta in ((BF16, 1.0, 0.0), (F32, 1.5, 0.5)):
             err, path = check(c.A, c.B, c.C0, alpha, beta, out)
@@ -361,6 +362,40 @@ def test_bf16_tc_half_width_last_wave(cuda_lib, M, N, K):
         assert g.last_tc_pair() == 2
         # the same products in the same order: identical bits
         assert torch.equal(a1, b)
+    finally:
+        g.force_split_tiles(1)
+        g.force_tc_pair(0)
+        g.force_tile_n(0)
+
+
+@pytest.mark.parametrize("M,N,K", [(2560, 2560, 1024), (1536, 1280, 1024), (1300, 1000, 520),
+                                   (2048, 4096, 768), (300, 520, 4096), (1000, 1008, 1000)])
+def test_bf16_tc_stream_k_tail(cuda_lib, M, N, K):
+    # the tiles past the last whole wave of pairs run stream-K: their K-steps
+    # spread evenly over the pairs, partial tiles added by each tile's
+    # finisher in pair order.  (2560, 2560): 100 tiles, 24 in the tail;
+    # (1536, 1280), (300, 520), (1000, 1008): fewer tiles than pairs, all in
+    # the tail; (1300, 1000): 9 K-steps a tile; (2048, 4096): 52 tail tiles
+    # of 12 K-steps over every pair, up to three pairs meeting in a tile
+    c = inputs.make("decode_m16_o", M=M, N=N, K=K)
+    g.force_tc_pair(2)
+    g.force_tile_n(256)
+    g.force_split_tiles(2)   # pin the stream-K tail
+    try:
+        for out, alpha, beta in ((BF16, 1.0, 0.0), (F32, 1.5, 0.5)):
+            err, path = check(c.A, c.B, c.C0, alpha, beta, out)
+            assert path == g.PATH_BF16_TC and g.last_tc_pair() == 6, g.last_tc_pair()
+        # the addition order depends on the shape alone: identical bits on
+        # every call (five calls: every workspace slot is used)
+        first = run_abi(c.A, c.B, c.C0, 1.5, 0.5, F32)[0]
+        for _ in range(4):
+            assert torch.equal(run_abi(c.A, c.B, c.C0, 1.5, 0.5, F32)[0], first)
+        g.force_split_tiles(0)
+        whole = run_abi(c.A, c.B, c.C0, 1.5, 0.5, F32)[0]
+        assert g.last_tc_pair() == 2
+        # another fp32 summation order of the same products: the same bound
+        den = oracle.normwise_denominator(c.A, c.B, 1.5, 0.5, c.C0.to(F32))
+        assert oracle.normwise_error(first, oracle.to_f64(whole), den) <= oracle.TOL_BF16_F32OUT
     finally:
         g.force_split_tiles(1)
         g.force_tc_pair(0)
@@ -391,7 +426,7 @@ def test_bf16_tc_pair_8192_sampled(cuda_lib, out):
     try:
         g.gemm(A, B, C, 1.0, 0.0)
         torch.cuda.synchronize()
-        assert g.last_tc_pair() in (2, 4)
+        assert g.last_tc_pair() in (2, 4, 6)
     finally:
         g.force_tc_pair(0)
     gen = np.random.default_rng(7)

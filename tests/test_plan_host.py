@@ -56,6 +56,29 @@ def test_tensor_core_config_counts_the_halved_last_wave(plan):
         assert tc(plan, M, N, allowed=0) == without, (M, N)
 
 
+def test_pair_stream_k_pairs(plan):
+    # every pair streams at least 8 K-steps, and no range may span three
+    # tiles (at least as many pairs as tail tiles)
+    ask = lambda rem, k: int(plan(("tcsk", rem, k, 76))[0])
+    assert ask(28, 64) == 76       # bf16 4096^3: 28 tail tiles, 64 K-steps each
+    assert ask(6, 64) == 48        # 6 tiles x 64 / 8
+    assert ask(16, 9) == 18
+    assert ask(16, 4) == 0         # fewer than 8 K-steps a tile
+    assert ask(100, 8) == 0        # 100 tiles, at most 76 pairs: a range would span 3 tiles
+    assert ask(0, 64) == 0
+
+
+def test_pair_tail_choice(plan):
+    # measured on GB300: half-width tiles beat whole tiles, and stream-K (its
+    # fix-up on the critical path) loses to both, so it is never chosen
+    ask = lambda rem, half, sk: int(plan(("tctail", rem, 76, half, sk))[0])
+    assert ask(28, 1, 76) == 1     # bf16 4096^3: half-width
+    assert ask(52, 0, 76) == 0     # o-proj 2048 x 4096: halves do not fit
+    assert ask(28, 0, 76) == 0     # FP8 (no half-width tiles)
+    assert ask(12, 1, 76) == 1     # lm head 2048 x 32000
+    assert ask(0, 1, 76) == 0
+
+
 def test_single_cta_tile_width(plan):
     # single-CTA tiles timed on GB300 at K = 4096 (256 / 192 / 128 wide):
     # 512 x 11008: 62.3 / 51.2 / 52.4 us; 1024 x 4096: 33.0 / 45.2 / 34.8 us;
