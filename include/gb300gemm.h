@@ -325,6 +325,11 @@ const char* gemm_get_last_error(void);
  * kernel-specific location code of the first failure (0 if none).  The
  * `where` argument is this library's addition to the surveyed
  * gemm_device_status(stream); NULL is accepted.
+ * When it returns GEMM_ERR_DEVICE_TIMEOUT it also lowers every flag of the
+ * device's stream-K workspace (a call that gave up may have left flags
+ * raised), with a device-wide memset: take a timeout status while no other
+ * stream-K call (see gemm_force_split_tiles) is executing on the device, or
+ * that call may report a timeout of its own.
  */
 int gemm_device_status(cudaStream_t stream, int* where);
 
