@@ -92,7 +92,8 @@ int gemm_f32(int M, int N, int K, float alpha, const float* A, int lda, const fl
  * under a fixed memory budget) cannot let a library allocate later -- the
  * allocation may fail, or break the pool's accounting; and a caller on a
  * latency-critical thread cannot take the device-wide wait that the first
- * gemm_f32 call on a device makes while it sets up its workspace.
+ * GEMM call of the other entry points makes on a device while it sets up
+ * the stream-K workspace.
  *
  * Same arguments, result and error codes as gemm_f32, the same plan and
  * the same kernels (so the same bits for the same inputs).  The one
