@@ -72,6 +72,25 @@ def test_several_query_blocks_and_key_tiles(cuda_lib, D, Sq, Sk, causal):
     assert ran == g.PATH_ATTN
 
 
+@pytest.mark.parametrize("D", [128, 64])
+def test_causal_tiles_outnumber_resident_ctas(cuda_lib, D):
+    # 8 query tiles x 80 heads = 640 CTAs, more than fit on the GPU at once:
+    # the longest-first causal dispatch runs in waves of tiles of different
+    # lengths, with grouped key/value heads; every output row checked
+    c = inputs.make_attention(B=2, Hq=40, Hkv=8, Sq=1000, Sk=1000, D=D, seed=41 + D)
+    _, ran = _check(c, True)
+    assert ran == g.PATH_ATTN
+
+
+def test_causal_tiles_without_keys_among_many_ctas(cuda_lib):
+    # Sq > Sk: the first three query tiles of every head see no key, so their
+    # CTAs load nothing and issue no MMA but still write zero rows, among
+    # 640 CTAs that do (10 query tiles x 64 heads)
+    c = inputs.make_attention(B=1, Hq=64, Hkv=8, Sq=1200, Sk=700, D=128, seed=43)
+    _, ran = _check(c, True)
+    assert ran == g.PATH_ATTN
+
+
 def test_grouped_kv_heads_and_scale(cuda_lib):
     c = inputs.make_attention(B=2, Hq=8, Hkv=2, Sq=192, Sk=320, D=128, seed=3)
     _check(c, True)
