@@ -148,6 +148,22 @@ def random_matrix(rows: int, cols: int, seed: int, dtype: str = "f32",
     return round_to(x, dtype)
 
 
+def device_uniform(rows: int, cols: int, seed: int, device, dtype: str = "bf16",
+                   block_rows: int = 4096) -> torch.Tensor:
+    """A seeded U[-1, 1) matrix drawn on `device` itself, a block of rows at a
+    time, for operands too large to draw on the host and copy over; the same
+    seed on the same kind of device gives the same values."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    tdt = {"bf16": torch.bfloat16, "f32": torch.float32}[dtype]
+    out = torch.empty((rows, cols), dtype=tdt, device=device)
+    for r0 in range(0, rows, block_rows):
+        r1 = min(rows, r0 + block_rows)
+        x = torch.rand((r1 - r0, cols), generator=gen, device=device, dtype=torch.float32)
+        out[r0:r1] = (x * 2.0 - 1.0).to(tdt)
+    return out
+
+
 @dataclasses.dataclass
 class SwigluCase:
     A: torch.Tensor        # M x K activations, bf16, CPU
