@@ -90,3 +90,24 @@ def test_decode_weight_past_2_31_elements(cuda_lib):
     C_cols = C[:, cols].cpu()
     del B, C
     _check(A, None, B_cols, None, C_cols, list(range(M)), cols, 1.0, oracle.TOL_BF16_OUT)
+
+
+def test_fp8_pairs_c_past_2_31_elements(cuda_lib):
+    # 65536 x 40000 bf16 C from E4M3 codes (K = 128: one stage)
+    from oracle import fp8
+    M, N, K = 65536, 40000, 128
+    c = inputs.make_fp8(M, N, K, inputs.FP8_E4M3, inputs.FP8_E4M3, seed=67)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    g.gemm_fp8_tensors(c.A.cuda(), c.fmt_a, c.B.cuda(), c.fmt_b, C, c.alpha)
+    assert g.last_path() == g.PATH_BF16_TC
+    _status_ok()
+    rows = _samples(M, [53687, 53688], 6)
+    cols = _samples(N, [], 7)
+    C_rows, C_cols = C[rows].cpu(), C[:, cols].cpu()
+    del C
+    worst = 0.0
+    for A_s, B_s, got in ((c.A[rows], c.B, C_rows), (c.A, c.B[:, cols], C_cols)):
+        ref = fp8.gemm_fp8(A_s, c.fmt_a, B_s, c.fmt_b, c.alpha)
+        den = fp8.normwise_denominator_fp8(A_s, c.fmt_a, B_s, c.fmt_b, c.alpha)
+        worst = max(worst, oracle.normwise_error(got, ref, den))
+    assert worst <= oracle.TOL_BF16_OUT, worst
