@@ -202,6 +202,14 @@ __global__ void __launch_bounds__(THREADS, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if (warp == 0 && lane == 0 && my_kt > 0) {
+    // While the previous kernel on the stream finishes, pull this CTA's
+    // first stages of codes into L2 (a prefetch only: the copies after the
+    // wait read whatever memory holds then, through L2).
+    const uint8_t* tiles = p.qk + ((size_t)blockIdx.y * p.k_tiles + kt_begin) * CODE_CHUNK_BYTES;
+    const int pre = my_kt < CPS * SSTAGES ? my_kt : CPS * SSTAGES;
+    bulk_prefetch_l2(tiles, (uint32_t)pre * CODE_CHUNK_BYTES);
+  }
   griddep_wait();  // inputs may come from the previous kernel on the stream
 
   float acc[MN];
